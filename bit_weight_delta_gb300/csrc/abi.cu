@@ -1,0 +1,346 @@
+// abi.cu — the C ABI of include/bitdelta.h: host-side argument checks, the
+// per-device error word, TMA descriptor encoding and kernel dispatch.
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "bitdelta.h"
+#include "kernels.h"
+
+namespace {
+
+// Sticky device error word; kernels receive its device address.
+__device__ uint32_t g_error_word;
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDecodeMaxRows = 16;
+
+struct DeviceState {
+  bool ready = false;
+  uint32_t* err = nullptr;
+  int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bd_status current_device(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return BD_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BD_ERR_CUDA;
+    if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) return BD_ERR_CUDA;
+    s.err = static_cast<uint32_t*>(p);
+    s.num_sms = sms;
+    s.ready = true;
+  }
+  *out = &s;
+  return BD_OK;
+}
+
+bd::DevCtx make_ctx(const DeviceState* s) {
+  bd::DevCtx c;
+  c.err = s->err;
+  c.wait_limit_ns = g_wait_limit_ns.load();
+  return c;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bd_status check_dims(int64_t d_out, int64_t d_in) {
+  if (d_out < 1 || d_in < 1) return BD_ERR_INVALID_ARG;
+  if (d_in % 8 != 0) return BD_ERR_UNSUPPORTED_SHAPE;
+  if (d_out > (int64_t{1} << 40) || d_in > (int64_t{1} << 40) ||
+      d_out > (int64_t{1} << 62) / d_in)
+    return BD_ERR_UNSUPPORTED_SHAPE;
+  return BD_OK;
+}
+
+bool mode_ok(bd_alpha_mode m) { return m == BD_ALPHA_PER_MATRIX || m == BD_ALPHA_PER_ROW; }
+
+bd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
+
+// ------------------------------------------------------------------ TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 [rows, cols] as a 2D tensor with a (box_cols x box_rows)
+// box in the 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                    uint32_t box_cols, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Can the tensor-core kernel take this problem?
+bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
+  return d_in % 128 == 0 && d_in < INT32_MAX && d_out < INT32_MAX && rows_x < INT32_MAX;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bitdelta_packed_bytes(int64_t d_out, int64_t d_in) {
+  if (check_dims(d_out, d_in) != BD_OK) return 0;
+  return static_cast<size_t>(d_out) * static_cast<size_t>(d_in / 8);
+}
+
+size_t bitdelta_compress_workspace_bytes(int64_t d_out, int64_t d_in, bd_alpha_mode mode) {
+  if (check_dims(d_out, d_in) != BD_OK || !mode_ok(mode)) return 0;
+  return mode == BD_ALPHA_PER_ROW ? 0 : static_cast<size_t>(d_out) * 8 + 256;
+}
+
+bd_status bitdelta_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
+                            int64_t d_in, bd_alpha_mode mode, uint8_t* packed_out,
+                            float* alpha_out, void* workspace, size_t workspace_bytes,
+                            bd_stream_t stream) {
+  if (!w_base || !w_ft || !packed_out || !alpha_out || !mode_ok(mode)) return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (!aligned(w_base, 16) || !aligned(w_ft, 16) || !aligned(alpha_out, 4))
+    return BD_ERR_MISALIGNED;
+  const size_t need = bitdelta_compress_workspace_bytes(d_out, d_in, mode);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return BD_ERR_WORKSPACE;
+  if (need > 0 && !aligned(workspace, 16)) return BD_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* counter = nullptr;
+  double* row_sums = nullptr;
+  if (mode == BD_ALPHA_PER_MATRIX) {
+    counter = static_cast<unsigned int*>(workspace);
+    row_sums = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + 256);
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess) return BD_ERR_CUDA;
+  }
+  return from_cuda(bd::launch_compress(w_base, w_ft, d_out, d_in, mode == BD_ALPHA_PER_ROW,
+                                       packed_out, alpha_out, row_sums, counter, dev->num_sms, s,
+                                       make_ctx(dev)));
+}
+
+bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, const float* alpha,
+                               bd_alpha_mode mode, int64_t d_out, int64_t d_in, uint16_t* w_out,
+                               bd_stream_t stream) {
+  if (!w_base || !packed || !alpha || !w_out || !mode_ok(mode)) return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (!aligned(w_base, 16) || !aligned(w_out, 16) || !aligned(alpha, 4)) return BD_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  return from_cuda(bd::launch_reconstruct(w_base, packed, alpha, mode == BD_ALPHA_PER_ROW, d_out,
+                                          d_in, w_out, dev->num_sms,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
+                          const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
+                          int64_t d_out, int64_t d_in, uint16_t* y, bd_stream_t stream) {
+  if (M < 0 || !mode_ok(mode)) return BD_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !w_base || !packed || !alpha || !y)) return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (M == 0) return BD_OK;
+  if (M > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(w_base, 16) || !aligned(y, 16) || !aligned(alpha, 4))
+    return BD_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bd::DevCtx ctx = make_ctx(dev);
+
+  if (M > kDecodeMaxRows && tc_shape_ok(M, d_out, d_in) && aligned(packed, 16)) {
+    CUtensorMap tw, tx;
+    if (make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
+        make_tmap_bf16(&tx, x, M, d_in, 64, bd::gemm_block_tokens())) {
+      bd::GemmArgs g{};
+      g.M = M;
+      g.d_out = d_out;
+      g.d_in = d_in;
+      g.packed = packed;
+      g.alpha = alpha;
+      g.per_row = mode == BD_ALPHA_PER_ROW;
+      g.y = y;
+      g.ctx = ctx;
+      const int64_t tiles = ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
+                            ((M + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens());
+      const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+      return from_cuda(bd::launch_gemm(g, tw, tx, grid, s));
+    }
+  }
+  bd::GemvArgs a{};
+  a.x = x;
+  a.M = M;
+  a.w = w_base;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.packed = packed;
+  a.alpha = alpha;
+  a.per_row = mode == BD_ALPHA_PER_ROW;
+  a.y = y;
+  a.ctx = ctx;
+  return from_cuda(bd::launch_gemv(a, s));
+}
+
+bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int32_t* seg_offsets,
+                                  const int32_t* seg_variant, int32_t n_seg, int32_t max_seg_len,
+                                  const uint16_t* w_base, const uint8_t* const* packed_table,
+                                  const float* const* alpha_table, int32_t n_var,
+                                  bd_alpha_mode mode, int64_t d_out, int64_t d_in, uint16_t* y,
+                                  bd_stream_t stream) {
+  if (M_total < 0 || n_seg < 0 || n_var < 0 || max_seg_len < 0 || !mode_ok(mode))
+    return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (M_total == 0 || n_seg == 0) return BD_OK;
+  if (!x || !seg_offsets || !seg_variant || !w_base || !y) return BD_ERR_INVALID_ARG;
+  if (n_var > 0 && (!packed_table || !alpha_table)) return BD_ERR_INVALID_ARG;
+  if (M_total > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(w_base, 16) || !aligned(y, 16) || !aligned(seg_offsets, 4) ||
+      !aligned(seg_variant, 4) || !aligned(packed_table, 8) || !aligned(alpha_table, 8))
+    return BD_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bd::DevCtx ctx = make_ctx(dev);
+
+  // Long segments on the tensor cores when the shape allows it; the decode
+  // kernel takes every segment the tensor-core kernel does not.
+  bool use_tc = max_seg_len > kDecodeMaxRows && tc_shape_ok(M_total, d_out, d_in) &&
+                n_seg <= bd::kGemmMaxSegs;
+  CUtensorMap tw, tx;
+  if (use_tc)
+    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
+             make_tmap_bf16(&tx, x, M_total, d_in, 64, bd::gemm_block_tokens());
+  const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
+
+  if (use_tc) {
+    bd::GemmArgs g{};
+    g.M = M_total;
+    g.d_out = d_out;
+    g.d_in = d_in;
+    g.per_row = mode == BD_ALPHA_PER_ROW;
+    g.y = y;
+    g.seg_off = seg_offsets;
+    g.seg_var = seg_variant;
+    g.n_seg = n_seg;
+    g.n_var = n_var;
+    g.max_short = short_limit;
+    g.packed_table = packed_table;
+    g.alpha_table = alpha_table;
+    g.ctx = ctx;
+    const int64_t tiles = ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
+                          ((M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() +
+                           n_seg);
+    const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+    if ((st = from_cuda(bd::launch_gemm(g, tw, tx, grid, s))) != BD_OK) return st;
+  }
+
+  const int64_t short_rows_bound =
+      use_tc ? (M_total < int64_t{n_seg} * kDecodeMaxRows ? M_total
+                                                           : int64_t{n_seg} * kDecodeMaxRows)
+             : M_total;
+  if (bd::gemv_grouped_smem_bytes(n_var, short_rows_bound) > 200 * 1024)
+    return BD_ERR_UNSUPPORTED_SHAPE;
+  bd::GemvArgs a{};
+  a.x = x;
+  a.M = M_total;
+  a.w = w_base;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.per_row = mode == BD_ALPHA_PER_ROW;
+  a.y = y;
+  a.seg_off = seg_offsets;
+  a.seg_var = seg_variant;
+  a.n_seg = n_seg;
+  a.n_var = n_var;
+  a.max_short = short_limit;
+  a.packed_table = packed_table;
+  a.alpha_table = alpha_table;
+  a.ctx = ctx;
+  return from_cuda(bd::launch_gemv_grouped(a, short_rows_bound, s));
+}
+
+bd_status bitdelta_check_error(bd_stream_t stream) {
+  DeviceState* dev = nullptr;
+  bd_status st = current_device(&dev);
+  if (st != BD_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BD_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BD_ERR_CUDA;
+  if (word != 0 && cudaMemset(dev->err, 0, sizeof(word)) != cudaSuccess) return BD_ERR_CUDA;
+  if (word & bd::kErrTimeout) return BD_ERR_DEVICE_TIMEOUT;
+  if (word & bd::kErrBounds) return BD_ERR_DEVICE_BOUNDS;
+  return BD_OK;
+}
+
+bd_status bitdelta_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns < 1000 ? 1000 : ns);
+  return BD_OK;
+}
+
+bd_status bitdelta_debug_wait_timeout(bd_stream_t stream) {
+  DeviceState* dev = nullptr;
+  bd_status st = current_device(&dev);
+  if (st != BD_OK) return st;
+  return from_cuda(
+      bd::launch_wait_timeout_probe(make_ctx(dev), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* bitdelta_status_string(bd_status status) {
+  switch (status) {
+    case BD_OK:
+      return "ok";
+    case BD_ERR_INVALID_ARG:
+      return "invalid argument";
+    case BD_ERR_UNSUPPORTED_SHAPE:
+      return "unsupported shape";
+    case BD_ERR_MISALIGNED:
+      return "misaligned pointer";
+    case BD_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case BD_ERR_CUDA:
+      return "CUDA runtime error";
+    case BD_ERR_DEVICE_TIMEOUT:
+      return "a bounded device wait ran out of time";
+    case BD_ERR_DEVICE_BOUNDS:
+      return "malformed segment table, variant id or table entry seen on the device";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

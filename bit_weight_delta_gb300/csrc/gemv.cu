@@ -1,0 +1,345 @@
+// gemv.cu — fused BitDelta linear for few rows (decode), bandwidth-bound.
+//
+// Page "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "Serving architecture": one fused kernel reads the base weight and the delta
+// bits together and never materialises W_eff in HBM; the conceptual
+// fused_bitdelta_linear computes F.linear(x, W_base + α·unpack(bits)).
+//
+// Arithmetic (exact rewriting of x·W_effᵀ with W_eff = W_base + α·S, S = ±1):
+//     y[m][n] = Σ_k x[m][k]·W_base[n][k]  +  α_n · Σ_k x[m][k]·S[n][k]
+// Both sums run on the tensor cores with warp-level mma.sync m16n8k16 (bf16
+// in, fp32 accumulate): the raw W_base words are the B fragments as loaded,
+// and S is turned into ±1 bf16 pairs with three integer ops per two weights.
+// The only difference from the canonical bf16-rounded W_eff is that W_eff is
+// not rounded to bf16 before the product (a half-ulp change per weight).
+//
+// Work layout: a CTA owns 8·NG output rows (n) and one group of up to 16 x
+// rows (m); its KW warps split d_in and reduce through shared memory in a
+// fixed order.  Each thread loads, per 32-column chunk, one 16-byte word of a
+// W_base row (8 adjacent columns; the 4 threads of a quad cover 64 contiguous
+// bytes) and the matching 8 columns of two x rows.  The columns inside a
+// fragment are permuted consistently for A and B, which a dot product allows.
+// Sign bits arrive as one 16-byte load per row per 128 columns.  Per weight
+// the kernel moves 2 + 1/8 bytes from HBM; x stays in L1/L2.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bd {
+namespace {
+
+constexpr int kKW = 4;  // warps splitting d_in in a CTA
+constexpr int kMaxGroupRows = 16;
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16x2 of ±1 for sign bits (2i, 2i+1) of `byte`: bit 1 -> +1.0 (0x3F80),
+// bit 0 -> −1.0 (0xBF80); column 2i in the low half.
+__device__ __forceinline__ uint32_t pm_one_pair(uint32_t byte, int i) {
+  return (((byte >> (2 * i)) * 0x40008000u) & 0x80008000u) ^ 0xBF80BF80u;
+}
+
+// One 32-column chunk for NG groups of 8 W rows: base and sign products.
+template <int NG>
+__device__ __forceinline__ void chunk_mma(float (&acc_b)[NG][4], float (&acc_s)[NG][4],
+                                          const uint4 (&wv)[NG], const uint32_t (&sb)[NG],
+                                          uint4 xa, uint4 xb, bool has_delta) {
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    mma_16816(acc_b[ng], xa.x, xb.x, xa.y, xb.y, wv[ng].x, wv[ng].y);
+    mma_16816(acc_b[ng], xa.z, xb.z, xa.w, xb.w, wv[ng].z, wv[ng].w);
+    if (has_delta) {
+      const uint32_t b = sb[ng];
+      mma_16816(acc_s[ng], xa.x, xb.x, xa.y, xb.y, pm_one_pair(b, 0), pm_one_pair(b, 1));
+      mma_16816(acc_s[ng], xa.z, xb.z, xa.w, xb.w, pm_one_pair(b, 2), pm_one_pair(b, 3));
+    }
+  }
+}
+
+struct RowGroup {
+  int32_t rows[kMaxGroupRows];  // x/y row index per slot, −1 = empty
+  int32_t variant;              // 0 = base model
+};
+
+template <int NG, bool kM16, bool kSignVec>
+__device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& grp,
+                                           const uint8_t* __restrict__ packed,
+                                           const float* __restrict__ alpha, bool has_delta,
+                                           float* red) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_in = p.d_in, d_out = p.d_out;
+  const int64_t row_bytes = d_in / 8;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * (8 * NG);
+
+  const int ra_idx = grp.rows[g];
+  const int rb_idx = kM16 ? grp.rows[g + 8] : -1;
+  const uint16_t* xra = ra_idx >= 0 ? p.x + static_cast<int64_t>(ra_idx) * d_in : nullptr;
+  const uint16_t* xrb = rb_idx >= 0 ? p.x + static_cast<int64_t>(rb_idx) * d_in : nullptr;
+
+  const uint16_t* wrow[NG];
+  const uint8_t* srow[NG];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    const int64_t n = n0 + 8 * ng + g;
+    wrow[ng] = n < d_out ? p.w + n * d_in : nullptr;
+    srow[ng] = n < d_out ? packed + n * row_bytes : nullptr;
+  }
+
+  float acc_b[NG][4], acc_s[NG][4];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc_b[ng][e] = acc_s[ng][e] = 0.f;
+
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  const int64_t n_sc = d_in / 128;
+  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+    const int64_t kc0 = sc * 128;
+    uint4 wv[4][NG];
+    uint32_t sb[4][NG];
+    uint4 xa[4], xb[4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      if (wrow[ng] != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j][ng] = ldg_stream_v4(wrow[ng] + kc0 + 32 * j + 8 * t);
+        if (has_delta) {
+          if (kSignVec) {
+            const uint4 s = ldg_v4(srow[ng] + kc0 / 8);
+            sb[0][ng] = (s.x >> (8 * t)) & 0xFFu;
+            sb[1][ng] = (s.y >> (8 * t)) & 0xFFu;
+            sb[2][ng] = (s.z >> (8 * t)) & 0xFFu;
+            sb[3][ng] = (s.w >> (8 * t)) & 0xFFu;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sb[j][ng] = __ldg(srow[ng] + kc0 / 8 + 4 * j + t);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sb[j][ng] = 0xFFu;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          wv[j][ng] = zero4;
+          sb[j][ng] = 0xFFu;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      xa[j] = xra != nullptr ? ldg_v4(xra + kc0 + 32 * j + 8 * t) : zero4;
+      xb[j] = (kM16 && xrb != nullptr) ? ldg_v4(xrb + kc0 + 32 * j + 8 * t) : zero4;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) chunk_mma<NG>(acc_b, acc_s, wv[j], sb[j], xa[j], xb[j], has_delta);
+  }
+  // Tail: 32-column chunks past the last full 128-column block.  d_in is a
+  // multiple of 8, so each thread's 8 columns are wholly inside or outside.
+  for (int64_t c32 = n_sc * 4 + warp; c32 * 32 < d_in; c32 += kKW) {
+    const int64_t col = c32 * 32 + 8 * t;
+    const bool ok = col < d_in;
+    uint4 wv[NG];
+    uint32_t sb[NG];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const bool v = ok && wrow[ng] != nullptr;
+      wv[ng] = v ? ldg_stream_v4(wrow[ng] + col) : zero4;
+      sb[ng] = (v && has_delta) ? static_cast<uint32_t>(__ldg(srow[ng] + col / 8)) : 0xFFu;
+    }
+    const uint4 xa = (ok && xra != nullptr) ? ldg_v4(xra + col) : zero4;
+    const uint4 xb = (kM16 && ok && xrb != nullptr) ? ldg_v4(xrb + col) : zero4;
+    chunk_mma<NG>(acc_b, acc_s, wv, sb, xa, xb, has_delta);
+  }
+
+  // y_part = acc_b + α_n·acc_s for (m = g, g+8; n = n0 + 8ng + 2t + {0,1}).
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = acc_b[ng][e];
+      if (has_delta) {
+        const int64_t n = n0 + 8 * ng + 2 * t + (e & 1);
+        const float a = n < d_out ? (p.per_row ? __ldg(alpha + n) : __ldg(alpha)) : 0.f;
+        v = fmaf(a, acc_s[ng][e], v);
+      }
+      red[(warp * NG * 4 + ng * 4 + e) * 32 + lane] = v;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float s = 0.f;
+        for (int w = 0; w < kKW; ++w) s += red[(w * NG * 4 + ng * 4 + e) * 32 + lane];
+        v[e] = s;
+      }
+      const int64_t n = n0 + 8 * ng + 2 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int slot = g + 8 * h;
+        const int row = grp.rows[slot];
+        if (row < 0 || n >= d_out) continue;
+        uint16_t* yr = p.y + static_cast<int64_t>(row) * d_out;
+        const uint32_t pk = pack_bf16x2_rn(v[2 * h], v[2 * h + 1]);
+        if (n + 1 < d_out && (d_out % 2) == 0) {
+          *reinterpret_cast<uint32_t*>(yr + n) = pk;
+        } else {
+          yr[n] = static_cast<uint16_t>(pk & 0xFFFFu);
+          if (n + 1 < d_out) yr[n + 1] = static_cast<uint16_t>(pk >> 16);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Single variant: blockIdx.y (strided) picks 16 consecutive x rows.
+template <int NG, bool kM16, bool kSignVec>
+__global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
+  __shared__ float red[kKW * NG * 4 * 32];
+  __shared__ RowGroup grp;
+  const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
+  for (int64_t c = blockIdx.y; c < n_chunks; c += gridDim.y) {
+    if (threadIdx.x < kMaxGroupRows) {
+      const int64_t r = c * kMaxGroupRows + threadIdx.x;
+      grp.rows[threadIdx.x] = r < p.M ? static_cast<int32_t>(r) : -1;
+    }
+    if (threadIdx.x == 0) grp.variant = 1;
+    __syncthreads();
+    gemv_group<NG, kM16, kSignVec>(p, grp, p.packed, p.alpha, true, red);
+  }
+}
+
+// Multi-tenant: rows of short segments, bucketed by variant into groups of
+// up to 16 rows.  Every CTA builds the same grouping in shared memory, then
+// covers its 8·NG output columns for every group.
+template <int NG>
+__global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
+  __shared__ float red[kKW * NG * 4 * 32];
+  __shared__ RowGroup grp;
+  extern __shared__ int32_t dyn[];
+  // dyn: [n_var+2] bucket counts | [n_var+2] bucket starts | [max_rows] rows
+  const int nb = p.n_var + 1;
+  int32_t* cnt = dyn;
+  int32_t* start = dyn + (nb + 1);
+  int32_t* rows = dyn + 2 * (nb + 1);
+  for (int i = threadIdx.x; i < nb + 1; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  // Validate the whole table first: offsets must be non-decreasing inside
+  // [0, M] and ids inside [0, n_var].  One bad entry rejects the table (the
+  // error word records it and no row is computed), so segments can never
+  // overlap and the row list below never exceeds its bound.
+  int bad_local = 0;
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+    const int32_t a = __ldg(p.seg_off + s), b = __ldg(p.seg_off + s + 1);
+    const int32_t v = __ldg(p.seg_var + s);
+    bad_local |= (a < 0 || b < a || b > p.M || v < 0 || v > p.n_var) ? 1 : 0;
+  }
+  if (__syncthreads_or(bad_local)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
+    return;
+  }
+  // pass 1: count short-segment rows per variant
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+    const int32_t a = __ldg(p.seg_off + s), b = __ldg(p.seg_off + s + 1);
+    const int32_t v = __ldg(p.seg_var + s);
+    if (b - a > 0 && b - a <= p.max_short) atomicAdd(&cnt[v], b - a);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t acc = 0;
+    for (int v = 0; v < nb; ++v) {
+      start[v] = acc;
+      acc += cnt[v];
+      cnt[v] = 0;  // reused as fill cursor
+    }
+    start[nb] = acc;
+  }
+  __syncthreads();
+  // pass 2: scatter row indices into their bucket
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+    const int32_t a = __ldg(p.seg_off + s), b = __ldg(p.seg_off + s + 1);
+    const int32_t v = __ldg(p.seg_var + s);
+    if (b - a <= 0 || b - a > p.max_short) continue;
+    const int32_t pos = start[v] + atomicAdd(&cnt[v], b - a);
+    for (int32_t r = a; r < b; ++r) rows[pos + (r - a)] = r;
+  }
+  __syncthreads();
+  // groups: each bucket in slices of 16 rows
+  for (int v = 0; v < nb; ++v) {
+    const int32_t b0 = start[v], b1 = start[v + 1];
+    for (int32_t r0 = b0; r0 < b1; r0 += kMaxGroupRows) {
+      if (threadIdx.x < kMaxGroupRows) {
+        const int32_t r = r0 + threadIdx.x;
+        grp.rows[threadIdx.x] = r < b1 ? rows[r] : -1;
+      }
+      if (threadIdx.x == 0) grp.variant = v;
+      __syncthreads();
+      const uint8_t* pk = v > 0 ? p.packed_table[v - 1] : nullptr;
+      const float* al = v > 0 ? p.alpha_table[v - 1] : nullptr;
+      const bool vec = (p.d_in % 128 == 0) && ((reinterpret_cast<uintptr_t>(pk) & 15u) == 0);
+      if (vec)
+        gemv_group<NG, true, true>(p, grp, pk, al, v > 0, red);
+      else
+        gemv_group<NG, true, false>(p, grp, pk, al, v > 0, red);
+    }
+  }
+}
+
+template <int NG>
+cudaError_t launch_single(const GemvArgs& p, bool sign_vec, cudaStream_t stream) {
+  const int64_t n_blocks = (p.d_out + 8 * NG - 1) / (8 * NG);
+  const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
+  dim3 grid(static_cast<unsigned>(n_blocks),
+            static_cast<unsigned>(n_chunks < 65535 ? n_chunks : 65535));
+  const bool m16 = p.M > 8;
+  if (m16 && sign_vec)
+    gemv_single_kernel<NG, true, true><<<grid, kKW * 32, 0, stream>>>(p);
+  else if (m16)
+    gemv_single_kernel<NG, true, false><<<grid, kKW * 32, 0, stream>>>(p);
+  else if (sign_vec)
+    gemv_single_kernel<NG, false, true><<<grid, kKW * 32, 0, stream>>>(p);
+  else
+    gemv_single_kernel<NG, false, false><<<grid, kKW * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows) {
+  return sizeof(int32_t) * (2 * (static_cast<size_t>(n_var) + 2) + static_cast<size_t>(max_rows));
+}
+
+cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream) {
+  const bool sign_vec = (p.d_in % 128 == 0) &&
+                        (reinterpret_cast<uintptr_t>(p.packed) % 16 == 0);
+  return launch_single<2>(p, sign_vec, stream);
+}
+
+cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream) {
+  const size_t smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
+  const int64_t n_blocks = (p.d_out + 15) / 16;
+  dim3 grid(static_cast<unsigned>(n_blocks));
+  cudaError_t e = cudaFuncSetAttribute(gemv_grouped_kernel<2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  gemv_grouped_kernel<2><<<grid, kKW * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bd

@@ -1,0 +1,71 @@
+// kernels.h — launchers of the BitDelta CUDA kernels (internal to the library;
+// the public interface is include/bitdelta.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace bd {
+
+cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
+                            int64_t d_in, bool per_row, uint8_t* packed, float* alpha,
+                            double* row_sums, unsigned int* done_counter, int num_sms,
+                            cudaStream_t stream, DevCtx ctx);
+
+cudaError_t launch_reconstruct(const uint16_t* w_base, const uint8_t* packed, const float* alpha,
+                               bool per_row, int64_t d_out, int64_t d_in, uint16_t* w_out,
+                               int num_sms, cudaStream_t stream);
+
+// Decode-size linear (mma.sync, bandwidth-bound).
+struct GemvArgs {
+  const uint16_t* x;
+  int64_t M;  // rows of x (single) or M_total (grouped)
+  const uint16_t* w;
+  int64_t d_out, d_in;
+  const uint8_t* packed;  // single-variant mode
+  const float* alpha;
+  int per_row;
+  uint16_t* y;
+  // multi-tenant mode
+  const int32_t* seg_off;
+  const int32_t* seg_var;
+  int32_t n_seg, n_var, max_short;
+  const uint8_t* const* packed_table;
+  const float* const* alpha_table;
+  DevCtx ctx;
+};
+
+cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream);
+size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows);
+cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream);
+
+// Prefill-size linear (tcgen05 + TMA).
+struct GemmArgs {
+  int64_t M, d_out, d_in;
+  const uint8_t* packed;  // single-variant mode
+  const float* alpha;
+  int per_row;
+  uint16_t* y;
+  // multi-tenant mode (seg_off == nullptr for the single-variant call)
+  const int32_t* seg_off;
+  const int32_t* seg_var;
+  int32_t n_seg, n_var, max_short;
+  const uint8_t* const* packed_table;
+  const float* const* alpha_table;
+  DevCtx ctx;
+};
+
+constexpr int kGemmMaxSegs = 1024;
+int gemm_block_rows();    // d_out rows per tile
+int gemm_block_tokens();  // x rows per tile
+cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
+                        int grid, cudaStream_t stream);
+
+// Test hook: one CTA waiting on an mbarrier nothing completes.
+cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream);
+
+}  // namespace bd

@@ -1,0 +1,86 @@
+// reconstruct.cu — W_eff = W_base + α·sign(Δ) written to memory.
+//
+// Page "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "Serving architecture", request step 3 (build the effective weight) and the
+// conceptual fused_bitdelta_linear listing (w_eff = w_base + alpha·unpack).
+// Each element: fp32(W_base) + (bit ? α : −α) as one IEEE binary32 add, then
+// round-to-nearest-even to bf16 (cvt.rn.bf16x2.f32).
+//
+// One warp per row (grid-stride).  Lane L handles 8-column chunks L, L+32, …:
+// one 16-byte load of W_base, one sign byte (32 lanes read 32 consecutive
+// bytes), one 16-byte store.  HBM traffic: 2 + 1/8 + 2 bytes per weight.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bd {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kUnroll = 4;
+
+// ±α as bit patterns: bit 1 keeps +α, bit 0 gives −α (α >= 0 so only the sign
+// bit changes).  `neg_alpha` is α with its sign bit set.
+__device__ __forceinline__ float signed_alpha(uint32_t byte, int col, uint32_t neg_alpha) {
+  return __uint_as_float(neg_alpha ^ ((byte << (31 - col)) & 0x80000000u));
+}
+
+__device__ __forceinline__ uint4 effective_chunk(uint4 w, uint32_t byte, uint32_t neg_alpha) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __fadd_rn(bf16lo_to_f32(in[j]), signed_alpha(byte, 2 * j, neg_alpha));
+    const float hi = __fadd_rn(bf16hi_to_f32(in[j]), signed_alpha(byte, 2 * j + 1, neg_alpha));
+    out[j] = pack_bf16x2_rn(lo, hi);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    reconstruct_kernel(const uint16_t* __restrict__ w_base, const uint8_t* __restrict__ packed,
+                       const float* __restrict__ alpha, int per_row, int64_t d_out,
+                       int64_t d_in, uint16_t* __restrict__ w_out) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t chunks = d_in / 8;
+  const int64_t row_step = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; row < d_out;
+       row += row_step) {
+    const float a = per_row ? __ldg(alpha + row) : __ldg(alpha);
+    const uint32_t neg_alpha = __float_as_uint(a) | 0x80000000u;
+    const uint4* src = reinterpret_cast<const uint4*>(w_base + row * d_in);
+    uint4* dst = reinterpret_cast<uint4*>(w_out + row * d_in);
+    const uint8_t* sg = packed + row * chunks;
+    int64_t k = lane;
+    for (; k + 32 * (kUnroll - 1) < chunks; k += 32 * kUnroll) {
+      uint4 v[kUnroll];
+      uint32_t s[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        v[u] = ldg_stream_v4(src + k + 32 * u);
+        s[u] = __ldg(sg + k + 32 * u);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) dst[k + 32 * u] = effective_chunk(v[u], s[u], neg_alpha);
+    }
+    for (; k < chunks; k += 32)
+      dst[k] = effective_chunk(ldg_stream_v4(src + k), __ldg(sg + k), neg_alpha);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reconstruct(const uint16_t* w_base, const uint8_t* packed, const float* alpha,
+                               bool per_row, int64_t d_out, int64_t d_in, uint16_t* w_out,
+                               int num_sms, cudaStream_t stream) {
+  const int64_t blocks_needed = (d_out + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+  reconstruct_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(w_base, packed, alpha,
+                                                              per_row ? 1 : 0, d_out, d_in, w_out);
+  return cudaGetLastError();
+}
+
+}  // namespace bd

@@ -1,0 +1,158 @@
+/*
+ * bitdelta.h — C ABI of the GB300 (sm_103a) BitDelta hot path.
+ *
+ * The method: a fine-tuned weight W_ft is stored as the shared base weight
+ * W_base plus a 1-bit delta, W_ft ≈ W_base + α·sign(Δ) with Δ = W_ft − W_base
+ * and α = mean|Δ| (page "BitDelta: serving 14 Zen models from one GPU
+ * cluster", hanzo blog 2026-02-28, section "Mathematical foundation").  At
+ * serving time one fused kernel reads W_base and the packed sign bits and
+ * multiplies by the effective weight without writing it to HBM (same page,
+ * section "Serving architecture", the fused-kernel paragraph and the
+ * conceptual fused_bitdelta_linear listing).
+ *
+ * Formats (all row-major, C order):
+ *   bf16 tensors   uint16_t bit patterns (IEEE binary32 upper half).
+ *   W_base, W_ft   bf16 [d_out, d_in]   (torch.nn.functional.linear layout).
+ *   packed         uint8 [d_out, d_in/8]: bit j of byte k of row r is the sign
+ *                  of Δ[r][8k+j]; bit 1 = +1, bit 0 = −1, and sign(0) = +1
+ *                  (section "Infrastructure details": 8 bits per byte,
+ *                  4096x4096 -> 4096x512).
+ *   alpha          float32: one value (BD_ALPHA_PER_MATRIX, section
+ *                  "Mathematical foundation") or one per output row
+ *                  (BD_ALPHA_PER_ROW, section "Infrastructure details").
+ *   x, y           bf16 [M, d_in] and [M, d_out]; M = batch·seq rows.
+ *   W_eff          bf16_rne(fp32(W_base) + (bit ? α : −α)).
+ *
+ * Rules common to every call:
+ *   - Pointers are device pointers (cudaMalloc / torch CUDA memory) owned by
+ *     the caller, unless a parameter says "host".  The library keeps no
+ *     pointer after a call returns and allocates no device memory.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and never synchronises the device.
+ *   - Arguments are checked on the host before any launch; an invalid call
+ *     returns an error status and launches nothing.  Nothing aborts or traps.
+ *   - d_in must be a positive multiple of 8 (one whole sign byte per 8
+ *     columns); d_out >= 1; M >= 0 (M == 0 is a no-op).
+ *   - bf16 tensors must start on a 16-byte boundary (BD_ERR_MISALIGNED).
+ *   - Device-side faults that cannot be seen on the host (a wait that ran out
+ *     of time, a variant id out of range in device memory) set a sticky error
+ *     word that bitdelta_check_error() reports.
+ */
+#ifndef BITDELTA_H_
+#define BITDELTA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st*). */
+typedef struct CUstream_st* bd_stream_t;
+
+typedef enum {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+  BD_ERR_UNSUPPORTED_SHAPE = 2, /* d_in not a positive multiple of 8, size too large */
+  BD_ERR_MISALIGNED = 3,        /* a bf16 tensor not 16-byte aligned */
+  BD_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
+  BD_ERR_CUDA = 5,              /* a CUDA runtime call failed (launch, attribute) */
+  BD_ERR_DEVICE_TIMEOUT = 6,    /* a bounded device wait ran out (check_error) */
+  BD_ERR_DEVICE_BOUNDS = 7      /* bad segment table / variant id seen on device */
+} bd_status;
+
+typedef enum { BD_ALPHA_PER_MATRIX = 0, BD_ALPHA_PER_ROW = 1 } bd_alpha_mode;
+
+/* Bytes of the packed sign matrix: d_out * d_in / 8 (0 on invalid sizes). */
+size_t bitdelta_packed_bytes(int64_t d_out, int64_t d_in);
+
+/* Workspace bytes bitdelta_compress needs: 0 for BD_ALPHA_PER_ROW,
+ * 8*d_out + 256 for BD_ALPHA_PER_MATRIX (per-row fp64 partial sums and a
+ * completion counter). */
+size_t bitdelta_compress_workspace_bytes(int64_t d_out, int64_t d_in, bd_alpha_mode mode);
+
+/*
+ * Compression ("Mathematical foundation": Δ = W_ft − W_base, sign(Δ) to one
+ * bit, α = (1/n)·‖Δ‖₁).  One pass over W_base and W_ft: writes packed_out
+ * [d_out, d_in/8] and alpha_out (1 float for PER_MATRIX, d_out floats for
+ * PER_ROW).  α is summed per row in compensated fp32 and fp64 across rows in
+ * a fixed order, so the result is deterministic run to run.
+ * workspace: device memory of at least bitdelta_compress_workspace_bytes()
+ * (may be NULL when that is 0); its contents on entry do not matter.  Two
+ * calls that share one workspace must not overlap on the GPU.
+ */
+bd_status bitdelta_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
+                            int64_t d_in, bd_alpha_mode mode, uint8_t* packed_out,
+                            float* alpha_out, void* workspace, size_t workspace_bytes,
+                            bd_stream_t stream);
+
+/*
+ * Reconstruction to memory ("Serving architecture", request step 3:
+ * W_eff = W_base + α·sign(Δ)).  Writes w_out bf16 [d_out, d_in]; bit-exact
+ * W_eff = bf16_rne(fp32(W_base) ± α).  w_out must not overlap the inputs.
+ */
+bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, const float* alpha,
+                               bd_alpha_mode mode, int64_t d_out, int64_t d_in, uint16_t* w_out,
+                               bd_stream_t stream);
+
+/*
+ * Fused delta linear ("Serving architecture", fused kernel paragraph and the
+ * conceptual fused_bitdelta_linear listing): y = x · W_effᵀ with W_eff built
+ * on chip and never written to memory.  x bf16 [M, d_in], y bf16 [M, d_out]
+ * (fp32 accumulation, one RNE rounding at the end), no bias.
+ * Dispatch: M <= 16 takes the bandwidth-bound decode kernel; larger M the
+ * tcgen05 tensor-core kernel when d_in % 128 == 0 and every pointer allows
+ * TMA, else the decode kernel over 16-row chunks.
+ * y must not overlap the inputs.
+ */
+bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
+                          const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
+                          int64_t d_out, int64_t d_in, uint16_t* y, bd_stream_t stream);
+
+/*
+ * Multi-tenant linear over one shared W_base ("Serving architecture": base
+ * weights shared-read by every variant; a request's model id selects its
+ * delta).  Rows [seg_offsets[s], seg_offsets[s+1]) of x use variant
+ * seg_variant[s]; variant 0 is the base model (W_eff = W_base, no delta),
+ * variant v in 1..n_var uses packed_table[v-1] and alpha_table[v-1].
+ *   seg_offsets   device int32 [n_seg+1], non-decreasing, seg_offsets[0] = 0,
+ *                 seg_offsets[n_seg] = M_total.
+ *   seg_variant   device int32 [n_seg], values in [0, n_var].
+ *   packed_table  device array of n_var device pointers (each [d_out, d_in/8]).
+ *   alpha_table   device array of n_var device pointers (each 1 or d_out floats).
+ *   max_seg_len   host upper bound on any segment's length (dispatch hint; a
+ *                 segment longer than 16 rows takes the tensor-core kernel).
+ * A malformed table found on the device sets BD_ERR_DEVICE_BOUNDS (see
+ * bitdelta_check_error) and leaves the affected rows of y unspecified.
+ */
+bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int32_t* seg_offsets,
+                                  const int32_t* seg_variant, int32_t n_seg, int32_t max_seg_len,
+                                  const uint16_t* w_base, const uint8_t* const* packed_table,
+                                  const float* const* alpha_table, int32_t n_var,
+                                  bd_alpha_mode mode, int64_t d_out, int64_t d_in, uint16_t* y,
+                                  bd_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device error word
+ * of the current device (BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_DEVICE_BOUNDS),
+ * or BD_ERR_CUDA if the synchronisation itself failed. */
+bd_status bitdelta_check_error(bd_stream_t stream);
+
+/* Upper bound, in nanoseconds, on any single bounded wait inside a kernel
+ * (default 2e9).  Values below 1000 are raised to 1000.  Host-side setting
+ * read at each launch. */
+bd_status bitdelta_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: launches one CTA that waits on an mbarrier nothing will complete,
+ * with the current wait limit.  The wait gives up, records
+ * BD_ERR_DEVICE_TIMEOUT in the error word and the kernel returns normally. */
+bd_status bitdelta_debug_wait_timeout(bd_stream_t stream);
+
+/* Static string for a status code. */
+const char* bitdelta_status_string(bd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITDELTA_H_ */

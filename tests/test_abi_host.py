@@ -1,0 +1,109 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (no GPU needed: every call here
+returns before any CUDA API call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import bit_weight_delta_gb300 as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitdelta.h")
+
+OK, INVALID, SHAPE, MISALIGNED, WORKSPACE = 0, 1, 2, 3, 4
+BAD = ctypes.c_void_p(0x1001)     # never dereferenced: rejected as misaligned first
+GOOD = ctypes.c_void_p(0x100000)  # 16-byte aligned fake address, never dereferenced
+NULL = ctypes.c_void_p(0)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return bd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(bitdelta_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("bitdelta_compress", "bitdelta_reconstruct", "bitdelta_linear",
+                     "bitdelta_linear_grouped", "bitdelta_check_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", bd.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(bd.EXPORTED) == set(declared_functions())
+
+
+def test_packed_bytes_and_workspace(lib):
+    assert bd.bitdelta_packed_bytes(4096, 4096) == 4096 * 512   # "Infrastructure details"
+    assert bd.bitdelta_packed_bytes(8, 16) == 16
+    assert bd.bitdelta_packed_bytes(8, 12) == 0                  # d_in % 8 != 0
+    assert bd.bitdelta_compress_workspace_bytes(4096, 4096, per_row=True) == 0
+    assert bd.bitdelta_compress_workspace_bytes(4096, 4096, per_row=False) == 8 * 4096 + 256
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert bd.status_string(code)
+    assert bd.status_string(99) == "unknown status"
+
+
+def test_compress_rejects_bad_arguments(lib):
+    f = lib.bitdelta_compress
+    assert f(NULL, GOOD, 8, 16, 1, GOOD, GOOD, NULL, 0, NULL) == INVALID
+    assert f(GOOD, GOOD, 8, 16, 7, GOOD, GOOD, NULL, 0, NULL) == INVALID     # bad mode
+    assert f(GOOD, GOOD, 0, 16, 1, GOOD, GOOD, NULL, 0, NULL) == INVALID     # d_out 0
+    assert f(GOOD, GOOD, 8, 12, 1, GOOD, GOOD, NULL, 0, NULL) == SHAPE       # d_in % 8
+    assert f(BAD, GOOD, 8, 16, 1, GOOD, GOOD, NULL, 0, NULL) == MISALIGNED
+    assert f(GOOD, GOOD, 8, 16, 0, GOOD, GOOD, NULL, 0, NULL) == WORKSPACE   # per-matrix
+    assert f(GOOD, GOOD, 8, 16, 0, GOOD, GOOD, GOOD, 16, NULL) == WORKSPACE  # too small
+
+
+def test_reconstruct_rejects_bad_arguments(lib):
+    f = lib.bitdelta_reconstruct
+    assert f(GOOD, NULL, GOOD, 1, 8, 16, GOOD, NULL) == INVALID
+    assert f(GOOD, GOOD, GOOD, 1, 8, 20, GOOD, NULL) == SHAPE
+    assert f(GOOD, GOOD, GOOD, 1, 8, 16, BAD, NULL) == MISALIGNED
+
+
+def test_linear_rejects_bad_arguments(lib):
+    f = lib.bitdelta_linear
+    assert f(GOOD, -1, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, NULL) == INVALID
+    assert f(NULL, 4, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, NULL) == INVALID
+    assert f(GOOD, 4, GOOD, GOOD, GOOD, 1, 8, 9, GOOD, NULL) == SHAPE
+    assert f(BAD, 4, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, NULL) == MISALIGNED
+    # M == 0 is a no-op that needs no pointers and no device
+    assert f(NULL, 0, NULL, NULL, NULL, 1, 8, 16, NULL, NULL) == OK
+
+
+def test_grouped_rejects_bad_arguments(lib):
+    f = lib.bitdelta_linear_grouped
+    args = dict(x=GOOD, M=4, so=GOOD, sv=GOOD, n_seg=1, max_len=4, wb=GOOD, pt=GOOD, at=GOOD,
+                n_var=1, mode=1, d_out=8, d_in=16, y=GOOD)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return f(a["x"], a["M"], a["so"], a["sv"], a["n_seg"], a["max_len"], a["wb"], a["pt"],
+                 a["at"], a["n_var"], a["mode"], a["d_out"], a["d_in"], a["y"], NULL)
+
+    assert call(n_seg=-1) == INVALID
+    assert call(n_var=-1) == INVALID
+    assert call(mode=3) == INVALID
+    assert call(so=NULL) == INVALID
+    assert call(pt=NULL) == INVALID
+    assert call(d_in=10) == SHAPE
+    assert call(y=BAD) == MISALIGNED
+    assert call(M=0, x=NULL, so=NULL) == OK      # empty batch is a no-op
+    assert call(n_seg=0, so=NULL) == OK

@@ -1,0 +1,105 @@
+"""GPU parity: bitdelta_linear_grouped (one shared W_base, per-segment variant
+ids, variant 0 = base model) against the oracle ("Serving architecture":
+base weights shared-read by every variant, the request's model id selects the
+delta)."""
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_delta_gb300 as bd
+import oracle
+import synth
+from gpu_util import assert_linear_close, bf16_values, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(seed, d_out, d_in, n_var, lengths, per_row=True, variants=None):
+    wb = synth.base_weight(seed, d_out, d_in)
+    scales = synth.variant_scales(seed, n_var)
+    packs, alphas = [], []
+    for v in range(n_var):
+        wf = synth.finetuned_weight(seed, wb, b=float(scales[v]), stream=100 + v)
+        p, a, _ = oracle.compress(wb, wf, per_row)
+        packs.append(p)
+        alphas.append(a)
+    off, var = synth.segments(seed, lengths, n_var)
+    if variants is not None:
+        var = np.asarray(variants, np.int32)
+    x = synth.activations(seed, int(off[-1]), d_in)
+    return wb, packs, alphas, off, var, x
+
+
+def _run(wb, packs, alphas, off, var, x, per_row):
+    dp = [to_dev(p) for p in packs]
+    da = [to_dev(a) for a in alphas]
+    pt, at = bd.variant_tables(dp, da, "cuda")
+    y = bd.bitdelta_linear_grouped(to_dev_bf16(x), to_dev(off), to_dev(var), to_dev_bf16(wb), pt,
+                                   at, n_var=len(packs), max_seg_len=int(np.diff(off).max()),
+                                   per_row=per_row)
+    assert bd.bitdelta_check_error() == 0
+    return bf16_values(y)
+
+
+@pytest.mark.parametrize("per_row", [True, False])
+def test_grouped_small_mixed(per_row):
+    """Decode rows and long segments, all variant ids including base."""
+    lengths = [1, 1, 3, 40, 1, 2, 300, 1, 16, 17, 5]
+    wb, packs, alphas, off, var, x = _setup(11, 200, 512, 4, lengths, per_row)
+    var = np.array([0, 1, 2, 3, 4, 0, 2, 1, 3, 0, 4], np.int32)
+    y = _run(wb, packs, alphas, off, var, x, per_row)
+    ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, per_row)
+    assert_linear_close(y, ref)
+    for s in range(len(var)):     # every segment on its own scale too
+        rows = slice(off[s], off[s + 1])
+        assert_linear_close(y[rows], ref[rows], f"segment {s}")
+
+
+def test_grouped_decode_only_ragged_d_in():
+    """All segments short; d_in not a multiple of 128 (byte-wise signs)."""
+    lengths = [1] * 20 + [2, 3]
+    wb, packs, alphas, off, var, x = _setup(12, 130, 200, 5, lengths)
+    y = _run(wb, packs, alphas, off, var, x, True)
+    assert_linear_close(y, oracle.linear_grouped(x, off, var, wb, packs, alphas, True))
+
+
+def test_grouped_long_segments_without_tma_shape():
+    """Long segments with d_in % 128 != 0 run through the decode kernel."""
+    lengths = [33, 1, 20]
+    wb, packs, alphas, off, var, x = _setup(13, 64, 136, 2, lengths)
+    y = _run(wb, packs, alphas, off, var, x, True)
+    assert_linear_close(y, oracle.linear_grouped(x, off, var, wb, packs, alphas, True))
+
+
+def test_grouped_base_rows_match_plain_gemm():
+    lengths = [5, 300, 1]
+    wb, packs, alphas, off, var, x = _setup(14, 256, 512, 2, lengths, variants=[0, 0, 0])
+    y = _run(wb, packs, alphas, off, var, x, True)
+    ref = (to_dev_bf16(x).float() @ to_dev_bf16(wb).float().T).double().cpu().numpy()
+    assert_linear_close(y, ref)
+
+
+def test_grouped_equals_single_variant_calls():
+    lengths = [2, 260, 1, 7]
+    wb, packs, alphas, off, var, x = _setup(15, 384, 1024, 3, lengths,
+                                            variants=[1, 2, 3, 2])
+    y = _run(wb, packs, alphas, off, var, x, True)
+    for s in range(4):
+        rows = slice(off[s], off[s + 1])
+        v = var[s] - 1
+        single = bd.bitdelta_linear(to_dev_bf16(x[rows]), to_dev_bf16(wb), to_dev(packs[v]),
+                                    to_dev(alphas[v]), per_row=True)
+        assert_linear_close(y[rows], bf16_values(single), f"segment {s}")
+
+
+def test_grouped_bad_variant_id_is_reported():
+    """A variant id outside [0, n_var] in device memory: no fault, an error status."""
+    lengths = [1, 2]
+    wb, packs, alphas, off, var, x = _setup(16, 64, 128, 1, lengths, variants=[0, 5])
+    dp = [to_dev(p) for p in packs]
+    da = [to_dev(a) for a in alphas]
+    pt, at = bd.variant_tables(dp, da, "cuda")
+    bd.bitdelta_linear_grouped(to_dev_bf16(x), to_dev(off), to_dev(var), to_dev_bf16(wb), pt, at,
+                               n_var=1, max_seg_len=2, per_row=True)
+    assert bd.bitdelta_check_error() == 7   # BD_ERR_DEVICE_BOUNDS
+    assert bd.bitdelta_check_error() == 0
