@@ -334,10 +334,19 @@ cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_
   const size_t smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
   const int64_t n_blocks = (p.d_out + 15) / 16;
   dim3 grid(static_cast<unsigned>(n_blocks));
-  cudaError_t e = cudaFuncSetAttribute(gemv_grouped_kernel<2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // Raise the dynamic shared-memory limit only when a call needs more than
+  // any earlier call on this device (so captured calls make no attribute call).
+  static size_t smem_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && smem > smem_set[dev]) {
+    e = cudaFuncSetAttribute(gemv_grouped_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    smem_set[dev] = smem;
+  }
   gemv_grouped_kernel<2><<<grid, kKW * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
