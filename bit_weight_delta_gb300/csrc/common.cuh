@@ -226,6 +226,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ PDL
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream finishes;
+// griddep_wait() blocks until that kernel has completed and its memory is
+// visible, so it must come before the first read of data a predecessor may
+// write and before the first global write.  Without the launch attribute both
+// are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// L2 prefetch hint for the line holding `p` (no data is returned; safe before
+// griddep_wait because L2 is the point of coherence).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2::evict_normal [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------------ bf16 bits
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }

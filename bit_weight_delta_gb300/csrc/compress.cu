@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                     float* __restrict__ alpha, double* __restrict__ row_sums,
                     unsigned int* __restrict__ done_counter, DevCtx ctx) {
   (void)ctx;
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t chunks = d_in / 8;  // sign bytes per row
@@ -157,13 +159,13 @@ cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_
   const int64_t blocks_needed = (d_out + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
   const int grid = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+  const dim3 block(kWarpsPerBlock * 32);
   if (per_row)
-    compress_kernel<true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-        w_base, w_ft, d_out, d_in, packed, alpha, nullptr, nullptr, ctx);
-  else
-    compress_kernel<false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-        w_base, w_ft, d_out, d_in, packed, alpha, row_sums, done_counter, ctx);
-  return cudaGetLastError();
+    return launch_pdl(compress_kernel<true>, dim3(grid), block, 0, stream, w_base, w_ft, d_out,
+                      d_in, packed, alpha, static_cast<double*>(nullptr),
+                      static_cast<unsigned int*>(nullptr), ctx);
+  return launch_pdl(compress_kernel<false>, dim3(grid), block, 0, stream, w_base, w_ft, d_out,
+                    d_in, packed, alpha, row_sums, done_counter, ctx);
 }
 
 }  // namespace bd

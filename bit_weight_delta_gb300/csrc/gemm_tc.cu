@@ -11,17 +11,19 @@
 // operand B = x) x 64 K per stage; D = W_eff·xᵀ = yᵀ accumulates in TMEM
 // (fp32, 128 lanes x 256 columns, double-buffered).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over tiles):
-//   warps 0-3  transform: wait for the TMA'd W_base stage, rewrite it in
-//              place as W_eff = bf16_rne(fp32(W_base) ± α) (same 128-byte
-//              swizzled layout, so each 16-byte chunk maps to itself), make the
-//              writes visible to the async proxy, arrive.  The signs (8 bytes
-//              per row per stage) and α are prefetched with cp.async into a
-//              small ring several stages ahead.
-//   warps 4-7  epilogue: tcgen05.ld the finished accumulator (lane = n,
-//              column = token), round to bf16, store y.
-//   warp 8     TMA producer: W_base tile [128 x 64] and x tile [256 x 64].
-//   warp 9     MMA issuer: 4 x tcgen05.mma (128x256x16) per stage, commit.
+// Warp roles (448 threads, one CTA per SM, persistent over tiles):
+//   warps 0-7   transform: each warp owns 16 of the 128 W rows.  It waits for
+//               the TMA'd W_base stage, rewrites its rows in place as
+//               W_eff = bf16_rne(fp32(W_base) ± α) (same 128-byte swizzled
+//               layout, so each 16-byte chunk maps to itself), makes the writes
+//               visible to the async proxy and arrives once.  Its lanes
+//               prefetch their rows' sign bytes (8 per row per stage) and α
+//               with cp.async into a ring several stages ahead.  The warps
+//               never synchronise with one another.
+//   warps 8-11  epilogue: tcgen05.ld the finished accumulator (lane = n,
+//               column = token), round to bf16, store y.
+//   warp 12     TMA producer: W_base tile [128 x 64] and x tile [256 x 64].
+//   warp 13     MMA issuer: 4 x tcgen05.mma (128x256x16) per stage, commit.
 // Every wait is bounded (kernel records a timeout and unwinds); TMEM is
 // released on every exit path.
 #include <cstdint>
@@ -32,21 +34,30 @@
 namespace bd {
 namespace {
 
-constexpr int kBM = 128;  // d_out rows per tile
-constexpr int kBN = 256;  // tokens per tile
-constexpr int kBK = 64;   // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 4;
+#ifndef BD_GEMM_BN
+#define BD_GEMM_BN 256
+#endif
+#ifndef BD_GEMM_STAGES
+#define BD_GEMM_STAGES 4
+#endif
+constexpr int kBM = 128;         // d_out rows per tile
+constexpr int kBN = BD_GEMM_BN;  // tokens per tile
+constexpr int kBK = 64;          // K per stage: one 128-byte swizzle atom of bf16
+constexpr int kStages = BD_GEMM_STAGES;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kPrefetch = 4;            // sign/α prefetch distance (stages)
 constexpr int kRing = kPrefetch + 2;    // ring slots (see the transform loop)
 constexpr int kAccCols = kBN;           // fp32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kThreads = 320;
-constexpr int kXfThreads = 128;
-constexpr int kEpiWarp0 = 4;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kXfWarps = 8;                     // transform warps (independent)
+constexpr int kXfRows = kBM / kXfWarps;         // W rows each transform warp owns
+constexpr int kEpiWarp0 = kXfWarps;             // 4 epilogue warps: TMEM lane quarters 0..3
+constexpr int kTmaWarp = kEpiWarp0 + 4;
+constexpr int kMmaWarp = kTmaWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start a warpgroup");
+static_assert(kXfRows == 16, "transform lane mapping assumes 16 rows per warp");
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 
 // Shared memory layout (offsets from a 1024-byte aligned base).
@@ -134,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&xform_bar[s], kXfThreads);
+      mbar_init(&xform_bar[s], kXfWarps);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -205,17 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total_q = my_tiles * n_kb;
   const int32_t* seg_off_tbl = grouped ? s_seg_off : nullptr;
 
-  if (warp < 4) {
+  if (warp < kXfWarps) {
     // ============================================================ transform
-    const int tid = threadIdx.x;  // 0..127: also the row this thread prefetches
-    const int p8 = lane & 7;      // physical 16-byte chunk within a 128-byte row
-    const int rq = lane >> 3;
+    const int p8 = lane & 7;    // physical 16-byte chunk within a 128-byte row
+    const int rsub = lane >> 3;  // rows of this lane: kXfRows*warp + 4*i + rsub
+    const int row0 = kXfRows * warp;
     uint8_t* sign_ring = smem + kOffSign;
     float* alpha_ring = reinterpret_cast<float*>(smem + kOffAlpha);
     const int64_t row_bytes = p.d_in / 8;
 
+    // Lanes 0..15 copy the sign bytes (and, at k-block 0, α) of row row0+lane
+    // for flat stage q into ring slot q % kRing.  Every lane commits a group.
     auto prefetch = [&](int64_t q) {
-      if (q < total_q) {
+      if (q < total_q && lane < kXfRows) {
         const int64_t i = q / n_kb;
         const int64_t kb = q - i * n_kb;
         const Tile tl = tile_at(p, blockIdx.x + i * gridDim.x, t_total, seg_off_tbl, s_seg_var,
@@ -224,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tl.variant > 0) {
           const uint8_t* pk = grouped ? p.packed_table[tl.variant - 1] : p.packed;
           const float* al = grouped ? p.alpha_table[tl.variant - 1] : p.alpha;
-          const int64_t row = tl.n0 + tid;
-          uint8_t* dst = sign_ring + (slot * kBM + tid) * 8;
+          const int r = row0 + lane;
+          const int64_t row = tl.n0 + r;
+          uint8_t* dst = sign_ring + (slot * kBM + r) * 8;
           if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & 7u) == 0) {
             cp_async_8(dst, pk + row * row_bytes + kb * 8);
           } else {
@@ -233,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
           }
           if (kb == 0) {
-            float* adst = alpha_ring + slot * kBM + tid;
+            float* adst = alpha_ring + slot * kBM + r;
             if (row < p.d_out)
               cp_async_4(adst, p.per_row ? al + row : al);
             else
@@ -245,8 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch(d);
-    uint32_t neg_alpha[8];
-    int32_t* ok_flag = reinterpret_cast<int32_t*>(smem + kOffMisc + 32);
+    uint32_t neg_alpha[4];
     Tile tl{0, 0, 0, 0};
     for (int64_t q = 0; q < total_q; ++q) {
       prefetch(q + kPrefetch);
@@ -255,51 +268,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t kb = q - i * n_kb;
       const int s = static_cast<int>(q % kStages);
       const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
-      // One thread waits; the named barrier publishes its verdict (and the ring
-      // bytes of stage q) so all 128 threads leave the loop together.  The
-      // flag alternates between two slots: thread 0 can only rewrite a slot
-      // after every thread has passed the next barrier, i.e. has read it.
-      volatile int32_t* flag = ok_flag + (q & 1);
-      if (tid == 0) *flag = mbar_wait(&full_bar[s], ph, p.ctx, abort) ? 1 : 0;
-      named_barrier(1, kXfThreads);
-      if (*flag == 0) break;
+      // lane 0 waits; the shuffle makes the verdict warp-uniform, __syncwarp
+      // publishes the lanes' ring bytes of stage q to the whole warp
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&full_bar[s], ph, p.ctx, abort) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
       if (kb == 0)
         tl = tile_at(p, blockIdx.x + i * gridDim.x, t_total, seg_off_tbl, s_seg_var, s_prefix);
       if (tl.variant > 0) {
         const int slot = static_cast<int>(q % kRing);
         if (kb == 0) {
 #pragma unroll
-          for (int r8 = 0; r8 < 8; ++r8) {
-            const int r = 32 * warp + 4 * r8 + rq;
-            neg_alpha[r8] = __float_as_uint(alpha_ring[slot * kBM + r]) | 0x80000000u;
+          for (int r4 = 0; r4 < 4; ++r4) {
+            const int r = row0 + 4 * r4 + rsub;
+            neg_alpha[r4] = __float_as_uint(alpha_ring[slot * kBM + r]) | 0x80000000u;
           }
         }
         uint8_t* a_tile = smem + kOffA + s * kABytes;
+        uint4 w[4];
+        uint32_t byte[4];
 #pragma unroll
-        for (int r8 = 0; r8 < 8; ++r8) {
-          const int r = 32 * warp + 4 * r8 + rq;
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int r = row0 + 4 * r4 + rsub;
           const int c = p8 ^ (r & 7);  // logical chunk: columns 8c .. 8c+7
-          const uint32_t byte = sign_ring[(slot * kBM + r) * 8 + c];
-          uint4* chunk = reinterpret_cast<uint4*>(a_tile + r * 128 + p8 * 16);
-          const uint4 w = *chunk;
-          const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+          byte[r4] = sign_ring[(slot * kBM + r) * 8 + c];
+          w[r4] = *reinterpret_cast<const uint4*>(a_tile + r * 128 + p8 * 16);
+        }
+#pragma unroll
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int r = row0 + 4 * r4 + rsub;
+          const uint32_t in[4] = {w[r4].x, w[r4].y, w[r4].z, w[r4].w};
           uint32_t out[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float lo =
-                __fadd_rn(bf16lo_to_f32(in[j]), signed_alpha(byte, 2 * j, neg_alpha[r8]));
+                __fadd_rn(bf16lo_to_f32(in[j]), signed_alpha(byte[r4], 2 * j, neg_alpha[r4]));
             const float hi =
-                __fadd_rn(bf16hi_to_f32(in[j]), signed_alpha(byte, 2 * j + 1, neg_alpha[r8]));
+                __fadd_rn(bf16hi_to_f32(in[j]), signed_alpha(byte[r4], 2 * j + 1, neg_alpha[r4]));
             out[j] = pack_bf16x2_rn(lo, hi);
           }
-          *chunk = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(a_tile + r * 128 + p8 * 16) =
+              make_uint4(out[0], out[1], out[2], out[3]);
         }
         fence_proxy_async_smem();
       }
-      mbar_arrive(&xform_bar[s]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xform_bar[s]);
     }
     cp_async_wait<0>();
-  } else if (warp < 8) {
+  } else if (warp < kTmaWarp) {
     // ============================================================ epilogue
     const int quarter = warp - kEpiWarp0;  // TMEM lanes 32*quarter ..
     for (int64_t i = 0; i < my_tiles; ++i) {

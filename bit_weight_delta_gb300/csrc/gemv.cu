@@ -19,8 +19,11 @@
 // W_base row (8 adjacent columns; the 4 threads of a quad cover 64 contiguous
 // bytes) and the matching 8 columns of two x rows.  The columns inside a
 // fragment are permuted consistently for A and B, which a dot product allows.
-// Sign bits arrive as one 16-byte load per row per 128 columns.  Per weight
-// the kernel moves 2 + 1/8 bytes from HBM; x stays in L1/L2.
+// Sign bits arrive as one 16-byte load per row per super-chunk of 128 columns;
+// each warp keeps two super-chunks of loads in flight.  Per weight the kernel
+// moves 2 + 1/8 bytes from HBM; x stays in L1/L2.  Launched with programmatic
+// dependent launch: the CTA prefetches its weight slice into L2 before it
+// waits for the previous kernel, so consecutive layers overlap.
 #include <cstdint>
 
 #include "common.cuh"
@@ -29,7 +32,22 @@
 namespace bd {
 namespace {
 
-constexpr int kKW = 4;  // warps splitting d_in in a CTA
+// Launch shape: kNG groups of 8 output rows per CTA, kKW warps splitting d_in,
+// super-chunks of kCPS x 32 columns (two in flight per warp).  The defaults
+// were the fastest of a sweep on the 4096x4096 decode layer.
+#ifndef BD_GEMV_NG
+#define BD_GEMV_NG 2
+#endif
+#ifndef BD_GEMV_KW
+#define BD_GEMV_KW 4
+#endif
+#ifndef BD_GEMV_CPS
+#define BD_GEMV_CPS 4
+#endif
+constexpr int kNG = BD_GEMV_NG;
+constexpr int kKW = BD_GEMV_KW;
+constexpr int kCPS = BD_GEMV_CPS;
+static_assert(kCPS == 4, "sign words are fetched 16 bytes (128 columns) at a time");
 constexpr int kMaxGroupRows = 16;
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -69,7 +87,16 @@ struct RowGroup {
   int32_t variant;              // 0 = base model
 };
 
-template <int NG, bool kM16, bool kSignVec>
+// Register-resident operands of one super-chunk (CPS chunks of 32 columns).
+template <int NG, int CPS, bool kM16>
+struct Frag {
+  uint4 w[CPS][NG];
+  uint32_t s[CPS][NG];  // raw sign data: a 4-byte word per chunk, or one byte
+  uint4 xa[CPS];
+  uint4 xb[kM16 ? CPS : 1];
+};
+
+template <int NG, int CPS, bool kM16, bool kSignVec>
 __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& grp,
                                            const uint8_t* __restrict__ packed,
                                            const float* __restrict__ alpha, bool has_delta,
@@ -102,51 +129,81 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
     for (int e = 0; e < 4; ++e) acc_b[ng][e] = acc_s[ng][e] = 0.f;
 
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-  const int64_t n_sc = d_in / 128;
-  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
-    const int64_t kc0 = sc * 128;
-    uint4 wv[4][NG];
-    uint32_t sb[4][NG];
-    uint4 xa[4], xb[4];
+  using F = Frag<NG, CPS, kM16>;
+
+  auto load = [&](F& f, int64_t kc0) {
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
       if (wrow[ng] != nullptr) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) wv[j][ng] = ldg_stream_v4(wrow[ng] + kc0 + 32 * j + 8 * t);
+        for (int j = 0; j < CPS; ++j) f.w[j][ng] = ldg_stream_v4(wrow[ng] + kc0 + 32 * j + 8 * t);
         if (has_delta) {
           if (kSignVec) {
-            const uint4 s = ldg_v4(srow[ng] + kc0 / 8);
-            sb[0][ng] = (s.x >> (8 * t)) & 0xFFu;
-            sb[1][ng] = (s.y >> (8 * t)) & 0xFFu;
-            sb[2][ng] = (s.z >> (8 * t)) & 0xFFu;
-            sb[3][ng] = (s.w >> (8 * t)) & 0xFFu;
+            const uint4 v = ldg_v4(srow[ng] + kc0 / 8);
+            f.s[0][ng] = v.x;
+            f.s[1 % CPS][ng] = v.y;
+            f.s[2 % CPS][ng] = v.z;
+            f.s[3 % CPS][ng] = v.w;
           } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sb[j][ng] = __ldg(srow[ng] + kc0 / 8 + 4 * j + t);
+            for (int j = 0; j < CPS; ++j) f.s[j][ng] = __ldg(srow[ng] + kc0 / 8 + 4 * j + t);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sb[j][ng] = 0xFFu;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          wv[j][ng] = zero4;
-          sb[j][ng] = 0xFFu;
+        for (int j = 0; j < CPS; ++j) {
+          f.w[j][ng] = zero4;
+          f.s[j][ng] = 0u;
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      xa[j] = xra != nullptr ? ldg_v4(xra + kc0 + 32 * j + 8 * t) : zero4;
-      xb[j] = (kM16 && xrb != nullptr) ? ldg_v4(xrb + kc0 + 32 * j + 8 * t) : zero4;
+    for (int j = 0; j < CPS; ++j) {
+      f.xa[j] = xra != nullptr ? ldg_v4(xra + kc0 + 32 * j + 8 * t) : zero4;
+      if (kM16) f.xb[j] = xrb != nullptr ? ldg_v4(xrb + kc0 + 32 * j + 8 * t) : zero4;
     }
+  };
+  auto compute = [&](const F& f) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) chunk_mma<NG>(acc_b, acc_s, wv[j], sb[j], xa[j], xb[j], has_delta);
+    for (int j = 0; j < CPS; ++j) {
+      uint32_t sb[NG];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+        sb[ng] = kSignVec ? (f.s[j][ng] >> (8 * t)) & 0xFFu : f.s[j][ng];
+      chunk_mma<NG>(acc_b, acc_s, f.w[j], sb, f.xa[j], kM16 ? f.xb[kM16 ? j : 0] : zero4,
+                    has_delta);
+    }
+  };
+
+  const int64_t n_sc = d_in / (32 * CPS);
+  if constexpr (kSignVec) {
+    // Two super-chunks in flight per warp: the loads of the next one are
+    // issued before the products of the current one.
+    F f0, f1;
+    int64_t sc = warp;
+    if (sc < n_sc) load(f0, sc * 32 * CPS);
+    while (sc < n_sc) {
+      const int64_t sc1 = sc + kKW;
+      if (sc1 < n_sc) load(f1, sc1 * 32 * CPS);
+      compute(f0);
+      if (sc1 >= n_sc) break;
+      const int64_t sc2 = sc1 + kKW;
+      if (sc2 < n_sc) load(f0, sc2 * 32 * CPS);
+      compute(f1);
+      sc = sc2;
+    }
+  } else {
+    // Sign rows not 16-byte aligned: byte-wise sign loads, one super-chunk
+    // at a time.
+    for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+      F f;
+      load(f, sc * 32 * CPS);
+      compute(f);
+    }
   }
-  // Tail: 32-column chunks past the last full 128-column block.  d_in is a
+  // Tail: 32-column chunks past the last full super-chunk.  d_in is a
   // multiple of 8, so each thread's 8 columns are wholly inside or outside.
-  for (int64_t c32 = n_sc * 4 + warp; c32 * 32 < d_in; c32 += kKW) {
+  for (int64_t c32 = n_sc * CPS + warp; c32 * 32 < d_in; c32 += kKW) {
     const int64_t col = c32 * 32 + 8 * t;
     const bool ok = col < d_in;
     uint4 wv[NG];
@@ -208,10 +265,31 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
 }
 
 // Single variant: blockIdx.y (strided) picks 16 consecutive x rows.
+// Before waiting on the previous kernel in the stream, pull this CTA's slice
+// of W_base (and its sign rows) towards L2: weights stream from HBM while the
+// previous kernel drains, and the main loop then reads them from L2.
+template <int NG>
+__device__ __forceinline__ void prefetch_weights(const GemvArgs& p) {
+  const int64_t rows = 8 * NG;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * rows;
+  const int64_t n_rows = p.d_out - n0 < rows ? p.d_out - n0 : rows;
+  const int64_t row_lines = (p.d_in * 2 + 127) / 128;
+  for (int64_t i = threadIdx.x; i < n_rows * row_lines; i += blockDim.x) {
+    const int64_t r = i / row_lines, l = i - r * row_lines;
+    prefetch_l2(reinterpret_cast<const uint8_t*>(p.w + (n0 + r) * p.d_in) + 128 * l);
+  }
+  const int64_t sign_bytes = n_rows * (p.d_in / 8);
+  const uint8_t* s0 = p.packed + n0 * (p.d_in / 8);
+  for (int64_t i = threadIdx.x * 128; i < sign_bytes; i += blockDim.x * 128) prefetch_l2(s0 + i);
+}
+
 template <int NG, bool kM16, bool kSignVec>
 __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
   __shared__ float red[kKW * NG * 4 * 32];
   __shared__ RowGroup grp;
+  if (blockIdx.y == 0) prefetch_weights<NG>(p);
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
   for (int64_t c = blockIdx.y; c < n_chunks; c += gridDim.y) {
     if (threadIdx.x < kMaxGroupRows) {
@@ -220,7 +298,7 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
     }
     if (threadIdx.x == 0) grp.variant = 1;
     __syncthreads();
-    gemv_group<NG, kM16, kSignVec>(p, grp, p.packed, p.alpha, true, red);
+    gemv_group<NG, kCPS, kM16, kSignVec>(p, grp, p.packed, p.alpha, true, red);
   }
 }
 
@@ -232,6 +310,8 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
   __shared__ float red[kKW * NG * 4 * 32];
   __shared__ RowGroup grp;
   extern __shared__ int32_t dyn[];
+  griddep_launch_dependents();
+  griddep_wait();
   // dyn: [n_var+2] bucket counts | [n_var+2] bucket starts | [max_rows] rows
   const int nb = p.n_var + 1;
   int32_t* cnt = dyn;
@@ -293,9 +373,9 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
       const float* al = v > 0 ? p.alpha_table[v - 1] : nullptr;
       const bool vec = (p.d_in % 128 == 0) && ((reinterpret_cast<uintptr_t>(pk) & 15u) == 0);
       if (vec)
-        gemv_group<NG, true, true>(p, grp, pk, al, v > 0, red);
+        gemv_group<NG, kCPS, true, true>(p, grp, pk, al, v > 0, red);
       else
-        gemv_group<NG, true, false>(p, grp, pk, al, v > 0, red);
+        gemv_group<NG, kCPS, true, false>(p, grp, pk, al, v > 0, red);
     }
   }
 }
@@ -307,15 +387,12 @@ cudaError_t launch_single(const GemvArgs& p, bool sign_vec, cudaStream_t stream)
   dim3 grid(static_cast<unsigned>(n_blocks),
             static_cast<unsigned>(n_chunks < 65535 ? n_chunks : 65535));
   const bool m16 = p.M > 8;
+  const dim3 block(kKW * 32);
   if (m16 && sign_vec)
-    gemv_single_kernel<NG, true, true><<<grid, kKW * 32, 0, stream>>>(p);
-  else if (m16)
-    gemv_single_kernel<NG, true, false><<<grid, kKW * 32, 0, stream>>>(p);
-  else if (sign_vec)
-    gemv_single_kernel<NG, false, true><<<grid, kKW * 32, 0, stream>>>(p);
-  else
-    gemv_single_kernel<NG, false, false><<<grid, kKW * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_pdl(gemv_single_kernel<NG, true, true>, grid, block, 0, stream, p);
+  if (m16) return launch_pdl(gemv_single_kernel<NG, true, false>, grid, block, 0, stream, p);
+  if (sign_vec) return launch_pdl(gemv_single_kernel<NG, false, true>, grid, block, 0, stream, p);
+  return launch_pdl(gemv_single_kernel<NG, false, false>, grid, block, 0, stream, p);
 }
 
 }  // namespace
@@ -327,12 +404,12 @@ size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows) {
 cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream) {
   const bool sign_vec = (p.d_in % 128 == 0) &&
                         (reinterpret_cast<uintptr_t>(p.packed) % 16 == 0);
-  return launch_single<2>(p, sign_vec, stream);
+  return launch_single<kNG>(p, sign_vec, stream);
 }
 
 cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream) {
   const size_t smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
-  const int64_t n_blocks = (p.d_out + 15) / 16;
+  const int64_t n_blocks = (p.d_out + 8 * kNG - 1) / (8 * kNG);
   dim3 grid(static_cast<unsigned>(n_blocks));
   // Raise the dynamic shared-memory limit only when a call needs more than
   // any earlier call on this device (so captured calls make no attribute call).
@@ -342,13 +419,12 @@ cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > 48 * 1024 && smem > smem_set[dev]) {
-    e = cudaFuncSetAttribute(gemv_grouped_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     smem_set[dev] = smem;
   }
-  gemv_grouped_kernel<2><<<grid, kKW * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gemv_grouped_kernel<kNG>, grid, dim3(kKW * 32), smem, stream, p);
 }
 
 }  // namespace bd

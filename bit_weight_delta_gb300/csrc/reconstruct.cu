@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     reconstruct_kernel(const uint16_t* __restrict__ w_base, const uint8_t* __restrict__ packed,
                        const float* __restrict__ alpha, int per_row, int64_t d_out,
                        int64_t d_in, uint16_t* __restrict__ w_out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t chunks = d_in / 8;
@@ -78,9 +80,8 @@ cudaError_t launch_reconstruct(const uint16_t* w_base, const uint8_t* packed, co
   const int64_t blocks_needed = (d_out + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
   const int grid = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-  reconstruct_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(w_base, packed, alpha,
-                                                              per_row ? 1 : 0, d_out, d_in, w_out);
-  return cudaGetLastError();
+  return launch_pdl(reconstruct_kernel, dim3(grid), dim3(kWarpsPerBlock * 32), 0, stream,
+                    w_base, packed, alpha, per_row ? 1 : 0, d_out, d_in, w_out);
 }
 
 }  // namespace bd
