@@ -20,9 +20,11 @@ __host__ __device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
   return z ^ (z >> 31);
 }
 
-// Uniform in (0, 1): 24 random bits, offset by half a step.
-__device__ __forceinline__ float u01(uint32_t bits24) {
-  return (static_cast<float>(bits24) + 0.5f) * (1.0f / 16777216.0f);
+// Uniform strictly inside (0, 1): 23 random bits, offset by half a step.  The
+// largest value, 1 - 2^-24, is exact in binary32 (with 24 bits the top value
+// would round up to 1.0 and the inverse CDFs below would reach log(0)).
+__device__ __forceinline__ float u01(uint32_t bits23) {
+  return (static_cast<float>(bits23) + 0.5f) * (1.0f / 8388608.0f);
 }
 
 __host__ __device__ __forceinline__ uint64_t key(uint64_t seed, uint64_t stream) {
@@ -32,8 +34,8 @@ __host__ __device__ __forceinline__ uint64_t key(uint64_t seed, uint64_t stream)
 // Standard normal for element i (one Box-Muller draw per element).
 __device__ __forceinline__ float normal_at(uint64_t k, uint64_t i) {
   const uint64_t r = splitmix64(k ^ (i * 0xD1B54A32D192ED03ull));
-  const float u1 = u01(static_cast<uint32_t>(r >> 40));
-  const float u2 = u01(static_cast<uint32_t>(r >> 8) & 0xFFFFFFu);
+  const float u1 = u01(static_cast<uint32_t>(r >> 41));
+  const float u2 = u01(static_cast<uint32_t>(r >> 8) & 0x7FFFFFu);
   float s, c;
   sincospif(2.0f * u2, &s, &c);
   return sqrtf(-2.0f * logf(u1)) * c;
@@ -42,7 +44,7 @@ __device__ __forceinline__ float normal_at(uint64_t k, uint64_t i) {
 // Laplace(0, b) for element i, inverse CDF.
 __device__ __forceinline__ float laplace_at(uint64_t k, uint64_t i, float b) {
   const uint64_t r = splitmix64(k ^ (i * 0xA0761D6478BD642Full));
-  const float u = u01(static_cast<uint32_t>(r >> 40)) - 0.5f;
+  const float u = u01(static_cast<uint32_t>(r >> 41)) - 0.5f;
   const float a = fabsf(u);
   const float mag = -b * logf(1.0f - 2.0f * a);
   return u < 0.f ? -mag : mag;
