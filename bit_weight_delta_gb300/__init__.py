@@ -32,7 +32,7 @@ EXPORTED = (
     "bitdelta_packed_bytes", "bitdelta_compress_workspace_bytes", "bitdelta_compress",
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
-    "bitdelta_status_string",
+    "bitdelta_status_string", "bitdelta_compress_noalloc",
 )
 
 
@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_compress_workspace_bytes.restype = sz
     lib.bitdelta_compress.argtypes = [p, p, i64, i64, st, p, p, p, sz, p]
     lib.bitdelta_compress.restype = st
+    lib.bitdelta_compress_noalloc.argtypes = [p, p, i64, i64, st, p, p, p]
+    lib.bitdelta_compress_noalloc.restype = st
     lib.bitdelta_reconstruct.argtypes = [p, p, p, st, i64, i64, p, p]
     lib.bitdelta_reconstruct.restype = st
     lib.bitdelta_linear.argtypes = [p, i64, p, p, p, st, i64, i64, p, p]
@@ -145,6 +147,21 @@ def bitdelta_compress(w_base, w_ft, per_row: bool = True, packed_out=None, alpha
     _check("bitdelta_compress", load().bitdelta_compress(
         _ptr(w_base), _ptr(w_ft), d_out, d_in, _mode(per_row), _ptr(packed_out), _ptr(alpha_out),
         _ptr(workspace), ws_bytes, _stream(stream)))
+    return packed_out, alpha_out
+
+
+def bitdelta_compress_noalloc(w_base, w_ft, per_row: bool, packed_out, alpha_out, stream=None):
+    """bitdelta_compress for callers that cannot allocate device memory: the
+    outputs are passed in and the library allocates nothing (per-matrix α
+    uses a fixed device array, d_out <= 65536).  Returns (packed, alpha)."""
+    _dev(w_base, torch.bfloat16, "w_base")
+    _dev(w_ft, torch.bfloat16, "w_ft")
+    _dev(packed_out, torch.uint8, "packed_out")
+    _dev(alpha_out, torch.float32, "alpha_out")
+    d_out, d_in = w_base.shape
+    _check("bitdelta_compress_noalloc", load().bitdelta_compress_noalloc(
+        _ptr(w_base), _ptr(w_ft), d_out, d_in, _mode(per_row), _ptr(packed_out),
+        _ptr(alpha_out), _stream(stream)))
     return packed_out, alpha_out
 
 

@@ -112,6 +112,19 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
 
 }  // namespace
 
+namespace bd {
+// Error word, wait limit and SM count of the current device, for entry points
+// defined outside this file.  Returns a bd_status.
+int current_device_context(DevCtx* ctx, int* num_sms) {
+  DeviceState* dev = nullptr;
+  const bd_status st = current_device(&dev);
+  if (st != BD_OK) return st;
+  *ctx = make_ctx(dev);
+  *num_sms = dev->num_sms;
+  return BD_OK;
+}
+}  // namespace bd
+
 extern "C" {
 
 size_t bitdelta_packed_bytes(int64_t d_out, int64_t d_in) {

@@ -18,7 +18,9 @@
 // fixed order in the last block to finish, so the result does not depend on
 // scheduling.
 #include <cstdint>
+#include <mutex>
 
+#include "bitdelta.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -169,3 +171,69 @@ cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_
 }
 
 }  // namespace bd
+
+// ------------------------------------------------------------------ no-alloc
+
+// Fixed scratch for bitdelta_compress_noalloc: a 256-byte slot for the
+// completion counter, then one fp64 row total per output row.  Every GPU that
+// loads the library keeps this array for the life of the process.
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = 65536;
+constexpr size_t kNoAllocScratchBytes = 256 + 8 * static_cast<size_t>(kNoAllocMaxRows);
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device, looked up once per device
+// with that device current (the host-side symbol is not a device address).
+uint8_t* g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+
+bd_status noalloc_scratch(uint8_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return BD_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return BD_OK;
+}
+
+}  // namespace
+
+extern "C" bd_status bitdelta_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft,
+                                               int64_t d_out, int64_t d_in, bd_alpha_mode mode,
+                                               uint8_t* packed_out, float* alpha_out,
+                                               bd_stream_t stream) {
+  if (!w_base || !w_ft || !packed_out || !alpha_out) return BD_ERR_INVALID_ARG;
+  if (mode != BD_ALPHA_PER_MATRIX && mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+  if (d_out < 1 || d_in < 1) return BD_ERR_INVALID_ARG;
+  if (d_in % 8 != 0 || d_in > (int64_t{1} << 40) || d_out > (int64_t{1} << 62) / d_in)
+    return BD_ERR_UNSUPPORTED_SHAPE;
+  if (mode == BD_ALPHA_PER_MATRIX && d_out > kNoAllocMaxRows) return BD_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(w_base) % 16 || reinterpret_cast<uintptr_t>(w_ft) % 16 ||
+      reinterpret_cast<uintptr_t>(alpha_out) % 4)
+    return BD_ERR_MISALIGNED;
+  bd::DevCtx ctx;
+  int num_sms = 0;
+  bd_status st = static_cast<bd_status>(bd::current_device_context(&ctx, &num_sms));
+  if (st != BD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* counter = nullptr;
+  double* row_sums = nullptr;
+  if (mode == BD_ALPHA_PER_MATRIX) {
+    uint8_t* scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != BD_OK) return st;
+    counter = reinterpret_cast<unsigned int*>(scratch);
+    row_sums = reinterpret_cast<double*>(scratch + 256);
+    // the counter must start at zero; the row totals are all overwritten
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess) return BD_ERR_CUDA;
+  }
+  return bd::launch_compress(w_base, w_ft, d_out, d_in, mode == BD_ALPHA_PER_ROW, packed_out,
+                             alpha_out, row_sums, counter, num_sms, s, ctx) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}

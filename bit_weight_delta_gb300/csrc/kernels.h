@@ -29,6 +29,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Current device's error word, wait limit and SM count (a bd_status code).
+int current_device_context(DevCtx* ctx, int* num_sms);
+
 cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
                             int64_t d_in, bool per_row, uint8_t* packed, float* alpha,
                             double* row_sums, unsigned int* done_counter, int num_sms,

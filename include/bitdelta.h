@@ -133,6 +133,31 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
                                   bd_alpha_mode mode, int64_t d_out, int64_t d_in, uint16_t* y,
                                   bd_stream_t stream);
 
+/*
+ * bitdelta_compress without a caller workspace.  (The page has no counterpart:
+ * this entry point exists for callers of this library, not for the method.)
+ * It is meant for callers that cannot allocate device memory at the point
+ * where they compress: for example a plug-in that only receives finished
+ * device buffers from a host framework and has no allocator handle, or a
+ * serving loop whose device memory is planned up front and where a
+ * cudaMalloc could block on a device-wide synchronisation or fail under
+ * memory pressure.  Same arguments and results as bitdelta_compress minus the
+ * workspace; it allocates nothing.
+ *   - Per-matrix α uses a fixed scratch array in the library's device memory
+ *     (256 B + 8 B per output row), so d_out is limited to 65536 rows in
+ *     BD_ALPHA_PER_MATRIX mode; larger d_out returns BD_ERR_WORKSPACE and
+ *     launches nothing.  Per-row α needs no scratch and has no such limit.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's
+ *     contents (the call clears its completion counter itself): calls that can
+ *     overlap on the GPU (different streams without ordering) race and give
+ *     wrong α.  Serialise them.
+ */
+bd_status bitdelta_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
+                                    int64_t d_in, bd_alpha_mode mode, uint8_t* packed_out,
+                                    float* alpha_out, bd_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device error word
  * of the current device (BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_DEVICE_BOUNDS),
  * or BD_ERR_CUDA if the synchronisation itself failed. */
