@@ -54,14 +54,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test for completion of the phase with `parity`; a thread whose phase is not
+// complete yet is suspended (no issue slots) until it completes or until
+// roughly `suspend_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 0) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return done != 0;
 }
@@ -69,21 +73,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase of `bar` with the given parity.  Returns true on
 // completion.  Returns false when the time limit passes (the timeout is
 // recorded in the error word and *abort is raised) or when another role has
-// already raised *abort.  Never spins without limit.
+// already raised *abort.  Never spins without limit: each try suspends the
+// thread for at most 20 us, and the limit is counted in SM clock cycles (two
+// per nanosecond, so at clocks below 2 GHz the real bound is longer).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const DevCtx& ctx,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t polls = 0;
+  const long long t0 = clock64();
+  const long long limit = static_cast<long long>(ctx.wait_limit_ns) * 2;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++polls & 31u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > ctx.wait_limit_ns) {
-        record_error(ctx, kErrTimeout);
-        if (abort != nullptr) *abort = 1;
-        return false;
-      }
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (clock64() - t0 > limit) {
+      record_error(ctx, kErrTimeout);
+      if (abort != nullptr) *abort = 1;
+      return false;
     }
   }
 }
