@@ -195,11 +195,9 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
   const bd::DevCtx ctx = make_ctx(dev);
 
   if (M > kDecodeMaxRows && tc_shape_ok(M, d_out, d_in) && aligned(packed, 16)) {
-    // Cluster size: CTAs that share one W_eff tile over consecutive token tiles.
     const int64_t t_total = (M + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens();
-    const int csize = t_total >= 4 ? 4 : (t_total >= 2 ? 2 : 1);
     CUtensorMap tw, tx;
-    if (make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows() / csize) &&
+    if (make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
         make_tmap_bf16(&tx, x, M, d_in, 64, bd::gemm_block_tokens())) {
       bd::GemmArgs g{};
       g.M = M;
@@ -210,9 +208,10 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
       g.per_row = mode == BD_ALPHA_PER_ROW;
       g.y = y;
       g.ctx = ctx;
-      const int64_t ctiles = ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
-                             ((t_total + csize - 1) / csize);
-      return from_cuda(bd::launch_gemm(g, tw, tx, csize, ctiles, s));
+      const int64_t tiles =
+          ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) * t_total;
+      const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+      return from_cuda(bd::launch_gemm(g, tw, tx, grid, s));
     }
   }
   bd::GemvArgs a{};
@@ -255,11 +254,9 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
   // kernel takes every segment the tensor-core kernel does not.
   bool use_tc = max_seg_len > kDecodeMaxRows && tc_shape_ok(M_total, d_out, d_in) &&
                 n_seg <= bd::kGemmMaxSegs;
-  // Long segments of two or more token tiles share W_eff across a cluster of 2.
-  const int csize = max_seg_len > bd::gemm_block_tokens() ? 2 : 1;
   CUtensorMap tw, tx;
   if (use_tc)
-    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows() / csize) &&
+    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
              make_tmap_bf16(&tx, x, M_total, d_in, 64, bd::gemm_block_tokens());
   const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
 
@@ -278,10 +275,11 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
     g.packed_table = packed_table;
     g.alpha_table = alpha_table;
     g.ctx = ctx;
-    const int64_t ctiles =
-        ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
-        ((M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() / csize + n_seg);
-    if ((st = from_cuda(bd::launch_gemm(g, tw, tx, csize, ctiles, s))) != BD_OK) return st;
+    const int64_t tiles = ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
+                          ((M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() +
+                           n_seg);
+    const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+    if ((st = from_cuda(bd::launch_gemm(g, tw, tx, grid, s))) != BD_OK) return st;
   }
 
   const int64_t short_rows_bound =

@@ -83,11 +83,9 @@ struct GemmArgs {
 constexpr int kGemmMaxSegs = 1024;
 int gemm_block_rows();    // d_out rows per tile
 int gemm_block_tokens();  // x rows per tile
-// cluster_size C in {1, 2, 4}: CTAs sharing one W_eff tile (tmap_w's box has
-// gemm_block_rows()/C rows); cluster_tiles_bound: upper bound on the number of
-// cluster tiles (caps the number of clusters launched).
+// grid: persistent CTAs (at most one per SM; each loops over tiles).
 cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
-                        int cluster_size, int64_t cluster_tiles_bound, cudaStream_t stream);
+                        int grid, cudaStream_t stream);
 
 // Test hook: one CTA waiting on an mbarrier nothing completes.
 cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream);

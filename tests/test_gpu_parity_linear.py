@@ -100,6 +100,25 @@ def test_tensor_core_many_tiles():
         assert_linear_close(y[m], oracle.linear(x[m:m + 1], wb, packed, alpha, True)[0])
 
 
+@pytest.mark.parametrize("d_in", [128, 384, 640])
+def test_tensor_core_k_blocks_and_tile_wrap(d_in):
+    """K-block counts of 2, 6 and 10 (not multiples of the transform's
+    warpgroup count, so a warpgroup's stages cross tile boundaries at varying
+    k-blocks) with 2 x 80 tiles: more tiles than SMs, some CTAs take two."""
+    d_out, M = 128 * 80, 300
+    wb, packed, alpha = _layer(8, d_out, d_in, True)
+    x = synth.activations(8, M, d_in)
+    y = bf16_values(_run(x, wb, packed, alpha, True))
+    assert bd.bitdelta_check_error() == 0
+    rng = np.random.default_rng(d_in)
+    mi = rng.integers(0, M, 3000)
+    ni = rng.integers(0, d_out, 3000)
+    assert_linear_close(y[mi, ni], oracle.linear_at(x, wb, packed, alpha, True, mi, ni))
+    for m in (0, 255, 256, 299):
+        assert_linear_close(y[m], oracle.linear(x[m:m + 1], wb, packed, alpha, True)[0],
+                            f"row {m}")
+
+
 def test_alpha_zero_is_plain_gemm():
     """α = 0: the fused linear is x·W_baseᵀ; compare with torch's cuBLAS GEMM."""
     import torch
