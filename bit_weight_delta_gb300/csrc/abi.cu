@@ -90,7 +90,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 [rows, cols] as a 2D tensor with a (box_cols x box_rows)
-// box in the 128-byte swizzle; out-of-range elements read as zero.
+// box; box_cols = 64 (32) uses the 128-byte (64-byte) swizzle.  Out-of-range
+// elements read as zero.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
                     uint32_t box_cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -101,7 +102,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t co
   cuuint32_t estr[2] = {1, 1};
   std::memset(map, 0, sizeof(*map));
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -197,8 +199,8 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
   if (M > kDecodeMaxRows && tc_shape_ok(M, d_out, d_in) && aligned(packed, 16)) {
     const int64_t t_total = (M + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens();
     CUtensorMap tw, tx;
-    if (make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
-        make_tmap_bf16(&tx, x, M, d_in, 64, bd::gemm_block_tokens())) {
+    if (make_tmap_bf16(&tw, w_base, d_out, d_in, bd::gemm_block_k(), bd::gemm_block_rows()) &&
+        make_tmap_bf16(&tx, x, M, d_in, bd::gemm_block_k(), bd::gemm_block_tokens())) {
       bd::GemmArgs g{};
       g.M = M;
       g.d_out = d_out;
@@ -256,8 +258,8 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
                 n_seg <= bd::kGemmMaxSegs;
   CUtensorMap tw, tx;
   if (use_tc)
-    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, 64, bd::gemm_block_rows()) &&
-             make_tmap_bf16(&tx, x, M_total, d_in, 64, bd::gemm_block_tokens());
+    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, bd::gemm_block_k(), bd::gemm_block_rows()) &&
+             make_tmap_bf16(&tx, x, M_total, d_in, bd::gemm_block_k(), bd::gemm_block_tokens());
   const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
 
   if (use_tc) {

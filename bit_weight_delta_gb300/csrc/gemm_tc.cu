@@ -45,16 +45,27 @@ namespace {
 
 constexpr int kBM = 128;  // d_out rows per tile
 constexpr int kBN = 256;  // tokens per tile
-constexpr int kBK = 64;   // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB of W_base per stage
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KB of x per stage
-constexpr int kPrefetch = 2;            // sign/α prefetch distance (own stages)
-constexpr int kRing = kPrefetch + 2;    // private ring slots per thread
-constexpr int kDCols = kBN;             // accumulator columns
-constexpr int kACol0 = kDCols;          // first column of the A slots
-constexpr int kAColsPerStage = kBK / 2;  // 64 bf16 per row = 32 columns
-constexpr int kTmemCols = 512;          // D (256) + 4 A slots (128), power of two
+#ifndef BD_GEMM_BK
+#define BD_GEMM_BK 64
+#endif
+// K per stage: one row of a swizzle atom, 128 bytes of bf16 (BK = 64, 128-byte
+// swizzle) or 64 bytes (BK = 32, 64-byte swizzle).  The ring holds 192 KB
+// either way.  Measured on 8192-wide projections at 2048 tokens, BK = 64 is
+// about 13% faster: the per-stage handoffs cost more than the deeper ring gains.
+constexpr int kBK = BD_GEMM_BK;
+static_assert(kBK == 32 || kBK == 64, "BK is one 64- or 128-byte swizzle row");
+constexpr int kStages = 256 / kBK;       // 8 stages of 24 KB or 4 of 48 KB
+constexpr int kABytes = kBM * kBK * 2;   // W_base per stage
+constexpr int kBBytes = kBN * kBK * 2;   // x per stage
+constexpr int kChunks = kBK / 8;         // 16-byte chunks per W row per stage
+constexpr int kSwzShift = kBK == 64 ? 0 : 1;  // row bits that select the chunk XOR
+constexpr int kSignBytes = kBK / 8;      // packed sign bytes per row per stage
+constexpr int kPrefetch = kBK == 64 ? 2 : 4;  // sign/α prefetch distance (own stages)
+constexpr int kRing = kPrefetch + 2;     // private ring slots per thread
+constexpr int kDCols = kBN;              // accumulator columns
+constexpr int kACol0 = kDCols;           // first column of the A slots
+constexpr int kAColsPerStage = kBK / 2;  // two bf16 per 32-bit column
+constexpr int kTmemCols = 512;           // D (256) + A slots (128), power of two
 #ifndef BD_GEMM_XF_GROUPS
 #define BD_GEMM_XF_GROUPS 2
 #endif
@@ -72,7 +83,7 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 // Shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128][8] B
+constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128] x 8 B
 constexpr int kOffAlpha = kOffSign + kXfGroups * kRing * kBM * 8;  // [G][kRing][128] floats
 constexpr int kOffBar = kOffAlpha + kXfGroups * kRing * kBM * 4;
 constexpr int kNumBars = 3 * kStages + 2 + 1;
@@ -123,9 +134,27 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs& p, int64_t t, int64_t t_
   return tl;
 }
 
-// ±α by the sign bit at `col` of `byte` (bit 1 -> +α); neg_alpha = α | sign.
-__device__ __forceinline__ float signed_alpha(uint32_t byte, int col, uint32_t neg_alpha) {
-  return __uint_as_float(neg_alpha ^ ((byte << (31 - col)) & 0x80000000u));
+// Sign-flip mask of one bf16 pair: bit 15 (the low element, column 2j of the
+// chunk) and bit 31 (the high element, column 2j+1) are set where the sign
+// bit is 0 (s = -1).  nb = the chunk's inverted sign byte (8 bits); the
+// multiply places nb bit 2j at bit 15 and bit 2j+1 at bit 31 (the two partial
+// products do not overlap, so no carry reaches either bit).
+template <int J>
+__device__ __forceinline__ uint32_t pair_flip_mask(uint32_t nb) {
+  return (nb * (0x40008000u >> (2 * J))) & 0x80008000u;
+}
+
+// bf16x2_rne(fp32(w.lo) + a, fp32(w.hi) + a), one packed fp32x2 add.
+__device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t w, uint32_t a) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b64 x, y, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "add.rn.f32x2 d, x, y;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w << 16), "r"(w & 0xFFFF0000u), "r"(a));
+  return pack_bf16x2_rn(__uint_as_float(lo), __uint_as_float(hi));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i writes lane (base+i).
@@ -140,6 +169,24 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32)
+    tmem_st_32x32b_x32(taddr, r);
+  else
+    tmem_st_32x32b_x16(taddr, r);
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -282,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return moved;
     };
 
-    // Prefetch cursor: row r's 8 sign bytes (and α at the warpgroup's first
+    // Prefetch cursor: row r's sign bytes (and α at the warpgroup's first
     // stage of each tile) into private ring slot (own index) % kRing.  Each
     // thread later reads only what it copied itself.
     Cursor pf{0, 0, 0};
@@ -295,8 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* al = grouped ? p.alpha_table[pf_tl.variant - 1] : p.alpha;
         const int64_t row = pf_tl.n0 + r;
         uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
-        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & 7u) == 0) {
-          cp_async_8(dst, pk + row * row_bytes + static_cast<int64_t>(pf.kb) * 8);
+        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & (kSignBytes - 1)) == 0) {
+          const uint8_t* src = pk + row * row_bytes + static_cast<int64_t>(pf.kb) * kSignBytes;
+          if constexpr (kSignBytes == 8)
+            cp_async_8(dst, src);
+          else
+            cp_async_4(dst, src);
         } else {
           if (row < p.d_out && blockIdx.x == 0 && pf.kb < kXfGroups)
             record_error(p.ctx, kErrBounds);
@@ -316,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch_next();
-    uint32_t neg_alpha = 0x80000000u;
+    uint32_t alpha_bits = 0u;  // α of the current tile's rows (fp32 bits)
     Cursor cur{0, 0, 0};
     advance(cur, wg);
     Tile tl = cur.i < my_tiles ? my_tile(cur.i) : Tile{0, 0, 0, 0};
@@ -333,33 +384,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!ok) break;
       if (cur.kb < kXfGroups && tl.variant > 0)
-        neg_alpha = __float_as_uint(alpha_ring[slot * kBM + r]) | 0x80000000u;
+        alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       const bool has_delta = tl.variant > 0;
-      const uint2 sg = has_delta
-                           ? *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8)
-                           : make_uint2(0u, 0u);
-      const uint8_t* w_row = smem + kOffA + s * kABytes + r * 128;
-      uint32_t packed[32];
+      uint2 sg = make_uint2(0u, 0u);
+      if (has_delta) {
+        if constexpr (kSignBytes == 8)
+          sg = *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8);
+        else
+          sg.x = *reinterpret_cast<const uint32_t*>(sign_ring + (slot * kBM + r) * 8);
+      }
+      const uint8_t* w_row = smem + kOffA + s * kABytes + r * (kBK * 2);
+      const int swz = (r >> kSwzShift) & (kChunks - 1);
+      uint4 wv[kChunks];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        // logical 16-byte chunk c (columns 8c..8c+7) sits at physical c ^ (r & 7)
-        const uint4 w = *reinterpret_cast<const uint4*>(w_row + ((c ^ (r & 7)) << 4));
-        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-        const uint32_t byte = ((c < 4 ? sg.x : sg.y) >> (8 * (c & 3))) & 0xFFu;
+      for (int c = 0; c < kChunks; ++c) {
+        // logical 16-byte chunk c (columns 8c..8c+7) sits at physical chunk
+        // c ^ swz: the TMA's 128-byte (64-byte) swizzle XORs the chunk index
+        // with address bits 7-9 (7-8), i.e. with row bits 0-2 (1-2)
+        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
+      }
+      uint32_t packed[kBK / 2];
+      if (has_delta) {
+        // W + s·α = s·(s·W + α): flip W where s = -1 (exact), add α in fp32,
+        // round to bf16, flip back.  Round-to-nearest-even is symmetric, so
+        // this is bf16_rne(fp32(W) + s·α) up to the sign of an exact zero
+        // (which no product or sum of the MMA can tell apart).
+        const uint32_t nsx = ~sg.x, nsy = ~sg.y;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (has_delta) {
-            const float lo =
-                __fadd_rn(bf16lo_to_f32(in[j]), signed_alpha(byte, 2 * j, neg_alpha));
-            const float hi =
-                __fadd_rn(bf16hi_to_f32(in[j]), signed_alpha(byte, 2 * j + 1, neg_alpha));
-            packed[4 * c + j] = pack_bf16x2_rn(lo, hi);
-          } else {
-            packed[4 * c + j] = in[j];
-          }
+        for (int c = 0; c < kChunks; ++c) {
+          const uint32_t nb = ((c < 4 ? nsx : nsy) >> (8 * (c & 3))) & 0xFFu;
+          const uint32_t f0 = pair_flip_mask<0>(nb), f1 = pair_flip_mask<1>(nb);
+          const uint32_t f2 = pair_flip_mask<2>(nb), f3 = pair_flip_mask<3>(nb);
+          packed[4 * c + 0] = add_round_bf16x2(wv[c].x ^ f0, alpha_bits) ^ f0;
+          packed[4 * c + 1] = add_round_bf16x2(wv[c].y ^ f1, alpha_bits) ^ f1;
+          packed[4 * c + 2] = add_round_bf16x2(wv[c].z ^ f2, alpha_bits) ^ f2;
+          packed[4 * c + 3] = add_round_bf16x2(wv[c].w ^ f3, alpha_bits) ^ f3;
+        }
+      } else {
+        // base rows (grouped mode, variant 0): W_base unchanged
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          packed[4 * c + 0] = wv[c].x;
+          packed[4 * c + 1] = wv[c].y;
+          packed[4 * c + 2] = wv[c].z;
+          packed[4 * c + 3] = wv[c].w;
         }
       }
-      tmem_st_32x32b_x32(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
+      tmem_st_32x32b(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -465,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kACol0 + kAColsPerStage * s);
-          const uint64_t b_desc = sdesc_k_sw128(b_base + s * kBBytes);
+          const uint64_t b_desc = kBK == 64 ? sdesc_k_sw128(b_base + s * kBBytes)
+                                            : sdesc_k_sw64(b_base + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
@@ -496,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int gemm_block_rows() { return kBM; }
 int gemm_block_tokens() { return kBN; }
+int gemm_block_k() { return kBK; }
 
 cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                         int grid, cudaStream_t stream) {

@@ -83,6 +83,7 @@ struct GemmArgs {
 constexpr int kGemmMaxSegs = 1024;
 int gemm_block_rows();    // d_out rows per tile
 int gemm_block_tokens();  // x rows per tile
+int gemm_block_k();       // K per stage: 32 (64-byte swizzle) or 64 (128-byte swizzle)
 // grid: persistent CTAs (at most one per SM; each loops over tiles).
 cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                         int grid, cudaStream_t stream);
