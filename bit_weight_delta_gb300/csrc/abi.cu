@@ -112,6 +112,38 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
   return d_in % 128 == 0 && d_in < INT32_MAX && d_out < INT32_MAX && rows_x < INT32_MAX;
 }
 
+#ifndef BD_GEMM_PAIR
+#define BD_GEMM_PAIR 1
+#endif
+
+// Launch the tensor-core kernel on g (x has rows_x rows; at most
+// token_tiles_bound 256-token tiles per row tile).  The pair kernel
+// (cta_group::2, 256 output rows per tile) unless built with BD_GEMM_PAIR=0.
+// Returns false, launching nothing, when a tensor map cannot be encoded.
+bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t rows_x,
+               int64_t token_tiles_bound, int num_sms, cudaStream_t s, cudaError_t* err) {
+  CUtensorMap tw, tx;
+  if (BD_GEMM_PAIR) {
+    const int bk = bd::gemm_pair_block_k();
+    if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
+        !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_pair_x_rows()))
+      return false;
+    const int64_t pair_tiles = ((g.d_out + 2 * bd::gemm_block_rows() - 1) /
+                                (2 * bd::gemm_block_rows())) * token_tiles_bound;
+    *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, s);
+    return true;
+  }
+  const int bk = bd::gemm_block_k();
+  if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
+      !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_block_tokens()))
+    return false;
+  const int64_t tiles =
+      ((g.d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) * token_tiles_bound;
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  *err = bd::launch_gemm(g, tw, tx, grid, s);
+  return true;
+}
+
 }  // namespace
 
 namespace bd {
@@ -198,23 +230,17 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
 
   if (M > kDecodeMaxRows && tc_shape_ok(M, d_out, d_in) && aligned(packed, 16)) {
     const int64_t t_total = (M + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens();
-    CUtensorMap tw, tx;
-    if (make_tmap_bf16(&tw, w_base, d_out, d_in, bd::gemm_block_k(), bd::gemm_block_rows()) &&
-        make_tmap_bf16(&tx, x, M, d_in, bd::gemm_block_k(), bd::gemm_block_tokens())) {
-      bd::GemmArgs g{};
-      g.M = M;
-      g.d_out = d_out;
-      g.d_in = d_in;
-      g.packed = packed;
-      g.alpha = alpha;
-      g.per_row = mode == BD_ALPHA_PER_ROW;
-      g.y = y;
-      g.ctx = ctx;
-      const int64_t tiles =
-          ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) * t_total;
-      const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
-      return from_cuda(bd::launch_gemm(g, tw, tx, grid, s));
-    }
+    bd::GemmArgs g{};
+    g.M = M;
+    g.d_out = d_out;
+    g.d_in = d_in;
+    g.packed = packed;
+    g.alpha = alpha;
+    g.per_row = mode == BD_ALPHA_PER_ROW;
+    g.y = y;
+    g.ctx = ctx;
+    cudaError_t e = cudaSuccess;
+    if (launch_tc(g, w_base, x, M, t_total, dev->num_sms, s, &e)) return from_cuda(e);
   }
   bd::GemvArgs a{};
   a.x = x;
@@ -256,12 +282,6 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
   // kernel takes every segment the tensor-core kernel does not.
   bool use_tc = max_seg_len > kDecodeMaxRows && tc_shape_ok(M_total, d_out, d_in) &&
                 n_seg <= bd::kGemmMaxSegs;
-  CUtensorMap tw, tx;
-  if (use_tc)
-    use_tc = make_tmap_bf16(&tw, w_base, d_out, d_in, bd::gemm_block_k(), bd::gemm_block_rows()) &&
-             make_tmap_bf16(&tx, x, M_total, d_in, bd::gemm_block_k(), bd::gemm_block_tokens());
-  const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
-
   if (use_tc) {
     bd::GemmArgs g{};
     g.M = M_total;
@@ -273,16 +293,19 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
     g.seg_var = seg_variant;
     g.n_seg = n_seg;
     g.n_var = n_var;
-    g.max_short = short_limit;
+    g.max_short = static_cast<int32_t>(kDecodeMaxRows);
     g.packed_table = packed_table;
     g.alpha_table = alpha_table;
     g.ctx = ctx;
-    const int64_t tiles = ((d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
-                          ((M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() +
-                           n_seg);
-    const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
-    if ((st = from_cuda(bd::launch_gemm(g, tw, tx, grid, s))) != BD_OK) return st;
+    // token tiles over all segments <= total tiles of M_total + one ragged
+    // tile per segment
+    const int64_t token_tiles =
+        (M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() + n_seg;
+    cudaError_t e = cudaSuccess;
+    use_tc = launch_tc(g, w_base, x, M_total, token_tiles, dev->num_sms, s, &e);
+    if (use_tc && (st = from_cuda(e)) != BD_OK) return st;
   }
+  const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
 
   const int64_t short_rows_bound =
       use_tc ? (M_total < int64_t{n_seg} * kDecodeMaxRows ? M_total

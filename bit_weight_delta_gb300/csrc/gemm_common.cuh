@@ -1,0 +1,334 @@
+// gemm_common.cuh — pieces shared by the two prefill kernels (one CTA per
+// tile in gemm_tc.cu, CTA pairs in gemm_pair.cu): the tile schedule, the
+// W_eff transform arithmetic, tensor-memory stores, the A-from-TMEM MMA, and
+// the cluster primitives of the pair kernel.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bd {
+namespace gemm_detail {
+
+struct Tile {
+  int64_t n0;       // first output row (d_out) of the tile
+  int64_t tok0;     // first token (x row) of the tile
+  int64_t tok_end;  // rows [tok0, min(tok0 + BN, tok_end)) are outputs
+  int32_t variant;  // 0 = base (no delta)
+};
+
+// Tile t of the flat schedule: t = nt * t_total + j, output rows
+// [nt*BM, nt*BM + BM), token tile j.  Plain mode: token tiles of [0, M).
+// Grouped mode: token tiles of each long segment in turn; `prefix` is the
+// inclusive prefix sum of tiles per segment (prefix[0] = 0).
+template <int BM, int BN>
+__device__ __forceinline__ Tile tile_at(const GemmArgs& p, int64_t t, int64_t t_total,
+                                        const int32_t* seg_off, const int32_t* seg_var,
+                                        const int32_t* prefix) {
+  Tile tl;
+  const int64_t nt = t / t_total;
+  const int64_t j = t - nt * t_total;
+  tl.n0 = nt * BM;
+  if (seg_off == nullptr) {
+    tl.tok0 = j * BN;
+    tl.tok_end = p.M;
+    tl.variant = 1;
+  } else {
+    // largest s with prefix[s] <= j (prefix is non-decreasing, prefix[0] = 0)
+    int lo = 0, hi = p.n_seg;  // invariant: prefix[lo] <= j < prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= j)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    tl.tok0 = seg_off[lo] + (j - prefix[lo]) * BN;
+    tl.tok_end = seg_off[lo + 1];
+    tl.variant = seg_var[lo];
+  }
+  return tl;
+}
+
+// Grouped mode set-up, run by every thread of the CTA: copy the segment table
+// to shared memory, validate it (one malformed entry rejects the whole table:
+// no tiles at all, error word set), and build the prefix sum of token tiles
+// (of BN rows) over the long segments.  Returns the total number of token
+// tiles through *t_total (written by warp 0, lane 0; visible after the
+// caller's next __syncthreads).
+template <int BN>
+__device__ __forceinline__ void load_segments(const GemmArgs& p, int32_t* s_seg_off,
+                                              int32_t* s_seg_var, int32_t* s_prefix,
+                                              int64_t* t_total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int s = threadIdx.x; s <= p.n_seg; s += blockDim.x) s_seg_off[s] = __ldg(p.seg_off + s);
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) s_seg_var[s] = __ldg(p.seg_var + s);
+  __syncthreads();
+  int bad_local = 0;
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+    const int32_t a = s_seg_off[s], b = s_seg_off[s + 1], v = s_seg_var[s];
+    bad_local |= (a < 0 || b < a || b > p.M || v < 0 || v > p.n_var) ? 1 : 0;
+  }
+  const bool table_bad = __syncthreads_or(bad_local) != 0;
+  if (table_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
+  for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+    const int32_t len = table_bad ? 0 : s_seg_off[s + 1] - s_seg_off[s];
+    s_prefix[s + 1] = len > p.max_short ? (len + BN - 1) / BN : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive scan of the tile counts
+    int32_t carry = 0;
+    if (lane == 0) s_prefix[0] = 0;
+    for (int base = 0; base < p.n_seg; base += 32) {
+      const int s = base + lane;
+      int32_t v = s < p.n_seg ? s_prefix[s + 1] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (s < p.n_seg) s_prefix[s + 1] = carry + v;
+      carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+    }
+    if (lane == 0) *t_total = carry;
+  }
+}
+
+// ------------------------------------------------------------------ W_eff
+
+// Sign-flip mask of one bf16 pair: bit 15 (the low element, column 2j of the
+// chunk) and bit 31 (the high element, column 2j+1) are set where the sign
+// bit is 0 (s = -1).  nb = the chunk's inverted sign byte (8 bits); the
+// multiply places nb bit 2j at bit 15 and bit 2j+1 at bit 31 (the two partial
+// products do not overlap, so no carry reaches either bit).
+template <int J>
+__device__ __forceinline__ uint32_t pair_flip_mask(uint32_t nb) {
+  return (nb * (0x40008000u >> (2 * J))) & 0x80008000u;
+}
+
+// bf16x2_rne(fp32(w.lo) + a, fp32(w.hi) + a), one packed fp32x2 add.
+__device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t w, uint32_t a) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b64 x, y, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "add.rn.f32x2 d, x, y;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w << 16), "r"(w & 0xFFFF0000u), "r"(a));
+  return pack_bf16x2_rn(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+// W_eff of one row's 8·C columns held as C 16-byte chunks of bf16 W_base:
+// W + s·α = s·(s·W + α).  The sign flip of W is exact and round-to-nearest-
+// even is symmetric, so flipping W where s = -1, adding α in fp32, rounding
+// to bf16 and flipping back gives bf16_rne(fp32(W) + s·α) (up to the sign of
+// an exact zero, which no product or sum of the MMA can tell apart).
+// sg: the row's sign bits for these columns (bit 1 = +1), 8 per chunk.
+template <int C>
+__device__ __forceinline__ void weff_chunks(const uint4 (&wv)[C], uint2 sg, uint32_t alpha_bits,
+                                            uint32_t (&packed)[4 * C]) {
+  const uint32_t nsx = ~sg.x, nsy = ~sg.y;
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const uint32_t nb = ((c < 4 ? nsx : nsy) >> (8 * (c & 3))) & 0xFFu;
+    const uint32_t f0 = pair_flip_mask<0>(nb), f1 = pair_flip_mask<1>(nb);
+    const uint32_t f2 = pair_flip_mask<2>(nb), f3 = pair_flip_mask<3>(nb);
+    packed[4 * c + 0] = add_round_bf16x2(wv[c].x ^ f0, alpha_bits) ^ f0;
+    packed[4 * c + 1] = add_round_bf16x2(wv[c].y ^ f1, alpha_bits) ^ f1;
+    packed[4 * c + 2] = add_round_bf16x2(wv[c].z ^ f2, alpha_bits) ^ f2;
+    packed[4 * c + 3] = add_round_bf16x2(wv[c].w ^ f3, alpha_bits) ^ f3;
+  }
+}
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t bf16_rn(float f) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+// ------------------------------------------------------------------ TMEM
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i writes lane (base+i).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32)
+    tmem_st_32x32b_x32(taddr, r);
+  else
+    tmem_st_32x32b_x16(taddr, r);
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Epilogue of one warp: its 32 accumulator lanes (lane = output row n, which
+// is this thread's row) x the tile's token columns (column c = token
+// tok0 + c, c < BN), rounded to bf16 and stored to y[tok][n] (row-major
+// [M, d_out]).  Tokens at or past tok_end and rows at or past d_out are not
+// stored.  taddr: TMEM address of the warp's lane quarter, column 0.
+template <int BN>
+__device__ __forceinline__ void store_acc_rows(uint32_t taddr, uint16_t* y, int64_t d_out,
+                                               int64_t n, int64_t tok0, int64_t tok_end) {
+  const int64_t span = tok_end - tok0;
+  const int cols = span <= 0 ? 0 : (span < BN ? static_cast<int>(span) : BN);
+  const bool n_ok = n < d_out;
+  uint16_t* yp = y + tok0 * d_out + n;
+#pragma unroll 1
+  for (int c = 0; c < cols; c += 32) {
+    uint32_t rr[32];
+    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), rr);
+    tmem_ld_wait();
+    if (n_ok) {
+      uint16_t* q = yp;
+      if (cols - c >= 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          *q = bf16_rn(__uint_as_float(rr[j]));
+          q += d_out;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < cols - c) *q = bf16_rn(__uint_as_float(rr[j]));
+          q += d_out;
+        }
+      }
+    }
+    yp += 32 * d_out;
+  }
+}
+
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ, kind::f16 (bf16 inputs, fp32 accumulate).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ CTA pairs
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the variable at `local_smem_addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by cluster address (possibly the other CTA's),
+// with the instruction's default ordering.  A release at cluster scope here
+// put a full memory barrier on every transform stage (ncu: 22% of the pair
+// kernel's warp samples stalled on it); what the consumer needs from these
+// arrivals is ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync
+// (tensor memory) and by the arriving thread's own acquire of the TMA barrier.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait (acquire at cluster scope) on a barrier that the other CTA of
+// the pair, or its MMAs, arrive on.  Same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const DevCtx& ctx, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+  const long long t0 = clock64();
+  const long long limit = static_cast<long long>(ctx.wait_limit_ns) * 2;
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (clock64() - t0 > limit) {
+      record_error(ctx, kErrTimeout);
+      if (abort != nullptr) *abort = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Pair forms of the tcgen05 instructions (every tcgen05 instruction of a
+// kernel that has a CTA-group qualifier must use the same group).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (+)= A · Bᵀ over the pair: M = 256 (128 rows of A and D in each CTA's
+// tensor memory), B's N rows split in halves, rank 0's half first, each in
+// its own CTA's shared memory at the same offset.  Issued by rank 0 only.
+__device__ __forceinline__ void umma_bf16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem,
+                                                      uint64_t b_desc, uint32_t idesc,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` (same offset) in both CTAs of the pair when the MMAs this
+// thread issued so far complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+}  // namespace gemm_detail
+}  // namespace bd

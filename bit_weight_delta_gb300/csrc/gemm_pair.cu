@@ -1,0 +1,413 @@
+// gemm_pair.cu — fused BitDelta linear for many rows (prefill) on pairs of
+// CTAs sharing one tcgen05 MMA (cta_group::2).
+//
+// Page "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "Serving architecture": the fused kernel reads the base weight and the delta
+// bits, builds the effective weight on chip — never the whole W_eff in HBM —
+// and multiplies in the same pass (conceptual fused_bitdelta_linear:
+// F.linear(x, W_base + α·unpack(bits))).
+//
+// Pair tile: 256 output rows x 256 tokens x 64 K per stage.  CTA rank r of the
+// pair owns output rows n0 + 128r .. +127: it loads those W_base rows, builds
+// their W_eff in its own tensor memory (the MMA's A operand) and holds their
+// fp32 accumulator (128 lanes x 256 token columns).  Each CTA loads half of
+// the x tile (tokens tok0 + 128r .. +127, the MMA's B operand, split in N).
+// Rank 0 issues one 256x256x16 MMA that reads both CTAs' operands.  Against
+// the one-CTA kernel, x moves half the bytes per SM through L2 and shared
+// memory for the same FLOPs, and the ring holds six 32 KB stages.
+//
+// Warp roles per CTA (448 threads, one CTA per SM, persistent over tiles):
+//   warps 0-7   transform: two warpgroups take the stages in turn; thread i
+//               of a warpgroup owns W row i (TMEM lane i), forms 64 W_eff
+//               values per stage and tcgen05.st's them to the stage's A
+//               slot, then its warp arrives on rank 0's xform barrier.
+//   warps 8-11  epilogue: tcgen05.ld this CTA's accumulator, store bf16 y.
+//   warp 12     TMA producer for this CTA's W_base rows and half of x.
+//   warp 13     rank 0: MMA issuer; rank 1: waits for the pair's last MMA.
+// Barriers: full[s] (TMA -> transform, local), xform[s] (both CTAs'
+// transforms -> rank 0's MMA), empty[s] and accfull (rank 0's MMA commits,
+// multicast to both CTAs), accempty (both CTAs' epilogues -> rank 0).  Every
+// wait is bounded; TMEM is released on every exit path.
+#include <cstdint>
+
+#include "gemm_common.cuh"
+
+namespace bd {
+namespace {
+using namespace gemm_detail;
+
+constexpr int kBM = 128;            // output rows per CTA
+constexpr int kPairM = 2 * kBM;     // output rows per pair tile (UMMA M)
+constexpr int kBN = 256;            // tokens per pair tile (UMMA N)
+constexpr int kHalfN = kBN / 2;     // tokens loaded by each CTA
+constexpr int kBK = 64;             // K per stage: one 128-byte swizzle row
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;     // 16 KB of W_base per stage
+constexpr int kBBytes = kHalfN * kBK * 2;  // 16 KB of x per stage
+constexpr int kChunks = kBK / 8;           // 16-byte chunks per W row per stage
+constexpr int kPrefetch = 2;               // sign/α prefetch distance (own stages)
+constexpr int kRing = kPrefetch + 2;       // private ring slots per thread
+constexpr int kDCols = kBN;                // accumulator columns
+constexpr int kACol0 = kDCols;             // first column of the A slots
+constexpr int kAColsPerStage = kBK / 2;    // 64 bf16 per row = 32 columns
+constexpr int kTmemCols = 512;             // D (256) + 6 A slots (192), power of two
+constexpr int kXfGroups = 2;
+constexpr int kXfWarps = 4 * kXfGroups;
+constexpr int kEpiWarp0 = kXfWarps;
+constexpr int kTmaWarp = kEpiWarp0 + 4;
+constexpr int kMmaWarp = kTmaWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start a warpgroup");
+static_assert(kACol0 + kStages * kAColsPerStage <= kTmemCols, "tensor memory budget");
+static_assert(kXfGroups <= kStages, "a warpgroup's stages must not alias in the ring");
+constexpr uint32_t kIdesc = idesc_bf16_f32(kPairM, kBN);
+constexpr uint32_t kXformArrivals = 2 * 4;   // 4 transform warps per stage, both CTAs
+constexpr uint32_t kAccEmptyArrivals = 2 * 4;  // 4 epilogue warps, both CTAs
+
+// Shared memory layout (offsets from a 1024-byte aligned base; identical in
+// both CTAs, so one offset names the same buffer in either).
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128] x 8 B
+constexpr int kOffAlpha = kOffSign + kXfGroups * kRing * kBM * 8;  // [G][kRing][128] floats
+constexpr int kOffBar = kOffAlpha + kXfGroups * kRing * kBM * 4;
+constexpr int kNumBars = 3 * kStages + 3;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, counts
+constexpr int kOffSeg = kOffMisc + 64;            // grouped-mode tables
+constexpr int kSegBytes = (3 * kGemmMaxSegs + 2) * 4;
+constexpr int kSmemBytes = kOffSeg + kSegBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort;
+  int64_t t_total;  // token tiles over all segments
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    bitdelta_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                              const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full_bar = bars;                 // own TMA -> own transform
+  uint64_t* xform_bar = bars + kStages;      // both transforms -> rank 0's MMA (rank 0 only)
+  uint64_t* empty_bar = bars + 2 * kStages;  // rank 0's MMA -> both TMA producers
+  uint64_t* accfull_bar = bars + 3 * kStages;
+  uint64_t* accempty_bar = accfull_bar + 1;  // both epilogues -> rank 0's MMA (rank 0 only)
+  uint64_t* drain_bar = accempty_bar + 1;
+  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  int32_t* s_seg_off = reinterpret_cast<int32_t*>(smem + kOffSeg);
+  int32_t* s_seg_var = s_seg_off + (kGemmMaxSegs + 1);
+  int32_t* s_prefix = s_seg_var + kGemmMaxSegs;
+  volatile int* abort = &misc->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool grouped = p.seg_off != nullptr;
+  const uint32_t rank = cluster_rank();
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&xform_bar[s], kXformArrivals);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(accfull_bar, 1);
+    mbar_init(accempty_bar, kAccEmptyArrivals);
+    mbar_init(drain_bar, 1);
+    misc->abort = 0;
+    fence_mbar_init();
+  }
+  if (grouped) {
+    load_segments<kBN>(p, s_seg_off, s_seg_var, s_prefix, &misc->t_total);
+  } else if (threadIdx.x == 0) {
+    misc->t_total = (p.M + kBN - 1) / kBN;
+  }
+  if (warp == kMmaWarp) {
+    // one warp in each CTA of the pair allocates, collectively
+    tmem_alloc_pair(&misc->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_x);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anyone arrives on them
+  tc_fence_after();
+
+  const uint32_t tmem_base = misc->tmem_base;
+  const int64_t t_total = misc->t_total;
+  const int64_t n_tiles_n = (p.d_out + kPairM - 1) / kPairM;
+  const int64_t num_tiles = n_tiles_n * t_total;
+  const int64_t pair_id = blockIdx.x >> 1;
+  const int64_t n_pairs = gridDim.x >> 1;
+  const int64_t my_tiles = pair_id < num_tiles ? (num_tiles - 1 - pair_id) / n_pairs + 1 : 0;
+  const int n_kb = static_cast<int>(p.d_in / kBK);
+  const int64_t total_q = my_tiles * n_kb;  // flat stages q = i * n_kb + kb
+  const int32_t* seg_off_tbl = grouped ? s_seg_off : nullptr;
+  auto my_tile = [&](int64_t i) {
+    return tile_at<kPairM, kBN>(p, pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
+                                s_prefix);
+  };
+  const int64_t row0 = static_cast<int64_t>(rank) * kBM;     // this CTA's rows in the tile
+  const int64_t tok_half = static_cast<int64_t>(rank) * kHalfN;  // this CTA's x rows
+
+  if (warp < kXfWarps) {
+    // ============================================================ transform
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;  // the W row (and TMEM lane) of this thread
+    const int quarter = warp & 3;     // TMEM lane quarter of this warp
+    uint8_t* sign_ring = smem + kOffSign + wg * (kRing * kBM * 8);
+    float* alpha_ring = reinterpret_cast<float*>(smem + kOffAlpha) + wg * (kRing * kBM);
+    const int64_t row_bytes = p.d_in / 8;
+
+    // A cursor over this warpgroup's flat stages q = wg, wg + G, ... as
+    // (tile i, k-block kb); kb < G marks the warpgroup's first stage of a tile.
+    struct Cursor {
+      int64_t q, i;
+      int kb;
+    };
+    auto advance = [&](Cursor& c, int64_t step) {
+      c.q += step;
+      c.kb += static_cast<int>(step);
+      bool moved = false;
+      while (c.kb >= n_kb && c.i < my_tiles) {
+        c.kb -= n_kb;
+        ++c.i;
+        moved = true;
+      }
+      return moved;
+    };
+
+    // Prefetch cursor: row r's 8 sign bytes of the stage (and α at the
+    // warpgroup's first stage of each tile) into private ring slot
+    // (own index) % kRing.  Each thread later reads only what it copied.
+    Cursor pf{0, 0, 0};
+    advance(pf, wg);
+    int pf_slot = 0;
+    Tile pf_tl = pf.i < my_tiles ? my_tile(pf.i) : Tile{0, 0, 0, 0};
+    auto prefetch_next = [&]() {
+      if (pf.q < total_q && pf_tl.variant > 0) {
+        const uint8_t* pk = grouped ? p.packed_table[pf_tl.variant - 1] : p.packed;
+        const float* al = grouped ? p.alpha_table[pf_tl.variant - 1] : p.alpha;
+        const int64_t row = pf_tl.n0 + row0 + r;
+        uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
+        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & 7u) == 0) {
+          cp_async_8(dst, pk + row * row_bytes + static_cast<int64_t>(pf.kb) * 8);
+        } else {
+          if (row < p.d_out && blockIdx.x == 0 && pf.kb < kXfGroups)
+            record_error(p.ctx, kErrBounds);
+          *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+        }
+        if (pf.kb < kXfGroups) {
+          float* adst = alpha_ring + pf_slot * kBM + r;
+          if (row < p.d_out)
+            cp_async_4(adst, p.per_row ? al + row : al);
+          else
+            *adst = 0.f;
+        }
+      }
+      cp_async_commit();
+      pf_slot = pf_slot + 1 == kRing ? 0 : pf_slot + 1;
+      if (pf.q < total_q && advance(pf, kXfGroups) && pf.i < my_tiles) pf_tl = my_tile(pf.i);
+    };
+
+    for (int d = 0; d < kPrefetch; ++d) prefetch_next();
+    uint32_t alpha_bits = 0u;  // α of the current tile's rows (fp32 bits)
+    Cursor cur{0, 0, 0};
+    advance(cur, wg);
+    Tile tl = cur.i < my_tiles ? my_tile(cur.i) : Tile{0, 0, 0, 0};
+    int slot = 0;
+    int s = wg % kStages;                                    // stage / A slot of q
+    uint32_t ph = static_cast<uint32_t>((wg / kStages) & 1);  // parity of q's round
+    const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+    const uint32_t xform_rank0 = map_to_rank(smem_addr(xform_bar), 0);
+    while (cur.q < total_q) {
+      prefetch_next();
+      cp_async_wait<kPrefetch>();
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&full_bar[s], ph, p.ctx, abort) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      if (cur.kb < kXfGroups && tl.variant > 0)
+        alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
+      const bool has_delta = tl.variant > 0;
+      const uint2 sg = has_delta
+                           ? *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8)
+                           : make_uint2(0u, 0u);
+      const uint8_t* w_row = smem + kOffA + s * kABytes + r * (kBK * 2);
+      uint4 wv[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        // logical 16-byte chunk c sits at physical chunk c ^ (r & 7) (the
+        // TMA's 128-byte swizzle XORs address bits 4-6 with bits 7-9)
+        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ (r & 7)) << 4));
+      }
+      uint32_t packed[kBK / 2];
+      if (has_delta) {
+        weff_chunks<kChunks>(wv, sg, alpha_bits, packed);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          packed[4 * c + 0] = wv[c].x;
+          packed[4 * c + 1] = wv[c].y;
+          packed[4 * c + 2] = wv[c].z;
+          packed[4 * c + 3] = wv[c].w;
+        }
+      }
+      tmem_st_32x32b_x32(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      // the A slot is written and this CTA's x half of the stage has landed
+      if (lane == 0) mbar_arrive_cluster(xform_rank0 + static_cast<uint32_t>(8 * s));
+      s += kXfGroups;
+      if (s >= kStages) {
+        s -= kStages;
+        ph ^= 1u;
+      }
+      slot = slot + 1 == kRing ? 0 : slot + 1;
+      if (advance(cur, kXfGroups) && cur.i < my_tiles) tl = my_tile(cur.i);
+    }
+    cp_async_wait<0>();
+  } else if (warp < kTmaWarp) {
+    // ============================================================ epilogue
+    const int quarter = warp - kEpiWarp0;  // TMEM lanes 32*quarter ..
+    const uint32_t accempty_rank0 = map_to_rank(smem_addr(accempty_bar), 0);
+    for (int64_t i = 0; i < my_tiles; ++i) {
+      const uint32_t ph = static_cast<uint32_t>(i & 1);
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait_cluster(accfull_bar, ph, p.ctx, abort) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+      const Tile tl = my_tile(i);
+      store_acc_rows<kBN>(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16), p.y, p.d_out,
+                          tl.n0 + row0 + 32 * quarter + lane, tl.tok0, tl.tok_end);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(accempty_rank0);
+    }
+  } else if (warp == kTmaWarp) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int64_t q = 0;
+      bool ok = true;
+      for (int64_t i = 0; i < my_tiles && ok; ++i) {
+        const Tile tl = my_tile(i);
+        for (int kb = 0; kb < n_kb; ++kb, ++q) {
+          const int s = static_cast<int>(q % kStages);
+          const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
+          if (!mbar_wait_cluster(&empty_bar[s], ph ^ 1u, p.ctx, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], kABytes + kBBytes);
+          tma_load_2d(smem + kOffA + s * kABytes, &tmap_w, &full_bar[s], kb * kBK,
+                      static_cast<int32_t>(tl.n0 + row0), pol_w);
+          tma_load_2d(smem + kOffB + s * kBBytes, &tmap_x, &full_bar[s], kb * kBK,
+                      static_cast<int32_t>(tl.tok0 + tok_half), pol_x);
+        }
+      }
+      // Drain: wait (bounded, ignoring abort) until every issued copy landed.
+      const int64_t first = q > kStages ? q - kStages : 0;
+      for (int64_t qq = first; qq < q; ++qq)
+        mbar_wait(&full_bar[qq % kStages], static_cast<uint32_t>((qq / kStages) & 1), p.ctx,
+                  nullptr);
+    }
+  } else if (warp == kMmaWarp) {
+    // ============================================================ MMA issuer
+    if (lane == 0 && rank == 0) {
+      const uint32_t b_base = smem_addr(smem + kOffB);
+      int64_t q = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int64_t i = 0; i < my_tiles && ok; ++i) {
+        // both CTAs' accumulators must have been drained by their epilogues
+        if (!mbar_wait_cluster(accempty_bar, static_cast<uint32_t>((i & 1) ^ 1), p.ctx, abort))
+          break;
+        tc_fence_after();
+        for (int kb = 0; kb < n_kb; ++kb, ++q) {
+          const int s = static_cast<int>(q % kStages);
+          const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
+          if (!mbar_wait_cluster(&xform_bar[s], ph, p.ctx, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kACol0 + kAColsPerStage * s);
+          const uint64_t b_desc = sdesc_k_sw128(b_base + s * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
+            umma_bf16_tmem_a_pair(tmem_base, a_tmem + 8 * k, b_desc + 2 * k, kIdesc,
+                                  (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit_pair(&empty_bar[s]);
+        }
+        if (!ok) break;
+        umma_commit_pair(accfull_bar);
+      }
+      if (issued) umma_commit_pair(drain_bar);
+      if (issued) mbar_wait_cluster(drain_bar, 0, p.ctx, nullptr);
+    } else if (lane == 0 && my_tiles > 0) {
+      // rank 1: its shared and tensor memory are operands of rank 0's MMAs;
+      // stay until the last of them has completed
+      mbar_wait_cluster(drain_bar, 0, p.ctx, nullptr);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while the other may still touch its memory
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+int gemm_pair_x_rows() { return kHalfN; }
+int gemm_pair_block_k() { return kBK; }
+
+cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
+                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
+                             cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  static int max_pairs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&n, bitdelta_gemm_pair_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = n;
+    attr_done[dev] = true;
+  }
+  const int64_t pairs = pair_tiles_bound < max_pairs[dev] ? pair_tiles_bound : max_pairs[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (pairs > 0 ? pairs : 1)));
+  return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel, tmap_w, tmap_x, p);
+}
+
+}  // namespace bd

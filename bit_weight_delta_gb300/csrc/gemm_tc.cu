@@ -13,9 +13,8 @@
 //
 // The effective weight goes to tensor memory, not shared memory: the MMA takes
 // its A operand from TMEM (row = lane, two bf16 along K per 32-bit column), so
-// shared-memory bandwidth — the limit of this kernel — carries only the TMA
-// writes of W_base and x, one read of W_base by the transform and the MMA's
-// reads of x.
+// shared memory carries only the TMA writes of W_base and x, one read of
+// W_base by the transform and the MMA's reads of x.
 //
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warps 0..4G-1  transform, G warpgroups taking the flat stages in turn.  Thread
@@ -30,18 +29,16 @@
 //   next 1      TMA producer: W_base tile [128 x 64] and x tile [256 x 64].
 //   last        MMA issuer: 4 x tcgen05.mma (128x256x16, A in TMEM) per stage.
 // G = 2 (448 threads).  Measured on 8192-wide projections at 2048 tokens, a
-// third warpgroup made the kernel about 10% slower: the transform is not
-// bound by its own instruction count but by shared-memory and L2 traffic,
-// which more warps only contend for.
+// third warpgroup made the kernel about 10% slower.
 // Every wait is bounded (the kernel records a timeout and unwinds); TMEM is
 // released on every exit path.
 #include <cstdint>
 
-#include "common.cuh"
-#include "kernels.h"
+#include "gemm_common.cuh"
 
 namespace bd {
 namespace {
+using namespace gemm_detail;
 
 constexpr int kBM = 128;  // d_out rows per tile
 constexpr int kBN = 256;  // tokens per tile
@@ -69,7 +66,21 @@ constexpr int kTmemCols = 512;           // D (256) + A slots (128), power of tw
 #ifndef BD_GEMM_XF_GROUPS
 #define BD_GEMM_XF_GROUPS 2
 #endif
-constexpr int kXfGroups = BD_GEMM_XF_GROUPS;  // transform warpgroups, stages in turn
+constexpr int kXfGroups = BD_GEMM_XF_GROUPS;  // transform warpgroups
+#ifndef BD_GEMM_SPLIT
+#define BD_GEMM_SPLIT 0
+#endif
+// Split stages: every warpgroup works on every stage, warpgroup w on columns
+// [w·BK/G, (w+1)·BK/G) of it, so a stage is transformed in 1/G of the time
+// (the ring slot's round trip is TMA latency + transform + MMA, and it bounds
+// the stage rate).  Otherwise the warpgroups take whole stages in turn.
+constexpr bool kSplit = BD_GEMM_SPLIT != 0;
+constexpr int kStep = kSplit ? 1 : kXfGroups;  // flat stages between a warpgroup's stages
+constexpr int kXfChunks = kSplit ? kChunks / kXfGroups : kChunks;  // per thread per stage
+constexpr int kXfSignBytes = kXfChunks;        // one sign byte per 8 columns
+constexpr int kXfCols = 4 * kXfChunks;         // TMEM columns per thread per stage
+constexpr uint32_t kXformArrivals = kSplit ? 4 * kXfGroups : 4;
+static_assert(!kSplit || kXfSignBytes == 4, "split stages take 4 sign bytes per thread");
 constexpr int kXfWarps = 4 * kXfGroups;
 constexpr int kEpiWarp0 = kXfWarps;      // 4 epilogue warps: TMEM lane quarters 0..3
 constexpr int kTmaWarp = kEpiWarp0 + 4;
@@ -86,7 +97,7 @@ constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128] x 8 B
 constexpr int kOffAlpha = kOffSign + kXfGroups * kRing * kBM * 8;  // [G][kRing][128] floats
 constexpr int kOffBar = kOffAlpha + kXfGroups * kRing * kBM * 4;
-constexpr int kNumBars = 3 * kStages + 2 + 1;
+constexpr int kNumBars = 4 * kStages + 2 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, counts
 constexpr int kOffSeg = kOffMisc + 64;            // grouped-mode tables
 constexpr int kSegBytes = (3 * kGemmMaxSegs + 2) * 4;
@@ -99,111 +110,6 @@ struct Misc {
   int64_t t_total;  // token tiles over all segments
 };
 
-struct Tile {
-  int64_t n0;
-  int64_t tok0;
-  int64_t tok_end;
-  int32_t variant;  // 0 = base (no delta)
-};
-
-__device__ __forceinline__ Tile tile_at(const GemmArgs& p, int64_t t, int64_t t_total,
-                                        const int32_t* seg_off, const int32_t* seg_var,
-                                        const int32_t* prefix) {
-  Tile tl;
-  const int64_t nt = t / t_total;
-  const int64_t j = t - nt * t_total;
-  tl.n0 = nt * kBM;
-  if (seg_off == nullptr) {
-    tl.tok0 = j * kBN;
-    tl.tok_end = p.M;
-    tl.variant = 1;
-  } else {
-    // largest s with prefix[s] <= j (prefix is non-decreasing, prefix[0] = 0)
-    int lo = 0, hi = p.n_seg;  // invariant: prefix[lo] <= j < prefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= j)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    tl.tok0 = seg_off[lo] + (j - prefix[lo]) * kBN;
-    tl.tok_end = seg_off[lo + 1];
-    tl.variant = seg_var[lo];
-  }
-  return tl;
-}
-
-// Sign-flip mask of one bf16 pair: bit 15 (the low element, column 2j of the
-// chunk) and bit 31 (the high element, column 2j+1) are set where the sign
-// bit is 0 (s = -1).  nb = the chunk's inverted sign byte (8 bits); the
-// multiply places nb bit 2j at bit 15 and bit 2j+1 at bit 31 (the two partial
-// products do not overlap, so no carry reaches either bit).
-template <int J>
-__device__ __forceinline__ uint32_t pair_flip_mask(uint32_t nb) {
-  return (nb * (0x40008000u >> (2 * J))) & 0x80008000u;
-}
-
-// bf16x2_rne(fp32(w.lo) + a, fp32(w.hi) + a), one packed fp32x2 add.
-__device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t w, uint32_t a) {
-  uint32_t lo, hi;
-  asm("{\n\t.reg .b64 x, y, d;\n\t"
-      "mov.b64 x, {%2, %3};\n\t"
-      "mov.b64 y, {%4, %4};\n\t"
-      "add.rn.f32x2 d, x, y;\n\t"
-      "mov.b64 {%0, %1}, d;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w << 16), "r"(w & 0xFFFF0000u), "r"(a));
-  return pack_bf16x2_rn(__uint_as_float(lo), __uint_as_float(hi));
-}
-
-// 32 lanes x 32 consecutive 32-bit columns: thread i writes lane (base+i).
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const uint32_t (&r)[N]) {
-  static_assert(N == 16 || N == 32, "16 or 32 columns");
-  if constexpr (N == 32)
-    tmem_st_32x32b_x32(taddr, r);
-  else
-    tmem_st_32x32b_x16(taddr, r);
-}
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// D[tmem] (+)= A[tmem] · B[smem]ᵀ, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
-                                                 uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     bitdelta_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                          const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
@@ -211,10 +117,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full_bar = bars;                 // TMA -> transform and MMA
-  uint64_t* xform_bar = bars + kStages;      // transform -> MMA (A slot written)
-  uint64_t* empty_bar = bars + 2 * kStages;  // MMA -> TMA (stage and A slot free)
-  uint64_t* accfull_bar = bars + 3 * kStages;
+  // Each stage's W_base and x complete on separate barriers: the transform
+  // starts as soon as its 16 KB of W_base has landed, while x is still
+  // arriving (the MMA waits for x and the transform).
+  uint64_t* full_bar = bars;                 // TMA (W_base) -> transform
+  uint64_t* xfull_bar = bars + kStages;      // TMA (x) -> MMA
+  uint64_t* xform_bar = bars + 2 * kStages;  // transform -> MMA (A slot written)
+  uint64_t* empty_bar = bars + 3 * kStages;  // MMA -> TMA (stage and A slot free)
+  uint64_t* accfull_bar = bars + 4 * kStages;
   uint64_t* accempty_bar = accfull_bar + 1;
   uint64_t* drain_bar = accempty_bar + 1;
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -231,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&xform_bar[s], 4);  // the 4 warps of the warpgroup owning the stage
+      mbar_init(&xfull_bar[s], 1);
+      mbar_init(&xform_bar[s], kXformArrivals);  // the transform warps of the stage
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(accfull_bar, 1);
@@ -241,39 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (grouped) {
-    // Copy the segment table, then count token tiles per valid long segment.
-    // One malformed entry rejects the whole table (no tiles at all).
-    for (int s = threadIdx.x; s <= p.n_seg; s += blockDim.x) s_seg_off[s] = __ldg(p.seg_off + s);
-    for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) s_seg_var[s] = __ldg(p.seg_var + s);
-    __syncthreads();
-    int bad_local = 0;
-    for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
-      const int32_t a = s_seg_off[s], b = s_seg_off[s + 1], v = s_seg_var[s];
-      bad_local |= (a < 0 || b < a || b > p.M || v < 0 || v > p.n_var) ? 1 : 0;
-    }
-    const bool table_bad = __syncthreads_or(bad_local) != 0;
-    if (table_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
-    for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
-      const int32_t len = table_bad ? 0 : s_seg_off[s + 1] - s_seg_off[s];
-      s_prefix[s + 1] = len > p.max_short ? (len + kBN - 1) / kBN : 0;
-    }
-    __syncthreads();
-    if (warp == 0) {  // inclusive scan of the tile counts
-      int32_t carry = 0;
-      if (lane == 0) s_prefix[0] = 0;
-      for (int base = 0; base < p.n_seg; base += 32) {
-        const int s = base + lane;
-        int32_t v = s < p.n_seg ? s_prefix[s + 1] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, off);
-          if (lane >= off) v += o;
-        }
-        if (s < p.n_seg) s_prefix[s + 1] = carry + v;
-        carry += __shfl_sync(0xFFFFFFFFu, v, 31);
-      }
-      if (lane == 0) misc->t_total = carry;
-    }
+    load_segments<kBN>(p, s_seg_off, s_seg_var, s_prefix, &misc->t_total);
   } else if (threadIdx.x == 0) {
     misc->t_total = (p.M + kBN - 1) / kBN;
   }
@@ -299,20 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total_q = my_tiles * n_kb;  // flat stages q = i * n_kb + kb
   const int32_t* seg_off_tbl = grouped ? s_seg_off : nullptr;
   auto my_tile = [&](int64_t i) {
-    return tile_at(p, blockIdx.x + i * gridDim.x, t_total, seg_off_tbl, s_seg_var, s_prefix);
+    return tile_at<kBM, kBN>(p, blockIdx.x + i * gridDim.x, t_total, seg_off_tbl, s_seg_var,
+                             s_prefix);
   };
 
   if (warp < kXfWarps) {
     // ============================================================ transform
-    const int wg = warp >> 2;          // warpgroup: flat stages q with q % kXfGroups == wg
+    const int wg = warp >> 2;          // warpgroup
+    const int c0 = kSplit ? wg * kXfChunks : 0;  // first 16-byte chunk of this warpgroup
     const int r = threadIdx.x & 127;   // the W row (and TMEM lane) of this thread
     const int quarter = warp & 3;      // TMEM lane quarter of this warp
     uint8_t* sign_ring = smem + kOffSign + wg * (kRing * kBM * 8);
     float* alpha_ring = reinterpret_cast<float*>(smem + kOffAlpha) + wg * (kRing * kBM);
     const int64_t row_bytes = p.d_in / 8;
 
-    // A cursor over this warpgroup's flat stages q = wg, wg + G, ... as
-    // (tile i, k-block kb); kb < G marks the warpgroup's first stage of a tile.
+    // A cursor over this warpgroup's flat stages (q = wg, wg + G, ... taking
+    // stages in turn; every q with split stages) as (tile i, k-block kb);
+    // kb < kStep marks the warpgroup's first stage of a tile.
     struct Cursor {
       int64_t q, i;
       int kb;
@@ -333,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage of each tile) into private ring slot (own index) % kRing.  Each
     // thread later reads only what it copied itself.
     Cursor pf{0, 0, 0};
-    advance(pf, wg);
+    advance(pf, kSplit ? 0 : wg);
     int pf_slot = 0;
     Tile pf_tl = pf.i < my_tiles ? my_tile(pf.i) : Tile{0, 0, 0, 0};
     auto prefetch_next = [&]() {
@@ -342,18 +224,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* al = grouped ? p.alpha_table[pf_tl.variant - 1] : p.alpha;
         const int64_t row = pf_tl.n0 + r;
         uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
-        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & (kSignBytes - 1)) == 0) {
-          const uint8_t* src = pk + row * row_bytes + static_cast<int64_t>(pf.kb) * kSignBytes;
-          if constexpr (kSignBytes == 8)
+        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & (kXfSignBytes - 1)) == 0) {
+          const uint8_t* src =
+              pk + row * row_bytes + static_cast<int64_t>(pf.kb) * kSignBytes + c0;
+          if constexpr (kXfSignBytes == 8)
             cp_async_8(dst, src);
           else
             cp_async_4(dst, src);
         } else {
-          if (row < p.d_out && blockIdx.x == 0 && pf.kb < kXfGroups)
-            record_error(p.ctx, kErrBounds);
+          if (row < p.d_out && blockIdx.x == 0 && pf.kb < kStep) record_error(p.ctx, kErrBounds);
           *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
         }
-        if (pf.kb < kXfGroups) {
+        if (pf.kb < kStep) {
           float* adst = alpha_ring + pf_slot * kBM + r;
           if (row < p.d_out)
             cp_async_4(adst, p.per_row ? al + row : al);
@@ -363,17 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cp_async_commit();
       pf_slot = pf_slot + 1 == kRing ? 0 : pf_slot + 1;
-      if (pf.q < total_q && advance(pf, kXfGroups) && pf.i < my_tiles) pf_tl = my_tile(pf.i);
+      if (pf.q < total_q && advance(pf, kStep) && pf.i < my_tiles) pf_tl = my_tile(pf.i);
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch_next();
     uint32_t alpha_bits = 0u;  // α of the current tile's rows (fp32 bits)
     Cursor cur{0, 0, 0};
-    advance(cur, wg);
+    advance(cur, kSplit ? 0 : wg);
     Tile tl = cur.i < my_tiles ? my_tile(cur.i) : Tile{0, 0, 0, 0};
     int slot = 0;
-    int s = wg % kStages;                            // smem stage / A slot of q
-    uint32_t ph = static_cast<uint32_t>((wg / kStages) & 1);  // parity of q's round
+    int s = static_cast<int>(cur.q % kStages);                      // stage / A slot of q
+    uint32_t ph = static_cast<uint32_t>((cur.q / kStages) & 1);     // parity of q's round
     const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
     while (cur.q < total_q) {
       prefetch_next();
@@ -383,66 +265,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      if (cur.kb < kXfGroups && tl.variant > 0)
+      if (cur.kb < kStep && tl.variant > 0)
         alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       const bool has_delta = tl.variant > 0;
       uint2 sg = make_uint2(0u, 0u);
       if (has_delta) {
-        if constexpr (kSignBytes == 8)
+        if constexpr (kXfSignBytes == 8)
           sg = *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8);
         else
           sg.x = *reinterpret_cast<const uint32_t*>(sign_ring + (slot * kBM + r) * 8);
       }
       const uint8_t* w_row = smem + kOffA + s * kABytes + r * (kBK * 2);
       const int swz = (r >> kSwzShift) & (kChunks - 1);
-      uint4 wv[kChunks];
+      uint4 wv[kXfChunks];
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        // logical 16-byte chunk c (columns 8c..8c+7) sits at physical chunk
-        // c ^ swz: the TMA's 128-byte (64-byte) swizzle XORs the chunk index
-        // with address bits 7-9 (7-8), i.e. with row bits 0-2 (1-2)
-        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
+      for (int c = 0; c < kXfChunks; ++c) {
+        // logical 16-byte chunk c0+c (columns 8(c0+c) ..) sits at physical
+        // chunk (c0+c) ^ swz: the TMA's 128-byte (64-byte) swizzle XORs the
+        // chunk index with address bits 7-9 (7-8), i.e. with row bits 0-2 (1-2)
+        wv[c] = *reinterpret_cast<const uint4*>(w_row + (((c0 + c) ^ swz) << 4));
       }
-      uint32_t packed[kBK / 2];
+      uint32_t packed[kXfCols];
       if (has_delta) {
-        // W + s·α = s·(s·W + α): flip W where s = -1 (exact), add α in fp32,
-        // round to bf16, flip back.  Round-to-nearest-even is symmetric, so
-        // this is bf16_rne(fp32(W) + s·α) up to the sign of an exact zero
-        // (which no product or sum of the MMA can tell apart).
-        const uint32_t nsx = ~sg.x, nsy = ~sg.y;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          const uint32_t nb = ((c < 4 ? nsx : nsy) >> (8 * (c & 3))) & 0xFFu;
-          const uint32_t f0 = pair_flip_mask<0>(nb), f1 = pair_flip_mask<1>(nb);
-          const uint32_t f2 = pair_flip_mask<2>(nb), f3 = pair_flip_mask<3>(nb);
-          packed[4 * c + 0] = add_round_bf16x2(wv[c].x ^ f0, alpha_bits) ^ f0;
-          packed[4 * c + 1] = add_round_bf16x2(wv[c].y ^ f1, alpha_bits) ^ f1;
-          packed[4 * c + 2] = add_round_bf16x2(wv[c].z ^ f2, alpha_bits) ^ f2;
-          packed[4 * c + 3] = add_round_bf16x2(wv[c].w ^ f3, alpha_bits) ^ f3;
-        }
+        weff_chunks<kXfChunks>(wv, sg, alpha_bits, packed);
       } else {
         // base rows (grouped mode, variant 0): W_base unchanged
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < kXfChunks; ++c) {
           packed[4 * c + 0] = wv[c].x;
           packed[4 * c + 1] = wv[c].y;
           packed[4 * c + 2] = wv[c].z;
           packed[4 * c + 3] = wv[c].w;
         }
       }
-      tmem_st_32x32b(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
+      tmem_st_32x32b(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s + 4 * c0),
+                     packed);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&xform_bar[s]);
-      // advance to this warpgroup's next stage (kXfGroups flat stages later)
-      s += kXfGroups;
+      // advance to this warpgroup's next stage (kStep flat stages later)
+      s += kStep;
       if (s >= kStages) {
         s -= kStages;
         ph ^= 1u;
       }
       slot = slot + 1 == kRing ? 0 : slot + 1;
-      if (advance(cur, kXfGroups) && cur.i < my_tiles) tl = my_tile(cur.i);
+      if (advance(cur, kStep) && cur.i < my_tiles) tl = my_tile(cur.i);
     }
     cp_async_wait<0>();
   } else if (warp < kTmaWarp) {
@@ -459,30 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const Tile tl = my_tile(i);
-      const int64_t n = tl.n0 + 32 * quarter + lane;
-      const bool n_ok = n < p.d_out;
-      const int64_t tok_limit = tl.tok_end < tl.tok0 + kBN ? tl.tok_end : tl.tok0 + kBN;
-      const int chunks =
-          tok_limit > tl.tok0 ? static_cast<int>((tok_limit - tl.tok0 + 31) / 32) : 0;
-#pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
-        uint32_t rr[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
-                               static_cast<uint32_t>(32 * c),
-                           rr);
-        tmem_ld_wait();
-        const int64_t tok_base = tl.tok0 + 32 * c;
-        if (n_ok) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t tok = tok_base + j;
-            if (tok < tok_limit) {
-              const uint32_t pk = pack_bf16x2_rn(__uint_as_float(rr[j]), 0.f);
-              p.y[tok * p.d_out + n] = static_cast<uint16_t>(pk & 0xFFFFu);
-            }
-          }
-        }
-      }
+      store_acc_rows<kBN>(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16), p.y, p.d_out,
+                          tl.n0 + 32 * quarter + lane, tl.tok0, tl.tok_end);
       tc_fence_before();
       mbar_arrive(accempty_bar);
     }
@@ -502,18 +349,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[s], kABytes + kBBytes);
+          mbar_arrive_expect_tx(&full_bar[s], kABytes);
           tma_load_2d(smem + kOffA + s * kABytes, &tmap_w, &full_bar[s], kb * kBK,
                       static_cast<int32_t>(tl.n0), pol_w);
-          tma_load_2d(smem + kOffB + s * kBBytes, &tmap_x, &full_bar[s], kb * kBK,
+          mbar_arrive_expect_tx(&xfull_bar[s], kBBytes);
+          tma_load_2d(smem + kOffB + s * kBBytes, &tmap_x, &xfull_bar[s], kb * kBK,
                       static_cast<int32_t>(tl.tok0), pol_x);
         }
       }
       // Drain: wait (bounded, ignoring abort) until every issued copy landed.
       const int64_t first = q > kStages ? q - kStages : 0;
-      for (int64_t qq = first; qq < q; ++qq)
-        mbar_wait(&full_bar[qq % kStages], static_cast<uint32_t>((qq / kStages) & 1), p.ctx,
-                  nullptr);
+      for (int64_t qq = first; qq < q; ++qq) {
+        const uint32_t par = static_cast<uint32_t>((qq / kStages) & 1);
+        mbar_wait(&full_bar[qq % kStages], par, p.ctx, nullptr);
+        mbar_wait(&xfull_bar[qq % kStages], par, p.ctx, nullptr);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
@@ -529,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < n_kb; ++kb, ++q) {
           const int s = static_cast<int>(q % kStages);
           const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
-          if (!mbar_wait(&full_bar[s], ph, p.ctx, abort)) { ok = false; break; }
+          if (!mbar_wait(&xfull_bar[s], ph, p.ctx, abort)) { ok = false; break; }
           if (!mbar_wait(&xform_bar[s], ph, p.ctx, abort)) {
             ok = false;
             break;

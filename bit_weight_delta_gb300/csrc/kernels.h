@@ -88,6 +88,16 @@ int gemm_block_k();       // K per stage: 32 (64-byte swizzle) or 64 (128-byte s
 cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                         int grid, cudaStream_t stream);
 
+// Prefill-size linear on CTA pairs (tcgen05 cta_group::2): tiles of
+// 2 * gemm_block_rows() output rows x gemm_block_tokens() tokens; tmap_w's box
+// has gemm_block_rows() rows, tmap_x's box gemm_pair_x_rows() (half a tile),
+// both gemm_pair_block_k() columns.  pair_tiles_bound caps the pairs launched.
+int gemm_pair_x_rows();
+int gemm_pair_block_k();
+cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
+                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
+                             cudaStream_t stream);
+
 // Test hook: one CTA waiting on an mbarrier nothing completes.
 cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream);
 
