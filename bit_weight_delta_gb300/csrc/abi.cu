@@ -118,8 +118,10 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
 
 // Launch the tensor-core kernel on g (x has rows_x rows; at most
 // token_tiles_bound 256-token tiles per row tile).  The pair kernel
-// (cta_group::2, 256 output rows per tile) unless built with BD_GEMM_PAIR=0.
-// Returns false, launching nothing, when a tensor map cannot be encoded.
+// (cta_group::2, 256 output rows per tile) unless built with BD_GEMM_PAIR=0,
+// or when the device cannot place a cluster of two of its CTAs: then the
+// one-CTA kernel.  Returns false, launching nothing, when a tensor map cannot
+// be encoded.
 bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t rows_x,
                int64_t token_tiles_bound, int num_sms, cudaStream_t s, cudaError_t* err) {
   CUtensorMap tw, tx;
@@ -131,7 +133,8 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
     const int64_t pair_tiles = ((g.d_out + 2 * bd::gemm_block_rows() - 1) /
                                 (2 * bd::gemm_block_rows())) * token_tiles_bound;
     *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, s);
-    return true;
+    if (*err != cudaErrorInvalidConfiguration) return true;
+    (void)cudaGetLastError();  // no cluster fits: fall through to one CTA per tile
   }
   const int bk = bd::gemm_block_k();
   if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||

@@ -70,6 +70,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
   return done != 0;
 }
 
+#ifndef BD_SUSPEND_NS
+#define BD_SUSPEND_NS 20000
+#endif
+// Suspend-time hint of one try_wait in the bounded waits below (ns).
+constexpr uint32_t kSuspendNs = BD_SUSPEND_NS;
+
 // Bounded wait for the phase of `bar` with the given parity.  Returns true on
 // completion.  Returns false when the time limit passes (the timeout is
 // recorded in the error word and *abort is raised) or when another role has
@@ -82,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   const long long t0 = clock64();
   const long long limit = static_cast<long long>(ctx.wait_limit_ns) * 2;
   while (true) {
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     if (abort != nullptr && *abort) return false;
     if (clock64() - t0 > limit) {
       record_error(ctx, kErrTimeout);

@@ -278,7 +278,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   const long long t0 = clock64();
   const long long limit = static_cast<long long>(ctx.wait_limit_ns) * 2;
   while (true) {
-    if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_cluster(bar, parity, kSuspendNs)) return true;
     if (abort != nullptr && *abort) return false;
     if (clock64() - t0 > limit) {
       record_error(ctx, kErrTimeout);

@@ -40,18 +40,30 @@ constexpr int kBM = 128;            // output rows per CTA
 constexpr int kPairM = 2 * kBM;     // output rows per pair tile (UMMA M)
 constexpr int kBN = 256;            // tokens per pair tile (UMMA N)
 constexpr int kHalfN = kBN / 2;     // tokens loaded by each CTA
-constexpr int kBK = 64;             // K per stage: one 128-byte swizzle row
-constexpr int kStages = 6;
-constexpr int kABytes = kBM * kBK * 2;     // 16 KB of W_base per stage
-constexpr int kBBytes = kHalfN * kBK * 2;  // 16 KB of x per stage
+#ifndef BD_PAIR_BK
+#define BD_PAIR_BK 64
+#endif
+// K per stage: one row of a swizzle atom, 128 bytes of bf16 (BK = 64, 128-byte
+// swizzle, 6 stages of 32 KB) or 64 bytes (BK = 32, 64-byte swizzle, 12
+// stages of 16 KB).
+constexpr int kBK = BD_PAIR_BK;
+static_assert(kBK == 32 || kBK == 64, "BK is one 64- or 128-byte swizzle row");
+constexpr int kStages = 384 / kBK;
+constexpr int kABytes = kBM * kBK * 2;     // W_base per stage
+constexpr int kBBytes = kHalfN * kBK * 2;  // x per stage
 constexpr int kChunks = kBK / 8;           // 16-byte chunks per W row per stage
+constexpr int kSwzShift = kBK == 64 ? 0 : 1;  // row bits that select the chunk XOR
+constexpr int kSignBytes = kBK / 8;        // sign bytes per row per stage
 constexpr int kPrefetch = 2;               // sign/α prefetch distance (own stages)
 constexpr int kRing = kPrefetch + 2;       // private ring slots per thread
 constexpr int kDCols = kBN;                // accumulator columns
 constexpr int kACol0 = kDCols;             // first column of the A slots
-constexpr int kAColsPerStage = kBK / 2;    // 64 bf16 per row = 32 columns
+constexpr int kAColsPerStage = kBK / 2;    // two bf16 per 32-bit column
 constexpr int kTmemCols = 512;             // D (256) + 6 A slots (192), power of two
-constexpr int kXfGroups = 2;
+#ifndef BD_PAIR_XF_GROUPS
+#define BD_PAIR_XF_GROUPS 2
+#endif
+constexpr int kXfGroups = BD_PAIR_XF_GROUPS;  // transform warpgroups, stages in turn
 constexpr int kXfWarps = 4 * kXfGroups;
 constexpr int kEpiWarp0 = kXfWarps;
 constexpr int kTmaWarp = kEpiWarp0 + 4;
@@ -148,7 +160,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int64_t n_pairs = gridDim.x >> 1;
   const int64_t my_tiles = pair_id < num_tiles ? (num_tiles - 1 - pair_id) / n_pairs + 1 : 0;
   const int n_kb = static_cast<int>(p.d_in / kBK);
-  const int64_t total_q = my_tiles * n_kb;  // flat stages q = i * n_kb + kb
   const int32_t* seg_off_tbl = grouped ? s_seg_off : nullptr;
   auto my_tile = [&](int64_t i) {
     return tile_at<kPairM, kBN>(p, pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
@@ -166,68 +177,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* alpha_ring = reinterpret_cast<float*>(smem + kOffAlpha) + wg * (kRing * kBM);
     const int64_t row_bytes = p.d_in / 8;
 
-    // A cursor over this warpgroup's flat stages q = wg, wg + G, ... as
-    // (tile i, k-block kb); kb < G marks the warpgroup's first stage of a tile.
-    struct Cursor {
-      int64_t q, i;
-      int kb;
-    };
-    auto advance = [&](Cursor& c, int64_t step) {
-      c.q += step;
-      c.kb += static_cast<int>(step);
-      bool moved = false;
-      while (c.kb >= n_kb && c.i < my_tiles) {
-        c.kb -= n_kb;
-        ++c.i;
-        moved = true;
-      }
-      return moved;
-    };
+    const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+    const uint32_t xform_rank0 = map_to_rank(smem_addr(xform_bar), 0);
 
-    // Prefetch cursor: row r's 8 sign bytes of the stage (and α at the
-    // warpgroup's first stage of each tile) into private ring slot
-    // (own index) % kRing.  Each thread later reads only what it copied.
-    Cursor pf{0, 0, 0};
-    advance(pf, wg);
-    int pf_slot = 0;
-    Tile pf_tl = pf.i < my_tiles ? my_tile(pf.i) : Tile{0, 0, 0, 0};
-    auto prefetch_next = [&]() {
-      if (pf.q < total_q && pf_tl.variant > 0) {
-        const uint8_t* pk = grouped ? p.packed_table[pf_tl.variant - 1] : p.packed;
-        const float* al = grouped ? p.alpha_table[pf_tl.variant - 1] : p.alpha;
-        const int64_t row = pf_tl.n0 + row0 + r;
-        uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
-        if (row < p.d_out && (reinterpret_cast<uintptr_t>(pk) & 7u) == 0) {
-          cp_async_8(dst, pk + row * row_bytes + static_cast<int64_t>(pf.kb) * 8);
-        } else {
-          if (row < p.d_out && blockIdx.x == 0 && pf.kb < kXfGroups)
-            record_error(p.ctx, kErrBounds);
-          *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-        }
-        if (pf.kb < kXfGroups) {
-          float* adst = alpha_ring + pf_slot * kBM + r;
-          if (row < p.d_out)
-            cp_async_4(adst, p.per_row ? al + row : al);
-          else
-            *adst = 0.f;
-        }
+    // Prefetch cursor, kPrefetch of this warpgroup's stages ahead of the
+    // transform: tile pf_i, k-block pf_kb.  Per tile it holds where this
+    // row's sign bytes come from (mode 1), or a fill of +1 signs for a
+    // variant table entry that is not aligned (mode 2, recorded as a bounds
+    // error), or nothing for base rows (mode 0), so the per-stage step is one
+    // cp.async.  Each thread later reads only what it copied itself, from
+    // private ring slot (own stage index) % kRing.
+    int64_t pf_i = 0;
+    int pf_kb = wg, pf_slot = 0, pf_mode = 0;
+    const uint8_t* pf_src = nullptr;
+    const float* pf_alpha = nullptr;
+    auto pf_load_tile = [&]() {
+      pf_mode = 0;
+      if (pf_i >= my_tiles) return;
+      const Tile t = my_tile(pf_i);
+      if (t.variant <= 0) return;
+      const uint8_t* pk = grouped ? p.packed_table[t.variant - 1] : p.packed;
+      const float* al = grouped ? p.alpha_table[t.variant - 1] : p.alpha;
+      // a row past d_out reads row d_out - 1: its products land in
+      // accumulator rows that the epilogue never stores
+      int64_t row = t.n0 + row0 + r;
+      row = row < p.d_out ? row : p.d_out - 1;
+      pf_alpha = p.per_row ? al + row : al;
+      if ((reinterpret_cast<uintptr_t>(pk) & (kSignBytes - 1)) == 0) {
+        pf_src = pk + row * row_bytes;
+        pf_mode = 1;
+      } else {
+        if (blockIdx.x == 0) record_error(p.ctx, kErrBounds);
+        pf_mode = 2;
       }
+    };
+    while (pf_kb >= n_kb && pf_i < my_tiles) {
+      pf_kb -= n_kb;
+      ++pf_i;
+    }
+    pf_load_tile();
+    auto prefetch_next = [&]() {
+      uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
+      if (pf_mode == 1) {
+        if constexpr (kSignBytes == 8)
+          cp_async_8(dst, pf_src + pf_kb * kSignBytes);
+        else
+          cp_async_4(dst, pf_src + pf_kb * kSignBytes);
+      } else if (pf_mode == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+      }
+      if (pf_mode != 0 && pf_kb < kXfGroups) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
       cp_async_commit();
       pf_slot = pf_slot + 1 == kRing ? 0 : pf_slot + 1;
-      if (pf.q < total_q && advance(pf, kXfGroups) && pf.i < my_tiles) pf_tl = my_tile(pf.i);
+      pf_kb += kXfGroups;
+      if (pf_kb >= n_kb) {
+        do {
+          pf_kb -= n_kb;
+          ++pf_i;
+        } while (pf_kb >= n_kb);
+        pf_load_tile();
+      }
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch_next();
     uint32_t alpha_bits = 0u;  // α of the current tile's rows (fp32 bits)
-    Cursor cur{0, 0, 0};
-    advance(cur, wg);
-    Tile tl = cur.i < my_tiles ? my_tile(cur.i) : Tile{0, 0, 0, 0};
+    // This warpgroup's stages: tile i, k-block kb (kb < G marks its first
+    // stage of a tile); s / ph: ring stage and phase parity of the flat stage
+    // index i * n_kb + kb.
+    int64_t i = 0;
+    int kb = wg;
+    while (kb >= n_kb && i < my_tiles) {
+      kb -= n_kb;
+      ++i;
+    }
+    Tile tl = i < my_tiles ? my_tile(i) : Tile{0, 0, 0, 0};
     int slot = 0;
-    int s = wg % kStages;                                    // stage / A slot of q
-    uint32_t ph = static_cast<uint32_t>((wg / kStages) & 1);  // parity of q's round
-    const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
-    const uint32_t xform_rank0 = map_to_rank(smem_addr(xform_bar), 0);
-    while (cur.q < total_q) {
+    const int64_t q0 = i * n_kb + kb;
+    int s = static_cast<int>(q0 % kStages);
+    uint32_t ph = static_cast<uint32_t>((q0 / kStages) & 1);
+    while (i < my_tiles) {
       prefetch_next();
       cp_async_wait<kPrefetch>();
       int ok = 0;
@@ -235,19 +263,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      if (cur.kb < kXfGroups && tl.variant > 0)
+      if (kb < kXfGroups && tl.variant > 0)
         alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       const bool has_delta = tl.variant > 0;
-      const uint2 sg = has_delta
-                           ? *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8)
-                           : make_uint2(0u, 0u);
+      uint2 sg = make_uint2(0u, 0u);
+      if (has_delta) {
+        if constexpr (kSignBytes == 8)
+          sg = *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8);
+        else
+          sg.x = *reinterpret_cast<const uint32_t*>(sign_ring + (slot * kBM + r) * 8);
+      }
       const uint8_t* w_row = smem + kOffA + s * kABytes + r * (kBK * 2);
+      const int swz = (r >> kSwzShift) & (kChunks - 1);
       uint4 wv[kChunks];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
-        // logical 16-byte chunk c sits at physical chunk c ^ (r & 7) (the
-        // TMA's 128-byte swizzle XORs address bits 4-6 with bits 7-9)
-        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ (r & 7)) << 4));
+        // logical 16-byte chunk c sits at physical chunk c ^ swz: the TMA's
+        // 128-byte (64-byte) swizzle XORs the chunk index with address bits
+        // 7-9 (7-8), i.e. with row bits 0-2 (1-2)
+        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
       }
       uint32_t packed[kBK / 2];
       if (has_delta) {
@@ -261,7 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           packed[4 * c + 3] = wv[c].w;
         }
       }
-      tmem_st_32x32b_x32(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
+      tmem_st_32x32b(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -273,7 +307,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ph ^= 1u;
       }
       slot = slot + 1 == kRing ? 0 : slot + 1;
-      if (advance(cur, kXfGroups) && cur.i < my_tiles) tl = my_tile(cur.i);
+      kb += kXfGroups;
+      if (kb >= n_kb) {
+        do {
+          kb -= n_kb;
+          ++i;
+        } while (kb >= n_kb);
+        if (i < my_tiles) tl = my_tile(i);
+      }
     }
     cp_async_wait<0>();
   } else if (warp < kTmaWarp) {
@@ -345,7 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kACol0 + kAColsPerStage * s);
-          const uint64_t b_desc = sdesc_k_sw128(b_base + s * kBBytes);
+          const uint64_t b_desc = kBK == 64 ? sdesc_k_sw128(b_base + s * kBBytes)
+                                            : sdesc_k_sw64(b_base + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
