@@ -449,11 +449,7 @@ def timed_run(cudart, wl, steps, warmup, dist, clock=None, graph_steps=None):
         clock.mark("end")
     if dist is not None:
         dist.barrier()
-    ms = start.elapsed_time(end) / steps
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, start.elapsed_time(end) / steps)
     phases = phase_times(cudart, wl, events, per_graph) if replays > 0 else {}
     del g, g_rem
     return ms, phases
@@ -525,19 +521,41 @@ def e2e_decode(bd, steps: int):
 # --------------------------------------------------------------------------- main
 
 
-def init_dist(args):
+def init_dist(args=None):
+    """One process per GPU (torchrun env).  NCCL when CUDA is present, gloo
+    otherwise (the host-side logic runs on CPU-only test hosts too)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
     if world > 1:
         import torch.distributed as tdist
-        torch.cuda.set_device(local)
-        tdist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            tdist.init_process_group("nccl")
+        else:
+            tdist.init_process_group("gloo")
         dist = tdist
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return dist, rank, world, local
+
+
+def max_over_ranks(dist, value: float) -> float:
+    """The slowest rank's time: an all-reduce (MAX) over the process group, or
+    the value itself for one process."""
+    if dist is None:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: every rank processes the same units per step
+    (independent replicas), over the slowest rank's time."""
+    return world * units_per_rank / seconds
 
 
 def run_reference(args, rank, world):
@@ -662,7 +680,7 @@ def main():
                            graph_steps=min(args.steps, 20))
     clocks = clock.stop() if clock else None
     bytes_step = dec.bytes_per_step()
-    value = world * bytes_step / (ms * 1e-3) / 1e9
+    value = weak_scaling_value(world, bytes_step, ms * 1e-3) / 1e9
 
     dom = dec.dominant()
     dom_bytes = sum(dec.bytes[p] * dec.L for p in dom)
