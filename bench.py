@@ -380,6 +380,145 @@ class Grouped:
                                         max_seg_len=512, per_row=True, out=self.y)
 
 
+class Slice40:
+    """A 40-layer slice of a Llama-70B-sized model: per layer QKV 8192->10240,
+    O 8192->8192, gate+up 8192->57344, down 28672->8192 (855.6M weights per
+    layer, 68.45 GB of bf16 base weights), two compressed variants resident
+    (per-row α), and per layer the compression of a third variant whose
+    fine-tuned weights are drawn on the device one layer at a time.
+
+    Phases: "prefill" (512 tokens of variant 1 through all 160 projections),
+    "decode" (batch of 8 rows alternating variants 1, 2, 1, 2, ... as eight
+    one-row segments of the grouped linear, all 160 projections) and
+    "compress" (variant 3, all 160 projections; its W_ft is drawn outside
+    the timed kernels).  Each projection takes a fresh N(0,1) input of its
+    width: the projections are not chained through attention."""
+
+    name = "slice40_llama70b_prefill512_decode8x2variants_compress3rd"
+    L = 40
+    shapes = Prefill.shapes
+    prefill_M = 512
+    decode_M = 8
+
+    def __init__(self, bd, seed: int = 5):
+        import synth
+        import synth.device as sd
+        self.bd = bd
+        self.layers = []
+        scales = synth.variant_scales(seed, 3)
+        for l in range(self.L):
+            mats = {}
+            for i, (nm, d_out, d_in) in enumerate(self.shapes):
+                wb = sd.normal_bf16((d_out, d_in), seed, 10000 + 10 * l + i, 0.02)
+                var = []
+                for v in range(2):
+                    wf = sd.finetuned_bf16(wb, seed, 20000 + 100 * l + 10 * i + v, float(scales[v]))
+                    var.append(bd.bitdelta_compress(wb, wf, per_row=True))
+                    del wf
+                pt, at = bd.variant_tables([var[0][0], var[1][0]], [var[0][1], var[1][1]], "cuda")
+                mats[nm] = (wb, var, pt, at)
+            self.layers.append(mats)
+        self.b3 = float(scales[2])
+        self.seed = seed
+        widths = sorted({d_in for _, _, d_in in self.shapes})
+        self.xp = {d: sd.normal_bf16((self.prefill_M, d), seed, 30000 + d) for d in widths}
+        self.xd = {d: sd.normal_bf16((self.decode_M, d), seed, 40000 + d) for d in widths}
+        self.yp = {nm: torch.empty((self.prefill_M, d_out), dtype=torch.bfloat16, device="cuda")
+                   for nm, d_out, _ in self.shapes}
+        self.yd = {nm: torch.empty((self.decode_M, d_out), dtype=torch.bfloat16, device="cuda")
+                   for nm, d_out, _ in self.shapes}
+        off = np.arange(self.decode_M + 1, dtype=np.int32)
+        var = np.array([1 + (r % 2) for r in range(self.decode_M)], np.int32)
+        self.seg_off = torch.from_numpy(off).cuda()
+        self.seg_var = torch.from_numpy(var).cuda()
+        # one layer's worth of variant-3 buffers, reused layer after layer
+        self.wf3 = {nm: torch.empty((d_out, d_in), dtype=torch.bfloat16, device="cuda")
+                    for nm, d_out, d_in in self.shapes}
+        self.p3 = {nm: torch.empty((d_out, d_in // 8), dtype=torch.uint8, device="cuda")
+                   for nm, d_out, d_in in self.shapes}
+        self.a3 = {nm: torch.empty((d_out,), dtype=torch.float32, device="cuda")
+                   for nm, d_out, _ in self.shapes}
+        torch.cuda.synchronize()
+        n = sum(d_out * d_in for _, d_out, d_in in self.shapes)
+        self.weights_per_layer = n
+        self.prefill_flops = 2.0 * self.prefill_M * n * self.L
+        # decode: W_base once + both variants' signs and α + x + y, per layer
+        rows = sum(d_out for _, d_out, _ in self.shapes)
+        self.decode_bytes = self.L * (2 * n + 2 * (n / 8 + 4 * rows)
+                                      + 2 * self.decode_M * sum(d_in + d_out
+                                                                for _, d_out, d_in in self.shapes))
+        # compress: W_base + W_ft read, signs + α written, per layer
+        self.compress_bytes = self.L * (4 * n + n / 8 + 4 * rows)
+
+    def run_prefill(self):
+        for mats in self.layers:
+            for nm, d_out, d_in in self.shapes:
+                wb, var, _, _ = mats[nm]
+                self.bd.bitdelta_linear(self.xp[d_in], wb, var[0][0], var[0][1], per_row=True,
+                                        out=self.yp[nm])
+
+    def run_decode(self):
+        for mats in self.layers:
+            for nm, d_out, d_in in self.shapes:
+                wb, _, pt, at = mats[nm]
+                self.bd.bitdelta_linear_grouped(self.xd[d_in], self.seg_off, self.seg_var, wb, pt,
+                                                at, n_var=2, max_seg_len=1, per_row=True,
+                                                out=self.yd[nm])
+
+    def timed(self, fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e))
+        return statistics.median(times)
+
+    def compress_ms(self):
+        """Per layer: draw variant 3's W_ft (untimed), then time its four
+        compress calls with CUDA events; returns the sum over the 40 layers."""
+        import synth.device as sd
+        total = 0.0
+        for l, mats in enumerate(self.layers):
+            for i, (nm, d_out, d_in) in enumerate(self.shapes):
+                wb = mats[nm][0]
+                rc = sd._load().synth_finetuned_bf16(
+                    ctypes.c_void_p(self.wf3[nm].data_ptr()), ctypes.c_void_p(wb.data_ptr()),
+                    wb.numel(), self.seed, 50000 + 10 * l + i, self.b3, sd._stream())
+                if rc != 0:
+                    raise RuntimeError(f"synth_finetuned_bf16 failed: cuda error {rc}")
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for nm, d_out, d_in in self.shapes:
+                self.bd.bitdelta_compress(mats[nm][0], self.wf3[nm], per_row=True,
+                                          packed_out=self.p3[nm], alpha_out=self.a3[nm])
+            e.record()
+            torch.cuda.synchronize()
+            total += s.elapsed_time(e)
+        return total
+
+    def report(self):
+        pre = self.timed(self.run_prefill)
+        dec = self.timed(self.run_decode)
+        comp = self.compress_ms()
+        return {
+            "workload": self.name,
+            "prefill": {"ms": pre, "TFLOP/s": self.prefill_flops / (pre * 1e-3) / 1e12,
+                        "tokens": self.prefill_M, "launches": 4 * self.L},
+            "decode": {"ms_per_step": dec, "GB/s": self.decode_bytes / (dec * 1e-3) / 1e9,
+                       "batch": self.decode_M, "variants": "rows alternate 1,2,1,2,...",
+                       "launches": 4 * self.L},
+            "compress": {"ms": comp, "GB/s": self.compress_bytes / (comp * 1e-3) / 1e9,
+                         "ms_per_layer": comp / self.L},
+            "resident_weights_gb": (2 * self.weights_per_layer * self.L
+                                    + 2 * self.L * (self.weights_per_layer / 8)) / 1e9,
+        }
+
+
 # --------------------------------------------------------------------------- timing
 
 
@@ -694,7 +833,7 @@ def main():
 
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"prefill", "grouped"} if args.workloads == "all" else set())
+        {"prefill", "grouped", "slice40"} if args.workloads == "all" else set())
     if "prefill" in wanted:
         pre = Prefill(bd)
         pms, pph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
@@ -728,6 +867,11 @@ def main():
                          "frac_of_roofline_time": t_roof * 1e3 / per_call, "traffic": None},
         }
         del grp
+        torch.cuda.empty_cache()
+    if "slice40" in wanted:
+        sl = Slice40(bd)
+        workloads["slice40"] = sl.report()
+        del sl
         torch.cuda.empty_cache()
 
     e2e = e2e_decode(bd, 20)

@@ -29,6 +29,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Row-major 2D tensor map [rows, cols] of elem_bytes-sized elements with a
+// (box_cols x box_rows) box; out-of-range elements read as zero.  False when
+// the driver rejects it (alignment, strides, box) or cannot be reached.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+                    int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows,
+                    CUtensorMapSwizzle swizzle);
+
 // Current device's error word, wait limit and SM count (a bd_status code).
 int current_device_context(DevCtx* ctx, int* num_sms);
 
@@ -61,6 +68,7 @@ struct GemvArgs {
 };
 
 cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream);
+
 size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows);
 cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream);
 
