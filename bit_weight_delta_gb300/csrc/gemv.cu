@@ -264,6 +264,199 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
   __syncthreads();
 }
 
+// ------------------------------------------------------------------ mixed groups
+
+// Up to 16 short rows of up to kMaxGroupVars distinct delta variants (and any
+// number of base rows) computed in ONE pass over this CTA's W_base rows: the
+// base product x·W_baseᵀ covers every row of the group at once, and the delta
+// product of variant v uses x fragments in which the rows of other variants
+// are zero, so each row collects exactly its own variant's α_v·(x·S_vᵀ).
+constexpr int kMaxGroupVars = 4;
+
+struct MixedGroup {
+  int32_t rows[kMaxGroupRows];     // x/y row per slot, −1 = empty
+  int32_t slot_var[kMaxGroupRows]; // index into vars[] of the slot's variant; −1 = base or empty
+  int32_t vars[kMaxGroupVars];     // the group's delta variant ids (>= 1)
+  int32_t n_vars;
+};
+
+template <int NG, bool kSignVec>
+__device__ __forceinline__ void gemv_group_mixed(const GemvArgs& p, const MixedGroup& grp,
+                                                 float* red) {
+  constexpr int CPS = kCPS;
+  constexpr int V = kMaxGroupVars;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_in = p.d_in, d_out = p.d_out;
+  const int64_t row_bytes = d_in / 8;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * (8 * NG);
+  const int nv = grp.n_vars;
+
+  const int ra_idx = grp.rows[g], rb_idx = grp.rows[g + 8];
+  const int va = grp.slot_var[g], vb = grp.slot_var[g + 8];
+  const uint16_t* xra = ra_idx >= 0 ? p.x + static_cast<int64_t>(ra_idx) * d_in : nullptr;
+  const uint16_t* xrb = rb_idx >= 0 ? p.x + static_cast<int64_t>(rb_idx) * d_in : nullptr;
+
+  const uint16_t* wrow[NG];
+  const uint8_t* srow[V][NG];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    const int64_t n = n0 + 8 * ng + g;
+    wrow[ng] = n < d_out ? p.w + n * d_in : nullptr;
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      srow[v][ng] = (v < nv && n < d_out) ? p.packed_table[grp.vars[v] - 1] + n * row_bytes
+                                          : nullptr;
+  }
+
+  float acc_b[NG][4], acc_s[V][NG][4];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc_b[ng][e] = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc_s[v][ng][e] = 0.f;
+    }
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+
+  // one 32-column chunk: base product for all rows, delta product per variant
+  auto chunk = [&](const uint4 (&wv)[NG], const uint32_t (&sb)[V][NG], uint4 xa, uint4 xb) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      mma_16816(acc_b[ng], xa.x, xb.x, xa.y, xb.y, wv[ng].x, wv[ng].y);
+      mma_16816(acc_b[ng], xa.z, xb.z, xa.w, xb.w, wv[ng].z, wv[ng].w);
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      if (v < nv) {
+        const uint4 xav = va == v ? xa : zero4;
+        const uint4 xbv = vb == v ? xb : zero4;
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          const uint32_t b = sb[v][ng];
+          mma_16816(acc_s[v][ng], xav.x, xbv.x, xav.y, xbv.y, pm_one_pair(b, 0),
+                    pm_one_pair(b, 1));
+          mma_16816(acc_s[v][ng], xav.z, xbv.z, xav.w, xbv.w, pm_one_pair(b, 2),
+                    pm_one_pair(b, 3));
+        }
+      }
+    }
+  };
+
+  const int64_t n_sc = d_in / (32 * CPS);
+  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+    const int64_t kc0 = sc * 32 * CPS;
+    uint4 w[CPS][NG];
+    uint32_t sw[CPS][V][NG];
+    uint4 xa[CPS], xb[CPS];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+      for (int j = 0; j < CPS; ++j)
+        w[j][ng] = wrow[ng] != nullptr ? ldg_stream_v4(wrow[ng] + kc0 + 32 * j + 8 * t) : zero4;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        if (kSignVec) {
+          const uint4 q = srow[v][ng] != nullptr ? ldg_v4(srow[v][ng] + kc0 / 8) : zero4;
+          sw[0][v][ng] = q.x;
+          sw[1][v][ng] = q.y;
+          sw[2][v][ng] = q.z;
+          sw[3][v][ng] = q.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < CPS; ++j)
+            sw[j][v][ng] = srow[v][ng] != nullptr ? __ldg(srow[v][ng] + kc0 / 8 + 4 * j + t) : 0u;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CPS; ++j) {
+      xa[j] = xra != nullptr ? ldg_v4(xra + kc0 + 32 * j + 8 * t) : zero4;
+      xb[j] = xrb != nullptr ? ldg_v4(xrb + kc0 + 32 * j + 8 * t) : zero4;
+    }
+#pragma unroll
+    for (int j = 0; j < CPS; ++j) {
+      uint32_t sb[V][NG];
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng)
+          sb[v][ng] = kSignVec ? (sw[j][v][ng] >> (8 * t)) & 0xFFu : sw[j][v][ng];
+      uint4 wj[NG];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) wj[ng] = w[j][ng];
+      chunk(wj, sb, xa[j], xb[j]);
+    }
+  }
+  // tail: 32-column chunks past the last full super-chunk
+  for (int64_t c32 = n_sc * CPS + warp; c32 * 32 < d_in; c32 += kKW) {
+    const int64_t col = c32 * 32 + 8 * t;
+    const bool ok = col < d_in;
+    uint4 wv[NG];
+    uint32_t sb[V][NG];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      wv[ng] = (ok && wrow[ng] != nullptr) ? ldg_stream_v4(wrow[ng] + col) : zero4;
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        sb[v][ng] = (ok && srow[v][ng] != nullptr)
+                        ? static_cast<uint32_t>(__ldg(srow[v][ng] + col / 8))
+                        : 0xFFu;
+    }
+    const uint4 xa = (ok && xra != nullptr) ? ldg_v4(xra + col) : zero4;
+    const uint4 xb = (ok && xrb != nullptr) ? ldg_v4(xrb + col) : zero4;
+    chunk(wv, sb, xa, xb);
+  }
+
+  // y_part = acc_b + Σ_v α_v[n]·acc_s[v]  (for m = g, g+8; n = n0 + 8ng + 2t + {0,1})
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t n = n0 + 8 * ng + 2 * t + (e & 1);
+      float val = acc_b[ng][e];
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        if (v < nv && n < d_out) {
+          const float* al = p.alpha_table[grp.vars[v] - 1];
+          val = fmaf(p.per_row ? __ldg(al + n) : __ldg(al), acc_s[v][ng][e], val);
+        }
+      }
+      red[(warp * NG * 4 + ng * 4 + e) * 32 + lane] = val;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      float vsum[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float sum = 0.f;
+        for (int w = 0; w < kKW; ++w) sum += red[(w * NG * 4 + ng * 4 + e) * 32 + lane];
+        vsum[e] = sum;
+      }
+      const int64_t n = n0 + 8 * ng + 2 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = grp.rows[g + 8 * h];
+        if (row < 0 || n >= d_out) continue;
+        uint16_t* yr = p.y + static_cast<int64_t>(row) * d_out;
+        const uint32_t pk = pack_bf16x2_rn(vsum[2 * h], vsum[2 * h + 1]);
+        if (n + 1 < d_out && (d_out % 2) == 0) {
+          *reinterpret_cast<uint32_t*>(yr + n) = pk;
+        } else {
+          yr[n] = static_cast<uint16_t>(pk & 0xFFFFu);
+          if (n + 1 < d_out) yr[n + 1] = static_cast<uint16_t>(pk >> 16);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // Single variant: blockIdx.y (strided) picks 16 consecutive x rows.
 // Before waiting on the previous kernel in the stream, pull this CTA's slice
 // of W_base (and its sign rows) towards L2: weights stream from HBM while the
@@ -302,13 +495,13 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
   }
 }
 
-// Multi-tenant: rows of short segments, bucketed by variant into groups of
-// up to 16 rows.  Every CTA builds the same grouping in shared memory, then
-// covers its 8·NG output columns for every group.
+// Multi-tenant: rows of short segments, bucketed by variant, then taken in
+// groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
+// builds the same grouping in shared memory, then covers its 8·NG output
+// columns for every group.
 template <int NG>
 __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
   __shared__ float red[kKW * NG * 4 * 32];
-  __shared__ RowGroup grp;
   extern __shared__ int32_t dyn[];
   griddep_launch_dependents();
   griddep_wait();
@@ -359,24 +552,53 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
     for (int32_t r = a; r < b; ++r) rows[pos + (r - a)] = r;
   }
   __syncthreads();
-  // groups: each bucket in slices of 16 rows
-  for (int v = 0; v < nb; ++v) {
-    const int32_t b0 = start[v], b1 = start[v + 1];
-    for (int32_t r0 = b0; r0 < b1; r0 += kMaxGroupRows) {
-      if (threadIdx.x < kMaxGroupRows) {
-        const int32_t r = r0 + threadIdx.x;
-        grp.rows[threadIdx.x] = r < b1 ? rows[r] : -1;
+  // Groups of up to 16 rows taken in bucket (variant) order, closed early
+  // when a fifth delta variant would join: each group is one pass over this
+  // CTA's W_base rows.  Thread 0 forms the next group in shared memory.
+  __shared__ MixedGroup mg;
+  __shared__ int32_t cursor, bucket;
+  __shared__ int mg_vec;
+  const int32_t total = start[nb];
+  if (threadIdx.x == 0) {
+    cursor = 0;
+    bucket = 0;
+  }
+  __syncthreads();
+  while (cursor < total) {
+    if (threadIdx.x == 0) {
+      int i = 0, nvars = 0;
+      int32_t c = cursor, bk = bucket;
+      bool vec = p.d_in % 128 == 0;
+      while (i < kMaxGroupRows && c < total) {
+        while (c >= start[bk + 1]) ++bk;  // the bucket (variant) of sorted row c
+        int slot = -1;
+        if (bk > 0) {
+          if (nvars == 0 || mg.vars[nvars - 1] != bk) {
+            if (nvars == kMaxGroupVars) break;
+            mg.vars[nvars++] = bk;
+            vec = vec && (reinterpret_cast<uintptr_t>(p.packed_table[bk - 1]) & 15u) == 0;
+          }
+          slot = nvars - 1;
+        }
+        mg.rows[i] = rows[c];
+        mg.slot_var[i] = slot;
+        ++i;
+        ++c;
       }
-      if (threadIdx.x == 0) grp.variant = v;
-      __syncthreads();
-      const uint8_t* pk = v > 0 ? p.packed_table[v - 1] : nullptr;
-      const float* al = v > 0 ? p.alpha_table[v - 1] : nullptr;
-      const bool vec = (p.d_in % 128 == 0) && ((reinterpret_cast<uintptr_t>(pk) & 15u) == 0);
-      if (vec)
-        gemv_group<NG, kCPS, true, true>(p, grp, pk, al, v > 0, red);
-      else
-        gemv_group<NG, kCPS, true, false>(p, grp, pk, al, v > 0, red);
+      for (; i < kMaxGroupRows; ++i) {
+        mg.rows[i] = -1;
+        mg.slot_var[i] = -1;
+      }
+      mg.n_vars = nvars;
+      mg_vec = vec ? 1 : 0;
+      cursor = c;
+      bucket = bk;
     }
+    __syncthreads();
+    if (mg_vec)
+      gemv_group_mixed<NG, true>(p, mg, red);
+    else
+      gemv_group_mixed<NG, false>(p, mg, red);
   }
 }
 
