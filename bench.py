@@ -519,6 +519,72 @@ class Slice40:
         }
 
 
+class DeltaCacheLoads:
+    """The delta cache's cold loads: variants of 1 GiB each (packed signs and
+    α of about 17 GB of bf16 weights) in pinned host memory, a device arena of
+    two slots, requests cycling over four variants so every request after the
+    first two evicts and loads.  Reports the copy bandwidth and the time a
+    full 70B-model delta (8.75 GB, the page's figure) would take at it."""
+
+    name = "delta_cache_cold_loads_4x1GiB_variants_2_slots"
+    blob = 1 << 30
+
+    def __init__(self, bd):
+        self.bd = bd
+        self.blobs = []
+        for v in range(4):
+            b = torch.empty(self.blob, dtype=torch.uint8).pin_memory()
+            b.fill_(v + 1)
+            self.blobs.append(b)
+        arena = torch.empty(2 * self.blob, dtype=torch.uint8, device="cuda")
+        self.cache = bd.DeltaCache(arena, self.blob, pin_top_k=0)
+        for v, b in enumerate(self.blobs):
+            self.cache.register(v, b)
+
+    def report(self, requests: int = 12):
+        cache = self.cache
+        stream = torch.cuda.current_stream()
+        cache.acquire(0)
+        cache.release(0)
+        stream.synchronize()
+        base = cache.stats()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        s.record()
+        host_us = []
+        for i in range(requests):
+            v = 1 + i % 3          # 1, 2, 3, 1, ...: with two slots, every request misses
+            h0 = time.perf_counter()
+            cache.acquire(v)
+            host_us.append((time.perf_counter() - h0) * 1e6)
+            cache.release(v)
+        e.record()
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+        ms = s.elapsed_time(e)
+        st = cache.stats()
+        loaded = st["bytes_loaded"] - base["bytes_loaded"]
+        gbs = loaded / (ms * 1e-3) / 1e9
+        last = 1 + (requests - 1) % 3   # the variant requested last is resident
+        h0 = time.perf_counter()
+        for _ in range(100):       # hits: acquire and release of a resident variant
+            cache.acquire(last)
+            cache.release(last)
+        hit_us = (time.perf_counter() - h0) / 100 * 1e6
+        return {
+            "workload": self.name, "loads": st["loads"] - base["loads"],
+            "bytes_loaded": loaded, "ms": ms, "wall_s": wall, "GB/s": gbs,
+            "ms_for_8.75GB_delta": 8.75e9 / (gbs * 1e9) * 1e3,
+            "page_ms_for_8.75GB_delta": 200.0,
+            "acquire_host_us_median_on_miss": statistics.median(host_us),
+            "acquire_release_host_us_on_hit": hit_us,
+            "evictions": st["evictions"] - base["evictions"],
+        }
+
+    def close(self):
+        self.cache.close()
+
+
 # --------------------------------------------------------------------------- timing
 
 
@@ -833,7 +899,7 @@ def main():
 
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"prefill", "grouped", "slice40"} if args.workloads == "all" else set())
+        {"prefill", "grouped", "slice40", "cache"} if args.workloads == "all" else set())
     if "prefill" in wanted:
         pre = Prefill(bd)
         pms, pph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
@@ -872,6 +938,12 @@ def main():
         sl = Slice40(bd)
         workloads["slice40"] = sl.report()
         del sl
+        torch.cuda.empty_cache()
+    if "cache" in wanted:
+        dc = DeltaCacheLoads(bd)
+        workloads["delta_cache"] = dc.report()
+        dc.close()
+        del dc
         torch.cuda.empty_cache()
 
     e2e = e2e_decode(bd, 20)

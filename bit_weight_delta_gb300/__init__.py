@@ -25,7 +25,7 @@ PER_ROW = 1
 _STATUS = {
     0: "BD_OK", 1: "BD_ERR_INVALID_ARG", 2: "BD_ERR_UNSUPPORTED_SHAPE", 3: "BD_ERR_MISALIGNED",
     4: "BD_ERR_WORKSPACE", 5: "BD_ERR_CUDA", 6: "BD_ERR_DEVICE_TIMEOUT",
-    7: "BD_ERR_DEVICE_BOUNDS",
+    7: "BD_ERR_DEVICE_BOUNDS", 8: "BD_ERR_CACHE_FULL",
 }
 
 EXPORTED = (
@@ -33,6 +33,10 @@ EXPORTED = (
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
     "bitdelta_status_string", "bitdelta_compress_noalloc",
+)
+CACHE_EXPORTED = (
+    "bd_cache_create", "bd_cache_destroy", "bd_cache_register", "bd_cache_acquire",
+    "bd_cache_release", "bd_cache_get_stats", "bd_cache_slot_of",
 )
 
 
@@ -84,6 +88,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_debug_wait_timeout.restype = st
     lib.bitdelta_status_string.argtypes = [st]
     lib.bitdelta_status_string.restype = ctypes.c_char_p
+    lib.bd_cache_create.argtypes = [p, sz, sz, i32, st, p, ctypes.POINTER(p)]
+    lib.bd_cache_destroy.argtypes = [p]
+    lib.bd_cache_register.argtypes = [p, i32, p, sz]
+    lib.bd_cache_acquire.argtypes = [p, i32, p, ctypes.POINTER(p)]
+    lib.bd_cache_release.argtypes = [p, i32, p]
+    lib.bd_cache_get_stats.argtypes = [p, ctypes.POINTER(_CacheStats)]
+    lib.bd_cache_slot_of.argtypes = [p, i32, ctypes.POINTER(i32)]
+    for name in CACHE_EXPORTED:
+        getattr(lib, name).restype = st
     _lib = lib
     return lib
 
@@ -242,3 +255,91 @@ def bitdelta_set_wait_limit_ns(ns: int) -> None:
 
 def bitdelta_debug_wait_timeout(stream=None) -> None:
     _check("bitdelta_debug_wait_timeout", load().bitdelta_debug_wait_timeout(_stream(stream)))
+
+
+# --------------------------------------------------------------------------- delta cache
+
+
+class _CacheStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in
+                ("acquires", "hits", "queued_behind_load", "loads", "evictions", "bytes_loaded")]
+
+
+class DeltaCache:
+    """The delta cache of include/bitdelta_cache.h over a caller-owned arena.
+
+    arena: a contiguous uint8 tensor, CUDA (device arena: loads are async
+    host-to-device copies on `copy_stream`) or CPU (host arena: loads are
+    memcpy, no CUDA).  Variants are registered as contiguous CPU uint8
+    tensors (pinned memory lets the copies run asynchronously); the caller
+    keeps them alive.  acquire() returns a uint8 view of the variant's bytes
+    in the arena, valid until the matching release()."""
+
+    def __init__(self, arena: torch.Tensor, slot_bytes: int, pin_top_k: int = 6,
+                 copy_stream=None):
+        if arena.dtype != torch.uint8 or not arena.is_contiguous():
+            raise ValueError("arena must be a contiguous uint8 tensor")
+        self.arena = arena
+        self.device = arena.is_cuda
+        self.copy_stream = (copy_stream if copy_stream is not None else
+                            (torch.cuda.Stream(device=arena.device) if self.device else None))
+        handle = ctypes.c_void_p()
+        cs = ctypes.c_void_p(self.copy_stream.cuda_stream if self.device else 0)
+        _check("bd_cache_create", load().bd_cache_create(
+            _ptr(arena), arena.numel(), slot_bytes, pin_top_k, 0 if self.device else 1, cs,
+            ctypes.byref(handle)))
+        self.handle = handle
+        self.slot_bytes = slot_bytes
+        self._blobs = {}
+
+    def register(self, variant: int, blob: torch.Tensor) -> None:
+        if blob.is_cuda or blob.dtype != torch.uint8 or not blob.is_contiguous():
+            raise ValueError("a variant's blob must be a contiguous CPU uint8 tensor")
+        _check("bd_cache_register", load().bd_cache_register(self.handle, variant, _ptr(blob),
+                                                             blob.numel()))
+        self._blobs[variant] = blob
+
+    def _s(self, stream) -> ctypes.c_void_p:
+        return _stream(stream) if self.device else ctypes.c_void_p(0)
+
+    def acquire(self, variant: int, stream=None) -> torch.Tensor:
+        ptr = ctypes.c_void_p()
+        _check("bd_cache_acquire", load().bd_cache_acquire(self.handle, variant, self._s(stream),
+                                                           ctypes.byref(ptr)))
+        off = ptr.value - self.arena.data_ptr()
+        return self.arena[off:off + self._blobs[variant].numel()]
+
+    def release(self, variant: int, stream=None) -> None:
+        _check("bd_cache_release", load().bd_cache_release(self.handle, variant,
+                                                           self._s(stream)))
+
+    def try_acquire(self, variant: int, stream=None):
+        """acquire(), or None when the cache is full (BD_ERR_CACHE_FULL)."""
+        try:
+            return self.acquire(variant, stream)
+        except BitDeltaError as e:
+            if e.code == 8:
+                return None
+            raise
+
+    def slot_of(self, variant: int) -> int:
+        slot = ctypes.c_int32()
+        _check("bd_cache_slot_of", load().bd_cache_slot_of(self.handle, variant,
+                                                           ctypes.byref(slot)))
+        return slot.value
+
+    def stats(self) -> dict:
+        st = _CacheStats()
+        _check("bd_cache_get_stats", load().bd_cache_get_stats(self.handle, ctypes.byref(st)))
+        return {n: int(getattr(st, n)) for n, _ in _CacheStats._fields_}
+
+    def close(self) -> None:
+        if self.handle is not None:
+            _check("bd_cache_destroy", load().bd_cache_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

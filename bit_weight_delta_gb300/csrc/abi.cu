@@ -389,6 +389,8 @@ const char* bitdelta_status_string(bd_status status) {
       return "a bounded device wait ran out of time";
     case BD_ERR_DEVICE_BOUNDS:
       return "malformed segment table, variant id or table entry seen on the device";
+    case BD_ERR_CACHE_FULL:
+      return "delta cache full: every slot is held by a caller or pinned";
   }
   return "unknown status";
 }

@@ -59,7 +59,8 @@ typedef enum {
   BD_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
   BD_ERR_CUDA = 5,              /* a CUDA runtime call failed (launch, attribute) */
   BD_ERR_DEVICE_TIMEOUT = 6,    /* a bounded device wait ran out (check_error) */
-  BD_ERR_DEVICE_BOUNDS = 7      /* bad segment table / variant id seen on device */
+  BD_ERR_DEVICE_BOUNDS = 7,     /* bad segment table / variant id seen on device */
+  BD_ERR_CACHE_FULL = 8         /* delta cache: every slot held or pinned (bitdelta_cache.h) */
 } bd_status;
 
 typedef enum { BD_ALPHA_PER_MATRIX = 0, BD_ALPHA_PER_ROW = 1 } bd_alpha_mode;

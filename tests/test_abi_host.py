@@ -46,6 +46,16 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(bd.EXPORTED) == set(declared_functions())
 
 
+def test_library_exports_the_delta_cache(lib):
+    text = open(os.path.join(os.path.dirname(HEADER), "bitdelta_cache.h")).read()
+    declared = sorted(set(re.findall(r"\b(bd_cache_\w+)\s*\(", text)))
+    out = subprocess.run(["nm", "-D", "--defined-only", bd.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert declared and set(declared) <= exported
+    assert set(bd.CACHE_EXPORTED) == set(declared)
+
+
 def test_packed_bytes_and_workspace(lib):
     assert bd.bitdelta_packed_bytes(4096, 4096) == 4096 * 512   # "Infrastructure details"
     assert bd.bitdelta_packed_bytes(8, 16) == 16
@@ -55,8 +65,8 @@ def test_packed_bytes_and_workspace(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
-        assert bd.status_string(code)
+    for code in range(9):
+        assert bd.status_string(code) != "unknown status"
     assert bd.status_string(99) == "unknown status"
 
 
