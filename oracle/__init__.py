@@ -63,6 +63,8 @@ def _load():
         lib.orc_linear_grouped_at.argtypes = [p, i64, p, p, i32, p, p, p, i32, ctypes.c_int,
                                               i64, i64, p, p, i64, p]
         lib.orc_linear_grouped_at.restype = None
+        lib.orc_sign_cosine.argtypes = [p, p, p, p, ctypes.c_int, i64, i64, p]
+        lib.orc_sign_cosine.restype = None
         _lib = lib
     return _lib
 
@@ -176,3 +178,15 @@ def linear_grouped_at(x, seg_offsets, seg_variant, w_base, packed_list, alpha_li
                                   _ptr(wb), pk_arr, al_arr, n_var, int(per_row), d_out, d_in,
                                   _ptr(mi), _ptr(ni), mi.shape[0], _ptr(out))
     return out
+
+
+def sign_cosine(packed_a, alpha_a, packed_b, alpha_b, per_row: bool):
+    """[K-Merge] cosine of the task vectors α_a⊙S_a and α_b⊙S_b (1-bit form).
+    Returns (cos, dot, |a|², |b|²), all fp64."""
+    pa, pb = _c(packed_a, np.uint8), _c(packed_b, np.uint8)
+    aa, ab = _c(alpha_a, np.float32), _c(alpha_b, np.float32)
+    d_out, row_bytes = pa.shape
+    out = np.zeros(4, np.float64)
+    _load().orc_sign_cosine(_ptr(pa), _ptr(aa), _ptr(pb), _ptr(ab), int(per_row), d_out,
+                            row_bytes * 8, _ptr(out))
+    return tuple(float(v) for v in out)

@@ -271,4 +271,33 @@ void orc_linear_grouped(const uint16_t* x, int64_t M_total, const int32_t* seg_o
   }
 }
 
+// [K-Merge] Cosine similarity of two task vectors held in their 1-bit form:
+// Δ̂ = α ⊙ S with S[n][k] = +1 / −1 from bit k of row n and α per row (or one
+// α for the matrix).  cos = <Δ̂_a, Δ̂_b> / (‖Δ̂_a‖·‖Δ̂_b‖), every product and
+// sum in fp64, element by element over the unpacked signs (the definition as
+// written: no counting shortcut).  Outputs the three sums too.
+void orc_sign_cosine(const uint8_t* packed_a, const float* alpha_a, const uint8_t* packed_b,
+                     const float* alpha_b, int per_row, int64_t d_out, int64_t d_in,
+                     double* out4) {
+  const int64_t row_bytes = d_in / 8;
+  double dot = 0.0, na = 0.0, nb = 0.0;
+  for (int64_t r = 0; r < d_out; ++r) {
+    const double a = static_cast<double>(alpha_for_row(alpha_a, per_row, r));
+    const double b = static_cast<double>(alpha_for_row(alpha_b, per_row, r));
+    for (int64_t c = 0; c < d_in; ++c) {
+      const int bit_a = (packed_a[r * row_bytes + c / 8] >> (c % 8)) & 1;
+      const int bit_b = (packed_b[r * row_bytes + c / 8] >> (c % 8)) & 1;
+      const double ea = bit_a ? a : -a;
+      const double eb = bit_b ? b : -b;
+      dot += ea * eb;
+      na += ea * ea;
+      nb += eb * eb;
+    }
+  }
+  out4[0] = dot / std::sqrt(na * nb);
+  out4[1] = dot;
+  out4[2] = na;
+  out4[3] = nb;
+}
+
 }  // extern "C"

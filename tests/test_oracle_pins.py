@@ -325,3 +325,51 @@ def test_grouped_at_matches_full():
     ni = np.tile(np.arange(N), M)
     at = oracle.linear_grouped_at(x, off, var, wb, packs, alphas, True, mi, ni)
     assert np.array_equal(at, y.ravel())
+
+
+# ------------------------------------------------------------ K-Merge cosine
+# Page section "K-Merge": cosine similarity of task vectors; here of their
+# 1-bit form α ⊙ S (per-row α).
+
+
+def test_sign_cosine_hand_example():
+    """Two rows of 8 columns worked by hand: row 0 agrees on 7 of 8 signs
+    (Σ s_a·s_b = 6), row 1 on 4 of 8 (Σ = 0); α_a = (1/2, 1/4), α_b = (1, 2):
+    dot = 1/2·1·6 = 3, |a|² = 8/4 + 8/16 = 2.5, |b|² = 8 + 32 = 40,
+    cos = 3 / √100 = 0.3."""
+    pa = np.array([[0b10110010], [0xFF]], np.uint8)
+    pb = np.array([[0b10010010], [0x0F]], np.uint8)
+    cos, dot, na, nb = oracle.sign_cosine(pa, np.array([0.5, 0.25], np.float32), pb,
+                                          np.array([1.0, 2.0], np.float32), True)
+    assert (dot, na, nb) == (3.0, 2.5, 40.0)
+    assert cos == pytest.approx(0.3, abs=1e-15)
+
+
+def test_sign_cosine_identical_negated_and_symmetric():
+    rng = np.random.default_rng(5)
+    pa = rng.integers(0, 256, (12, 6), dtype=np.uint8)
+    pb = rng.integers(0, 256, (12, 6), dtype=np.uint8)
+    aa = rng.uniform(1e-4, 2e-3, 12).astype(np.float32)
+    ab = rng.uniform(1e-4, 2e-3, 12).astype(np.float32)
+    assert oracle.sign_cosine(pa, aa, pa, aa, True)[0] == pytest.approx(1.0, abs=1e-15)
+    assert oracle.sign_cosine(pa, aa, ~pa, aa, True)[0] == pytest.approx(-1.0, abs=1e-15)
+    c1 = oracle.sign_cosine(pa, aa, pb, ab, True)[0]
+    c2 = oracle.sign_cosine(pb, ab, pa, aa, True)[0]
+    assert c1 == c2 and -1.0 <= c1 <= 1.0
+    # a common scale of one side's α (a power of two: exact in fp32) does not
+    # change the cosine
+    assert oracle.sign_cosine(pa, aa, pb, 4 * ab, True)[0] == pytest.approx(c1, rel=1e-12)
+
+
+def test_sign_cosine_per_matrix_is_the_sign_agreement():
+    """With one α per matrix the cosine is (agreements − disagreements)/n,
+    counted here with numpy's unpackbits, whatever the two α values."""
+    rng = np.random.default_rng(6)
+    pa = rng.integers(0, 256, (9, 4), dtype=np.uint8)
+    pb = rng.integers(0, 256, (9, 4), dtype=np.uint8)
+    ua, ub = np.unpackbits(pa, bitorder="little"), np.unpackbits(pb, bitorder="little")
+    agree = int((ua == ub).sum())
+    want = (2 * agree - ua.size) / ua.size
+    got = oracle.sign_cosine(pa, np.array([7e-4], np.float32), pb, np.array([2e-3], np.float32),
+                             False)[0]
+    assert got == pytest.approx(want, abs=1e-15)
