@@ -585,6 +585,55 @@ class DeltaCacheLoads:
         self.cache.close()
 
 
+class KMergeSimilarity:
+    """K-Merge's first step on the grouped workload's layer (W_base
+    4096->14336, 14 variants): the cosine similarity of variant 1's 1-bit task
+    vector with the other 13 and the most similar of them.  Reads 14 packed
+    sign matrices of 7.34 MB (plus α)."""
+
+    name = "kmerge_similarity_14336x4096_1_vs_13"
+    d_out, d_in, n_var = 14336, 4096, 14
+
+    def __init__(self, bd, seed: int = 4):
+        import synth
+        import synth.device as sd
+        self.bd = bd
+        scales = synth.variant_scales(seed, self.n_var)
+        wb = sd.normal_bf16((self.d_out, self.d_in), seed, 100, 0.02)
+        self.packs, self.alphas = [], []
+        for v in range(self.n_var):
+            wf = sd.finetuned_bf16(wb, seed, 1000 + v, float(scales[v]))
+            p, a = bd.bitdelta_compress(wb, wf, per_row=True)
+            self.packs.append(p)
+            self.alphas.append(a)
+            del wf
+        self.pt, self.at = bd.variant_tables(self.packs[1:], self.alphas[1:], "cuda")
+        self.bytes = self.n_var * (self.d_out * self.d_in / 8 + 4 * self.d_out)
+
+    def report(self, reps=50):
+        n_b = self.n_var - 1
+        cos = torch.empty(n_b, dtype=torch.float64, device="cuda")
+        best = torch.empty(1, dtype=torch.int32, device="cuda")
+        ws = torch.empty(self.bd.bitdelta_sign_similarity_workspace_bytes(self.d_out, n_b) + 256,
+                         dtype=torch.uint8, device="cuda")
+        f = lambda: self.bd.bitdelta_sign_similarity(self.packs[0], self.alphas[0], self.pt,
+                                                     self.at, n_b, True, out=cos, best=best,
+                                                     workspace=ws)
+        f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / reps
+        return {"workload": self.name, "us_per_call": ms * 1e3,
+                "GB/s": self.bytes / (ms * 1e-3) / 1e9, "most_similar_variant": int(best.item()) + 2,
+                "cos_max": float(cos.max()), "cos_min": float(cos.min()),
+                "note": "per call: a 4-byte memset of the workspace counter + the kernel"}
+
+
 # --------------------------------------------------------------------------- timing
 
 
@@ -899,7 +948,8 @@ def main():
 
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"prefill", "grouped", "slice40", "cache"} if args.workloads == "all" else set())
+        {"prefill", "grouped", "slice40", "cache", "kmerge"} if args.workloads == "all"
+        else set())
     if "prefill" in wanted:
         pre = Prefill(bd)
         pms, pph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
@@ -938,6 +988,11 @@ def main():
         sl = Slice40(bd)
         workloads["slice40"] = sl.report()
         del sl
+        torch.cuda.empty_cache()
+    if "kmerge" in wanted:
+        km = KMergeSimilarity(bd)
+        workloads["kmerge"] = km.report()
+        del km
         torch.cuda.empty_cache()
     if "cache" in wanted:
         dc = DeltaCacheLoads(bd)

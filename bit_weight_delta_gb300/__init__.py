@@ -32,7 +32,8 @@ EXPORTED = (
     "bitdelta_packed_bytes", "bitdelta_compress_workspace_bytes", "bitdelta_compress",
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
-    "bitdelta_status_string", "bitdelta_compress_noalloc",
+    "bitdelta_status_string", "bitdelta_compress_noalloc", "bitdelta_sign_similarity",
+    "bitdelta_sign_similarity_workspace_bytes",
 )
 CACHE_EXPORTED = (
     "bd_cache_create", "bd_cache_destroy", "bd_cache_register", "bd_cache_acquire",
@@ -88,6 +89,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_debug_wait_timeout.restype = st
     lib.bitdelta_status_string.argtypes = [st]
     lib.bitdelta_status_string.restype = ctypes.c_char_p
+    lib.bitdelta_sign_similarity_workspace_bytes.argtypes = [i64, i32]
+    lib.bitdelta_sign_similarity_workspace_bytes.restype = sz
+    lib.bitdelta_sign_similarity.argtypes = [p, p, p, p, i32, st, i64, i64, p, p, p, sz, p]
+    lib.bitdelta_sign_similarity.restype = st
     lib.bd_cache_create.argtypes = [p, sz, sz, i32, st, p, ctypes.POINTER(p)]
     lib.bd_cache_destroy.argtypes = [p]
     lib.bd_cache_register.argtypes = [p, i32, p, sz]
@@ -255,6 +260,37 @@ def bitdelta_set_wait_limit_ns(ns: int) -> None:
 
 def bitdelta_debug_wait_timeout(stream=None) -> None:
     _check("bitdelta_debug_wait_timeout", load().bitdelta_debug_wait_timeout(_stream(stream)))
+
+
+def bitdelta_sign_similarity(packed_a, alpha_a, packed_table, alpha_table, n_b: int,
+                             per_row: bool = True, out=None, best=None, workspace=None,
+                             stream=None):
+    """Cosines of the candidate's 1-bit task vector with n_b pool members (page
+    section K-Merge).  packed_table / alpha_table: int64 CUDA tensors of device
+    pointers (variant_tables()).  Returns (cos [n_b] float64, best [1] int32),
+    both CUDA tensors; out / best / workspace (uint8, at least
+    bitdelta_sign_similarity_workspace_bytes() + 256 bytes) may be passed in
+    to avoid allocations."""
+    _dev(packed_a, torch.uint8, "packed_a")
+    _dev(alpha_a, torch.float32, "alpha_a")
+    d_out, row_bytes = packed_a.shape
+    need = bitdelta_sign_similarity_workspace_bytes(d_out, n_b)
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=packed_a.device)
+    off = (-workspace.data_ptr()) % 256
+    if out is None:
+        out = torch.empty(n_b, dtype=torch.float64, device=packed_a.device)
+    if best is None:
+        best = torch.empty(1, dtype=torch.int32, device=packed_a.device)
+    _check("bitdelta_sign_similarity", load().bitdelta_sign_similarity(
+        _ptr(packed_a), _ptr(alpha_a), _ptr(packed_table), _ptr(alpha_table), n_b,
+        _mode(per_row), d_out, row_bytes * 8, _ptr(out), _ptr(best),
+        ctypes.c_void_p(workspace.data_ptr() + off), workspace.numel() - off, _stream(stream)))
+    return out, best
+
+
+def bitdelta_sign_similarity_workspace_bytes(d_out: int, n_b: int) -> int:
+    return int(load().bitdelta_sign_similarity_workspace_bytes(d_out, n_b))
 
 
 # --------------------------------------------------------------------------- delta cache

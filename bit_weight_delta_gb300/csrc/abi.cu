@@ -358,6 +358,38 @@ bd_status bitdelta_check_error(bd_stream_t stream) {
   return BD_OK;
 }
 
+size_t bitdelta_sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b) {
+  if (d_out <= 0 || n_b < 1 || n_b > 256) return 0;
+  return 256 + static_cast<size_t>(bd::sign_similarity_grid(d_out)) *
+                   (2 * static_cast<size_t>(n_b) + 1) * sizeof(double);
+}
+
+bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a,
+                                   const uint8_t* const* packed_table,
+                                   const float* const* alpha_table, int32_t n_b,
+                                   bd_alpha_mode mode, int64_t d_out, int64_t d_in,
+                                   double* cos_out, int32_t* best_out, void* workspace,
+                                   size_t ws_bytes, bd_stream_t stream) {
+  if (!packed_a || !alpha_a || !packed_table || !alpha_table || !cos_out || !best_out ||
+      !workspace || !mode_ok(mode))
+    return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (n_b < 1 || n_b > 256) return BD_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(alpha_a, 4) || !aligned(packed_table, 8) || !aligned(alpha_table, 8) ||
+      !aligned(cos_out, 8) || !aligned(best_out, 4) || !aligned(workspace, 256))
+    return BD_ERR_MISALIGNED;
+  if (ws_bytes < bitdelta_sign_similarity_workspace_bytes(d_out, n_b)) return BD_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s) != cudaSuccess) return BD_ERR_CUDA;
+  const bool vec = d_in % 128 == 0 && aligned(packed_a, 16);
+  return from_cuda(bd::launch_sign_similarity(packed_a, alpha_a, packed_table, alpha_table, n_b,
+                                              mode == BD_ALPHA_PER_ROW, d_out, d_in, cos_out,
+                                              best_out, workspace, vec, s));
+}
+
 bd_status bitdelta_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns < 1000 ? 1000 : ns);
   return BD_OK;

@@ -106,6 +106,15 @@ cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
                              const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
                              cudaStream_t stream);
 
+// Cosine similarity of 1-bit task vectors (K-Merge); grid and workspace:
+// 256 bytes (a counter) + grid · (2·n_b + 1) doubles.
+int sign_similarity_grid(int64_t d_out);
+cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
+                                   const uint8_t* const* pb_table, const float* const* ab_table,
+                                   int32_t n_b, bool per_row, int64_t d_out, int64_t d_in,
+                                   double* cos_out, int32_t* best_out, void* workspace,
+                                   bool vec, cudaStream_t stream);
+
 // Test hook: one CTA waiting on an mbarrier nothing completes.
 cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream);
 

@@ -1,0 +1,203 @@
+// similarity.cu — cosine similarity of task vectors in their 1-bit form.
+//
+// Page "BitDelta: serving 14 Zen models from one GPU cluster", section
+// "K-Merge": when an adapter that is not in the pool is requested, compute its
+// pairwise cosine similarity with every pool member on the task vectors and
+// pick the most similar one.  Here the task vectors are the BitDelta deltas
+// α ⊙ S (S = ±1 from the packed signs), which is what a server that keeps
+// only the compressed deltas holds:
+//     <α_a⊙S_a, α_b⊙S_b> = Σ_n α_a[n]·α_b[n]·(d_in − 2·popcount(S_a[n] ⊕ S_b[n]))
+//     ‖α⊙S‖² = Σ_n α[n]²·d_in
+// (one α for the matrix: the same with α constant).  The row's agreement
+// count is an exact integer; the α products and sums are fp64.
+//
+// HBM-bound: the candidate's signs are read once, each member's once
+// ((1 + n_b)/16 bytes per weight).  A warp takes one row of the candidate at
+// a time into registers (16 bytes per lane per 4096 columns) and streams the
+// pool members' same row, eight members per round of loads.  Per-CTA partial
+// sums go to the caller's workspace; the last CTA to finish reduces them in a
+// fixed order (deterministic) and writes the cosines and the argmax.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bd {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRound = 8;  // pool members whose row loads are in flight together
+
+struct SimArgs {
+  const uint8_t* pa;
+  const float* aa;
+  const uint8_t* const* pb_table;
+  const float* const* ab_table;
+  int32_t n_b;
+  int per_row;
+  int64_t d_out, d_in;
+  double* cos_out;
+  int32_t* best_out;
+  double* partial;         // [gridDim.x][2·n_b + 1]: dot[b], norm_b[b], norm_a
+  unsigned int* counter;   // CTAs finished (reset by the last one)
+  int vec;                 // 16-byte loads allowed (d_in % 128 == 0, candidate aligned)
+};
+
+__device__ __forceinline__ int popc4(uint4 a, uint4 b) {
+  return __popc(a.x ^ b.x) + __popc(a.y ^ b.y) + __popc(a.z ^ b.z) + __popc(a.w ^ b.w);
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
+  extern __shared__ double sm[];  // [kWarps][2·n_b + 1]
+  __shared__ const uint8_t* s_pb[256];
+  __shared__ const float* s_ab[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_b = p.n_b;
+  const int stride_w = 2 * n_b + 1;
+  double* mine = sm + warp * stride_w;
+  for (int i = lane; i < stride_w; i += 32) mine[i] = 0.0;
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int b = threadIdx.x; b < n_b; b += kThreads) {
+    s_pb[b] = p.pb_table[b];
+    s_ab[b] = p.ab_table[b];
+  }
+  __syncthreads();
+
+  const int64_t row_bytes = p.d_in / 8;
+  const double d_in = static_cast<double>(p.d_in);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + warp; r < p.d_out;
+       r += static_cast<int64_t>(gridDim.x) * kWarps) {
+    const uint8_t* ra = p.pa + r * row_bytes;
+    const double alpha_a = static_cast<double>(p.per_row ? __ldg(p.aa + r) : __ldg(p.aa));
+    for (int b0 = 0; b0 < n_b; b0 += kRound) {
+      int cnt[kRound];
+#pragma unroll
+      for (int j = 0; j < kRound; ++j) cnt[j] = 0;
+      // lane j fetches member b0 + j's α for this row while the signs stream
+      const bool mine_j = lane < kRound && b0 + lane < n_b;
+      const float ab_j = mine_j ? (p.per_row ? __ldg(s_ab[b0 + lane] + r) : __ldg(s_ab[b0 + lane]))
+                                : 0.f;
+      bool v4 = p.vec != 0;  // 16-byte loads when every member row is 16-byte aligned
+#pragma unroll
+      for (int j = 0; j < kRound; ++j)
+        if (b0 + j < n_b) v4 = v4 && (reinterpret_cast<uintptr_t>(s_pb[b0 + j]) & 15u) == 0;
+      if (v4) {
+        for (int64_t off = 16 * lane; off < row_bytes; off += 512) {
+          const uint4 va = ldg_stream_v4(ra + off);
+          uint4 vb[kRound];
+#pragma unroll
+          for (int j = 0; j < kRound; ++j)
+            vb[j] = b0 + j < n_b ? ldg_stream_v4(s_pb[b0 + j] + r * row_bytes + off) : va;
+#pragma unroll
+          for (int j = 0; j < kRound; ++j) cnt[j] += popc4(va, vb[j]);
+        }
+      } else {
+        for (int64_t off = lane; off < row_bytes; off += 32) {
+          const uint32_t a = __ldg(ra + off);
+#pragma unroll
+          for (int j = 0; j < kRound; ++j)
+            if (b0 + j < n_b) cnt[j] += __popc(a ^ __ldg(s_pb[b0 + j] + r * row_bytes + off));
+        }
+      }
+      // every lane ends with every member's total; lane j keeps member b0 + j
+      int d_mine = 0;
+#pragma unroll
+      for (int j = 0; j < kRound; ++j) {
+        const int d = warp_sum(cnt[j]);  // disagreeing signs of row r with member b0 + j
+        if (lane == j) d_mine = d;
+      }
+      if (mine_j) {
+        const double alpha_b = static_cast<double>(ab_j);
+        mine[b0 + lane] += alpha_a * alpha_b * (d_in - 2.0 * d_mine);
+        mine[n_b + b0 + lane] += alpha_b * alpha_b * d_in;
+      }
+    }
+    if (lane == 0) mine[2 * n_b] += alpha_a * alpha_a * d_in;
+  }
+  __syncthreads();
+  // CTA partials in a fixed warp order
+  for (int i = threadIdx.x; i < stride_w; i += kThreads) {
+    double s = 0.0;
+    for (int w = 0; w < kWarps; ++w) s += sm[w * stride_w + i];
+    p.partial[static_cast<int64_t>(blockIdx.x) * stride_w + i] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ unsigned int last;
+  if (threadIdx.x == 0) last = atomicAdd(p.counter, 1u) == gridDim.x - 1 ? 1u : 0u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // The last CTA: totals over CTAs, then cosines and argmax.  Warp w takes
+  // the values i ≡ w (mod kWarps); lane l sums CTAs c ≡ l (mod 32) with
+  // independent loads, then a butterfly over the lanes: a fixed order for a
+  // given grid, so the result is deterministic.
+  double* tot = sm;  // reuse: [stride_w]
+  for (int i = warp; i < stride_w; i += kWarps) {
+    double s = 0.0;
+#pragma unroll 4
+    for (unsigned int c = lane; c < gridDim.x; c += 32)
+      s += p.partial[static_cast<int64_t>(c) * stride_w + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) tot[i] = s;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < n_b; b += kThreads)
+    p.cos_out[b] = tot[b] / sqrt(tot[2 * n_b] * tot[n_b + b]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = 0;
+    double bv = -2.0;
+    for (int b = 0; b < n_b; ++b) {
+      const double c = p.cos_out[b];
+      if (c > bv) {  // ties keep the lower index
+        bv = c;
+        best = b;
+      }
+    }
+    *p.best_out = best;
+    *p.counter = 0u;
+  }
+}
+
+}  // namespace
+
+int sign_similarity_grid(int64_t d_out) {
+  const int64_t want = (d_out + kWarps - 1) / kWarps;
+  return static_cast<int>(want < 512 ? want : 512);
+}
+
+cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
+                                   const uint8_t* const* pb_table, const float* const* ab_table,
+                                   int32_t n_b, bool per_row, int64_t d_out, int64_t d_in,
+                                   double* cos_out, int32_t* best_out, void* workspace,
+                                   bool vec, cudaStream_t stream) {
+  SimArgs a{};
+  a.pa = pa;
+  a.aa = aa;
+  a.pb_table = pb_table;
+  a.ab_table = ab_table;
+  a.n_b = n_b;
+  a.per_row = per_row ? 1 : 0;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.cos_out = cos_out;
+  a.best_out = best_out;
+  a.counter = static_cast<unsigned int*>(workspace);
+  a.partial = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + 256);
+  a.vec = vec ? 1 : 0;
+  const int grid = sign_similarity_grid(d_out);
+  const size_t smem = static_cast<size_t>(kWarps) * (2 * n_b + 1) * sizeof(double);
+  return launch_pdl(sign_similarity_kernel, dim3(grid), dim3(kThreads), smem, stream, a);
+}
+
+}  // namespace bd

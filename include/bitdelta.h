@@ -159,6 +159,34 @@ bd_status bitdelta_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft
                                     int64_t d_in, bd_alpha_mode mode, uint8_t* packed_out,
                                     float* alpha_out, bd_stream_t stream);
 
+/*
+ * Cosine similarity of task vectors in their 1-bit form (page section
+ * "K-Merge": when an adapter outside the pool is requested, its pairwise
+ * cosine similarity with every pool member on the task vectors decides the
+ * most similar member).  The task vectors are the BitDelta deltas α ⊙ S, S = ±1
+ * from the packed signs: for each pool member b
+ *     cos[b] = <α_a⊙S_a, α_b⊙S_b> / (‖α_a⊙S_a‖·‖α_b⊙S_b‖)
+ * computed as Σ_n α_a[n]·α_b[n]·(d_in − 2·popcount(S_a[n] xor S_b[n])) over
+ * the rows (fp64; one α per matrix in BD_ALPHA_PER_MATRIX mode).
+ *   packed_a, alpha_a      the candidate: packed [d_out, d_in/8], α [d_out] or [1]
+ *   packed_table[b], alpha_table[b]   device arrays of n_b pool members' pointers
+ *   n_b                    1 .. 256
+ *   cos_out                device double [n_b]
+ *   best_out               device int32 [1]: argmax of cos_out (ties: lowest b)
+ *   workspace              device, bitdelta_sign_similarity_workspace_bytes()
+ *                          bytes, 256-byte aligned; its first word is zeroed by
+ *                          the call (deterministic reduction, fixed order)
+ * Reads (1 + n_b) · d_out · d_in / 8 sign bytes.  Errors as bitdelta_linear
+ * (BD_ERR_UNSUPPORTED_SHAPE for n_b outside 1 .. 256).
+ */
+size_t bitdelta_sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b);
+bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a,
+                                   const uint8_t* const* packed_table,
+                                   const float* const* alpha_table, int32_t n_b,
+                                   bd_alpha_mode mode, int64_t d_out, int64_t d_in,
+                                   double* cos_out, int32_t* best_out, void* workspace,
+                                   size_t ws_bytes, bd_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device error word
  * of the current device (BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_DEVICE_BOUNDS),
  * or BD_ERR_CUDA if the synchronisation itself failed. */
