@@ -45,10 +45,11 @@ import torch  # noqa: E402
 
 METRIC = "bitdelta_linear TFLOP/s (prefill) & GB/s (decode) as % of GB300 roofline"
 # DRAM bytes (read + write) of one decode launch (4096 x 4096, M = 8) from an ncu
-# capture of `python bench.py --profile decode`, summarised in
-# profiles/gemv_single_decode_4096x4096_M8.md.  Valid for the gemv_single_kernel
-# build that capture was taken on; reset to None whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 35_769_600
+# capture of `python bench.py --profile decode`, summarised in the file named by
+# DECODE_PROFILE.  Valid for the kernel build that capture was taken on; reset
+# to None whenever that kernel changes.
+DECODE_TRAFFIC_BYTES = 35_762_176
+DECODE_PROFILE = "profiles/gemv_single_async_decode_4096x4096_M8.md"
 
 # --------------------------------------------------------------------------- peaks
 
@@ -1022,9 +1023,9 @@ def main():
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": DECODE_TRAFFIC_BYTES,
                          "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, "
-                                           "one M=8 launch (profiles/gemv_single_decode_"
-                                           "4096x4096_M8.md)",
-                         "kernel": "bitdelta_linear decode (gemv_single_kernel), M=1..16",
+                                           f"one M=8 launch ({DECODE_PROFILE})",
+                         "kernel": "bitdelta_linear decode: gemv_single_async_kernel (M=1..8), "
+                                   "gemv_single_kernel (M=16)",
                          "peak_source": peaks["source"]},
             "per_kernel": per_kernel,
             "cpu_baseline": cpu,

@@ -20,8 +20,12 @@
 // bytes) and the matching 8 columns of two x rows.  The columns inside a
 // fragment are permuted consistently for A and B, which a dot product allows.
 // Sign bits arrive as one 16-byte load per row per super-chunk of 128 columns;
-// each warp keeps two super-chunks of loads in flight.  Per weight the kernel
-// moves 2 + 1/8 bytes from HBM; x stays in L1/L2.  Launched with programmatic
+// each warp keeps two super-chunks of loads in flight in registers (M = 9..16,
+// and shapes without 16-byte sign rows).  For M <= 8 the "deep queue" kernel
+// instead routes W_base, signs and x through a per-warp cp.async ring in
+// shared memory (four super-chunks in flight per warp, no registers held) and
+// puts the W rows on the MMA's A side.  Per weight the kernels move
+// 2 + 1/8 bytes from HBM; x stays in L1/L2.  Launched with programmatic
 // dependent launch: the CTA prefetches its weight slice into L2 before it
 // waits for the previous kernel, so consecutive layers overlap.
 #include <cstdint>
@@ -95,6 +99,40 @@ struct Frag {
   uint4 xa[CPS];
   uint4 xb[kM16 ? CPS : 1];
 };
+
+// Warp 0 sums the KW warps' partial products in a fixed order and writes the
+// group's y rows (bf16, round to nearest even).
+template <int NG>
+__device__ __forceinline__ void store_group_rows(const GemvArgs& p, const RowGroup& grp,
+                                                 const float* red, int64_t n0, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_out = p.d_out;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float s = 0.f;
+      for (int w = 0; w < kKW; ++w) s += red[(w * NG * 4 + ng * 4 + e) * 32 + lane];
+      v[e] = s;
+    }
+    const int64_t n = n0 + 8 * ng + 2 * t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int slot = g + 8 * h;
+      const int row = grp.rows[slot];
+      if (row < 0 || n >= d_out) continue;
+      uint16_t* yr = p.y + static_cast<int64_t>(row) * d_out;
+      const uint32_t pk = pack_bf16x2_rn(v[2 * h], v[2 * h + 1]);
+      if (n + 1 < d_out && (d_out % 2) == 0) {
+        *reinterpret_cast<uint32_t*>(yr + n) = pk;
+      } else {
+        yr[n] = static_cast<uint16_t>(pk & 0xFFFFu);
+        if (n + 1 < d_out) yr[n + 1] = static_cast<uint16_t>(pk >> 16);
+      }
+    }
+  }
+}
 
 template <int NG, int CPS, bool kM16, bool kSignVec>
 __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& grp,
@@ -234,33 +272,238 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
     }
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0) store_group_rows<NG>(p, grp, red, n0, lane);
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ deep queue
+
+// The same products with W_base, the sign words and x routed through shared
+// memory by cp.async (the decode path for M <= 8): each warp keeps several
+// super-chunks of its rows in flight in its own slice of a ring, holding no
+// registers while they travel, where the register pipeline above holds two.
+// The copies are mapped for coalescing, not for the MMA fragments: one copy
+// instruction moves two whole 256-byte row segments (lanes 0-15 one row,
+// 16-31 the next), and the fragment reads come back from shared memory after
+// a warp barrier.  Row r's 16-byte word w sits at r·16 + (w ^ 4·(r & 1)), so
+// the fragment reads (rows g and g+1 in one 128-byte phase) hit distinct
+// banks.  The products use the swapped operands of chunk_mma_t.  Requires
+// d_in % 128 == 0 and 16-byte aligned sign rows.
+#ifndef BD_GEMV_ASYNC_MAX_M
+#define BD_GEMV_ASYNC_MAX_M 8
+#endif
+constexpr int kStageRows = 8 * kNG;  // W rows of a CTA
+// One warp's stage: W row segments, sign words, then the x segments of the
+// NT·8 token rows (x goes through the ring too: every CTA reads it from L2,
+// and a load issued one iteration ahead would not hide that latency).
+template <int NT>
+__host__ __device__ constexpr int stage_bytes() { return kStageRows * 256 + kStageRows * 16 + NT * 8 * 256; }
+// Ring depth: two CTAs per SM (a ~100 KB ring each).
+template <int NT>
+__host__ __device__ constexpr int ring_stages() { return NT == 1 ? 4 : 3; }
+template <int NT>
+constexpr size_t gemv_ring_bytes() {
+  return static_cast<size_t>(ring_stages<NT>()) * kKW * stage_bytes<NT>();
+}
+
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// x rows are read by every CTA at the same K position at about the same
+// time: keep them in L1 too (.ca), so the CTAs of an SM fetch each line from
+// L2 once instead of every warp queueing on the same few L2 lines.
+__device__ __forceinline__ void cp_async_16_x(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Operands swapped for the deep-queue path: the CTA's 16 W rows are the
+// m16 A operand (rows g and g+8 of the fragment are W rows n0+g and n0+8+g)
+// and up to 8 tokens are the n8 B operand, so M <= 8 issues half the MMAs of
+// the x-as-A form.  Same column permutation as chunk_mma: thread t's 16-byte
+// word (columns 8t..8t+7 of the chunk) feeds k-slots {2t, 2t+1, 2t+8, 2t+9}
+// of two MMAs.  C: c0/c1 = (row g, tokens 2t, 2t+1), c2/c3 = row g+8.
+template <int NT>
+__device__ __forceinline__ void chunk_mma_t(float (&acc_b)[NT][4], float (&acc_s)[NT][4],
+                                            const uint4 (&wv)[2], const uint32_t (&sb)[2],
+                                            const uint4 (&xv)[NT], bool has_delta) {
+  uint32_t s0[4], s1[4];
+  if (has_delta) {
 #pragma unroll
-    for (int ng = 0; ng < NG; ++ng) {
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float s = 0.f;
-        for (int w = 0; w < kKW; ++w) s += red[(w * NG * 4 + ng * 4 + e) * 32 + lane];
-        v[e] = s;
-      }
-      const int64_t n = n0 + 8 * ng + 2 * t;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int slot = g + 8 * h;
-        const int row = grp.rows[slot];
-        if (row < 0 || n >= d_out) continue;
-        uint16_t* yr = p.y + static_cast<int64_t>(row) * d_out;
-        const uint32_t pk = pack_bf16x2_rn(v[2 * h], v[2 * h + 1]);
-        if (n + 1 < d_out && (d_out % 2) == 0) {
-          *reinterpret_cast<uint32_t*>(yr + n) = pk;
-        } else {
-          yr[n] = static_cast<uint16_t>(pk & 0xFFFFu);
-          if (n + 1 < d_out) yr[n + 1] = static_cast<uint16_t>(pk >> 16);
-        }
-      }
+    for (int i = 0; i < 4; ++i) {
+      s0[i] = pm_one_pair(sb[0], i);
+      s1[i] = pm_one_pair(sb[1], i);
     }
   }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    mma_16816(acc_b[nt], wv[0].x, wv[1].x, wv[0].y, wv[1].y, xv[nt].x, xv[nt].y);
+    mma_16816(acc_b[nt], wv[0].z, wv[1].z, wv[0].w, wv[1].w, xv[nt].z, xv[nt].w);
+    if (has_delta) {
+      mma_16816(acc_s[nt], s0[0], s1[0], s0[1], s1[1], xv[nt].x, xv[nt].y);
+      mma_16816(acc_s[nt], s0[2], s1[2], s0[3], s1[3], xv[nt].z, xv[nt].w);
+    }
+  }
+}
+
+// Warp 0 sums the KW warps' partial products (transposed fragments) in a
+// fixed order and writes y[token][n] (bf16, round to nearest even).
+template <int NT>
+__device__ __forceinline__ void store_group_rows_t(const GemvArgs& p, const RowGroup& grp,
+                                                   const float* red, int64_t n0, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = 0.f;
+      for (int w = 0; w < kKW; ++w) v += red[(w * NT * 4 + nt * 4 + e) * 32 + lane];
+      const int64_t n = n0 + g + 8 * (e >> 1);
+      const int row = grp.rows[8 * nt + 2 * t + (e & 1)];
+      if (row < 0 || n >= p.d_out) continue;
+      p.y[static_cast<int64_t>(row) * p.d_out + n] =
+          static_cast<uint16_t>(pack_bf16x2_rn(v, 0.f) & 0xFFFFu);
+    }
+  }
+}
+
+template <int NG, bool kM16>
+__device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGroup& grp,
+                                                 const uint8_t* __restrict__ packed,
+                                                 const float* __restrict__ alpha, bool has_delta,
+                                                 float* red, uint8_t* ring) {
+  static_assert(NG == kNG, "ring sized for kNG row groups");
+  constexpr int CPS = kCPS;
+  constexpr int R = 8 * NG;
+  constexpr int NT = kM16 ? 2 : 1;  // token tiles of 8
+  constexpr int D = ring_stages<NT>();
+  constexpr int kSB = stage_bytes<NT>();
+  constexpr int kXOff = R * 256 + R * 16;  // x segments within a stage
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_in = p.d_in, d_out = p.d_out;
+  const int64_t row_bytes = d_in / 8;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int64_t rows_here = d_out - n0 < R ? d_out - n0 : R;
+
+  bool x_ok[NT];  // token slot g (+8) holds a row of x
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) x_ok[nt] = grp.rows[g + 8 * nt] >= 0;
+
+  bool row_ok[NG];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) row_ok[ng] = 8 * ng + g < rows_here;
+
+  float acc_b[NT][4], acc_s[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc_b[nt][e] = acc_s[nt][e] = 0.f;
+
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  uint8_t* const wring = ring + static_cast<size_t>(warp) * D * kSB;
+  const uint32_t wring_sa = smem_addr(wring);
+
+  // copy side: lane L moves word (L & 15) of rows 2k + (L >> 4), k = 0..R/2-1,
+  // and lanes 0..R-1 the sign word of row L
+  const int cr = lane >> 4, cw = lane & 15;
+  const uint16_t* const wsrc0 = p.w + (n0 + cr) * d_in + 8 * cw;
+  const uint8_t* const ssrc0 = packed + (n0 + lane) * row_bytes;
+  // x rows copied by this lane: token slots 2k + cr, k = 0..4·NT-1
+  const uint16_t* xsrc[4 * NT];
+#pragma unroll
+  for (int k = 0; k < 4 * NT; ++k) {
+    const int row = grp.rows[2 * k + cr];
+    xsrc[k] = row >= 0 ? p.x + static_cast<int64_t>(row) * d_in + 8 * cw : nullptr;
+  }
+  const int64_t n_sc = d_in / (32 * CPS);
+  auto issue = [&](int s, int64_t sc) {
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * 32 * CPS;
+      const uint32_t st = wring_sa + s * kSB;
+#pragma unroll
+      for (int k = 0; k < R / 2; ++k) {
+        const int r = 2 * k + cr;
+        if (r < rows_here)
+          cp_async_16_cg(st + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), wsrc0 + 2 * k * d_in + kc0);
+      }
+      if (has_delta && lane < rows_here && lane < R)
+        cp_async_16_cg(st + R * 256 + 16u * lane, ssrc0 + kc0 / 8);
+#pragma unroll
+      for (int k = 0; k < 4 * NT; ++k) {
+        const int r = 2 * k + cr;
+        if (xsrc[k] != nullptr)
+          cp_async_16_x(st + kXOff + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), xsrc[k] + kc0);
+      }
+    }
+    cp_async_commit();  // one group per stage, empty past the end
+  };
+
+  int64_t next = warp;
+#pragma unroll
+  for (int s = 0; s < D - 1; ++s) {
+    issue(s, next);
+    next += kKW;
+  }
+  int s_rd = 0;
+  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+    __syncwarp();  // every lane is done reading the slot refilled next
+    issue(s_rd == 0 ? D - 1 : s_rd - 1, next);
+    next += kKW;
+    cp_async_wait<D - 1>();  // this lane's copies of the stage have landed
+    __syncwarp();            // ... and every other lane's
+    const uint8_t* st = wring + s_rd * kSB;
+    uint4 sw[NG];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+      sw[ng] = (row_ok[ng] && has_delta)
+                   ? *reinterpret_cast<const uint4*>(st + R * 256 + 16 * (8 * ng + g))
+                   : zero4;
+#pragma unroll
+    for (int j = 0; j < CPS; ++j) {
+      uint4 wv[NG];
+      uint32_t sb[NG];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        const int r = 8 * ng + g;
+        wv[ng] = row_ok[ng] ? *reinterpret_cast<const uint4*>(
+                                  st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
+                            : zero4;
+        const uint32_t word = j == 0 ? sw[ng].x : j == 1 ? sw[ng].y : j == 2 ? sw[ng].z : sw[ng].w;
+        sb[ng] = (word >> (8 * t)) & 0xFFu;
+      }
+      uint4 xv[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r = 8 * nt + g;
+        xv[nt] = x_ok[nt] ? *reinterpret_cast<const uint4*>(
+                                st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
+                          : zero4;
+      }
+      chunk_mma_t<NT>(acc_b, acc_s, wv, sb, xv, has_delta);
+    }
+    s_rd = s_rd == D - 1 ? 0 : s_rd + 1;
+  }
+  cp_async_wait<0>();
+
+  // y_part = acc_b + α_n·acc_s (n = W row of the fragment), then the
+  // fixed-order reduction over warps
+  float a_row[2] = {0.f, 0.f};
+  if (has_delta) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t n = n0 + g + 8 * h;
+      a_row[h] = n < d_out ? (p.per_row ? __ldg(alpha + n) : __ldg(alpha)) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      red[(warp * NT * 4 + nt * 4 + e) * 32 + lane] =
+          has_delta ? fmaf(a_row[e >> 1], acc_s[nt][e], acc_b[nt][e]) : acc_b[nt][e];
+  __syncthreads();
+  if (warp == 0) store_group_rows_t<NT>(p, grp, red, n0, lane);
   __syncthreads();
 }
 
@@ -495,6 +738,28 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
   }
 }
 
+// Single variant through the deep cp.async queue (d_in % 128 == 0, aligned
+// sign rows); same grid, prefetch and dependent-launch protocol as above.
+template <int NG, bool kM16>
+__global__ void __launch_bounds__(kKW * 32) gemv_single_async_kernel(GemvArgs p) {
+  extern __shared__ __align__(16) uint8_t ring[];
+  __shared__ float red[kKW * NG * 4 * 32];
+  __shared__ RowGroup grp;
+  if (blockIdx.y == 0) prefetch_weights<NG>(p);
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
+  for (int64_t c = blockIdx.y; c < n_chunks; c += gridDim.y) {
+    if (threadIdx.x < kMaxGroupRows) {
+      const int64_t r = c * kMaxGroupRows + threadIdx.x;
+      grp.rows[threadIdx.x] = r < p.M ? static_cast<int32_t>(r) : -1;
+    }
+    if (threadIdx.x == 0) grp.variant = 1;
+    __syncthreads();
+    gemv_group_async<NG, kM16>(p, grp, p.packed, p.alpha, true, red, ring);
+  }
+}
+
 // Multi-tenant: rows of short segments, bucketed by variant, then taken in
 // groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
 // builds the same grouping in shared memory, then covers its 8·NG output
@@ -610,6 +875,27 @@ cudaError_t launch_single(const GemvArgs& p, bool sign_vec, cudaStream_t stream)
             static_cast<unsigned>(n_chunks < 65535 ? n_chunks : 65535));
   const bool m16 = p.M > 8;
   const dim3 block(kKW * 32);
+  if (sign_vec && p.M <= BD_GEMV_ASYNC_MAX_M) {
+    // The ring needs more than the default 48 KB of dynamic shared memory:
+    // raise the limit once per device (outside any capture in practice: the
+    // first call on a device).
+    static bool attr_set[64][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const size_t smem = m16 ? gemv_ring_bytes<2>() : gemv_ring_bytes<1>();
+    if (!attr_set[dev][m16 ? 1 : 0]) {
+      e = cudaFuncSetAttribute(m16 ? gemv_single_async_kernel<NG, true>
+                                   : gemv_single_async_kernel<NG, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_set[dev][m16 ? 1 : 0] = true;
+    }
+    if (m16) return launch_pdl(gemv_single_async_kernel<NG, true>, grid, block, smem, stream, p);
+    return launch_pdl(gemv_single_async_kernel<NG, false>, grid, block, smem, stream, p);
+  }
   if (m16 && sign_vec)
     return launch_pdl(gemv_single_kernel<NG, true, true>, grid, block, 0, stream, p);
   if (m16) return launch_pdl(gemv_single_kernel<NG, true, false>, grid, block, 0, stream, p);
