@@ -190,3 +190,11 @@ def sign_cosine(packed_a, alpha_a, packed_b, alpha_b, per_row: bool):
     _load().orc_sign_cosine(_ptr(pa), _ptr(aa), _ptr(pb), _ptr(ab), int(per_row), d_out,
                             row_bytes * 8, _ptr(out))
     return tuple(float(v) for v in out)
+
+
+def monosoup_merge(w_base, w_ft_list, rank: int):
+    """[MonoSoup] W_base + (1/k)·Σ rank-r truncated SVD of each Δ_i.
+    Returns (W_merged bf16 bits, W_merged fp64, correction fp64);
+    see oracle/monosoup.py."""
+    from . import monosoup as _ms
+    return _ms.monosoup(_c(w_base, np.uint16), [_c(w, np.uint16) for w in w_ft_list], rank)

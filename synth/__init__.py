@@ -103,3 +103,28 @@ def variant_scales(seed: int, n_var: int, lo: float = 5e-4, hi: float = 2e-3) ->
     """Per-variant Laplace scales b_v ~ U[lo, hi]."""
     g = _rng(seed, 6)
     return g.uniform(lo, hi, size=n_var)
+
+
+def monosoup_checkpoints(seed: int, w_base: np.ndarray, k: int, rank: int,
+                         s_hi: float = 1.0, s_lo: float = 0.5, noise_b: float = 1e-4):
+    """k fine-tuned checkpoints W_i = bf16(W_base + Δ_i) for the MonoSoup merge.
+
+    Following the page's MonoSoup section (fine-tuning moves a model along a
+    few high-variance directions in weight space), each Δ_i is a rank-``rank``
+    signal plus small dense noise: Σ_j s_j·a_j·b_jᵀ with s_j spaced
+    geometrically from s_hi down to s_lo, a_j ~ N(0, 1/d_out) and
+    b_j ~ N(0, 1/d_in) drawn independently (near-orthogonal, near-unit columns
+    for d >> rank), plus Laplace(0, noise_b) per element.  Returns a list of
+    bf16 bit-pattern arrays.
+    """
+    d_out, d_in = w_base.shape
+    base = bf16_to_f32(w_base).astype(np.float64)
+    s = np.geomspace(s_hi, s_lo, rank) if rank > 0 else np.zeros(0)
+    out = []
+    for i in range(k):
+        g = _rng(seed, 100 + i)
+        a = g.standard_normal((d_out, rank)) / np.sqrt(d_out)
+        b = g.standard_normal((d_in, rank)) / np.sqrt(d_in)
+        delta = (a * s) @ b.T + g.laplace(0.0, noise_b, size=(d_out, d_in))
+        out.append(bf16_bits((base + delta).astype(np.float32)))
+    return out
