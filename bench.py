@@ -635,6 +635,56 @@ class KMergeSimilarity:
                 "note": "per call: a 4-byte memset of the workspace counter + the kernel"}
 
 
+class MonoSoupMerge:
+    """MonoSoup merge of k = 4 fine-tuned checkpoints of one 4096 x 4096 layer
+    at rank 32 (two power iterations).  Each checkpoint's Δ_i is a rank-32
+    signal plus Laplace(0, 1e-4) noise (synth.monosoup_checkpoints)."""
+
+    name = "monosoup_4096x4096_k4_rank32_q2"
+    d_out = d_in = 4096
+    k, rank, q = 4, 32, 2
+
+    def __init__(self, bd, seed: int = 6):
+        import synth
+        self.bd = bd
+        wb = synth.base_weight(seed, self.d_out, self.d_in)
+        ws = synth.monosoup_checkpoints(seed, wb, self.k, self.rank)
+        dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)
+        self.wb = dev(wb)
+        self.ws = [dev(w) for w in ws]
+        self.out = torch.empty_like(self.wb)
+        self.ws_buf = torch.empty(
+            bd.bitdelta_monosoup_workspace_bytes(self.d_out, self.d_in, self.k, self.rank) + 256,
+            dtype=torch.uint8, device="cuda")
+        n = self.d_out * self.d_in
+        passes = 2 * self.q + 2          # products with Δ_i per checkpoint
+        self.bytes = self.k * passes * 4 * n + 4 * n
+        self.flops = self.k * passes * 2 * n * self.rank + 2 * n * self.k * self.rank
+
+    def report(self, reps=10):
+        f = lambda: self.bd.bitdelta_monosoup(self.wb, self.ws, self.rank, power_iters=self.q,
+                                              seed=1, out=self.out, workspace=self.ws_buf)
+        for _ in range(2):
+            f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / reps
+        # fp32 FMA peak: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        tflops = self.flops / (ms * 1e-3) / 1e12
+        return {"workload": self.name, "ms_per_merge": ms,
+                "GB/s": self.bytes / (ms * 1e-3) / 1e9, "TFLOP/s_fp32": tflops,
+                "roofline": {"bound": "alu", "achieved": tflops, "peak": alu_peak,
+                             "unit": "TFLOP/s", "frac": tflops / alu_peak, "traffic": None,
+                             "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+                "algorithmic": {"bytes": self.bytes, "flops": self.flops}}
+
+
 # --------------------------------------------------------------------------- timing
 
 
@@ -949,7 +999,8 @@ def main():
 
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"prefill", "grouped", "slice40", "cache", "kmerge"} if args.workloads == "all"
+        {"prefill", "grouped", "slice40", "cache", "kmerge", "monosoup"}
+        if args.workloads == "all"
         else set())
     if "prefill" in wanted:
         pre = Prefill(bd)
@@ -994,6 +1045,11 @@ def main():
         km = KMergeSimilarity(bd)
         workloads["kmerge"] = km.report()
         del km
+        torch.cuda.empty_cache()
+    if "monosoup" in wanted:
+        ms_wl = MonoSoupMerge(bd)
+        workloads["monosoup"] = ms_wl.report()
+        del ms_wl
         torch.cuda.empty_cache()
     if "cache" in wanted:
         dc = DeltaCacheLoads(bd)

@@ -33,7 +33,8 @@ EXPORTED = (
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
     "bitdelta_status_string", "bitdelta_compress_noalloc", "bitdelta_sign_similarity",
-    "bitdelta_sign_similarity_workspace_bytes",
+    "bitdelta_sign_similarity_workspace_bytes", "bitdelta_monosoup",
+    "bitdelta_monosoup_workspace_bytes",
 )
 CACHE_EXPORTED = (
     "bd_cache_create", "bd_cache_destroy", "bd_cache_register", "bd_cache_acquire",
@@ -93,6 +94,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_sign_similarity_workspace_bytes.restype = sz
     lib.bitdelta_sign_similarity.argtypes = [p, p, p, p, i32, st, i64, i64, p, p, p, sz, p]
     lib.bitdelta_sign_similarity.restype = st
+    lib.bitdelta_monosoup_workspace_bytes.argtypes = [i64, i64, i32, i32]
+    lib.bitdelta_monosoup_workspace_bytes.restype = sz
+    lib.bitdelta_monosoup.argtypes = [p, p, i32, i32, i32, ctypes.c_uint64, i64, i64, p, p, p,
+                                      sz, p]
+    lib.bitdelta_monosoup.restype = st
     lib.bd_cache_create.argtypes = [p, sz, sz, i32, st, p, ctypes.POINTER(p)]
     lib.bd_cache_destroy.argtypes = [p]
     lib.bd_cache_register.argtypes = [p, i32, p, sz]
@@ -291,6 +297,40 @@ def bitdelta_sign_similarity(packed_a, alpha_a, packed_table, alpha_table, n_b: 
 
 def bitdelta_sign_similarity_workspace_bytes(d_out: int, n_b: int) -> int:
     return int(load().bitdelta_sign_similarity_workspace_bytes(d_out, n_b))
+
+
+def bitdelta_monosoup_workspace_bytes(d_out: int, d_in: int, k: int, rank: int) -> int:
+    return int(load().bitdelta_monosoup_workspace_bytes(d_out, d_in, k, rank))
+
+
+def bitdelta_monosoup(w_base, w_fts, rank: int, power_iters: int = 2, seed: int = 0,
+                      out=None, correction=None, workspace=None, stream=None):
+    """MonoSoup merge (page section MonoSoup): W_base + (1/k)·Σ rank-r truncated
+    SVD of each W_i − W_base.  w_fts: list of k bf16 CUDA tensors shaped like
+    w_base.  Returns W_merged (bf16); `correction` (float32 CUDA tensor, same
+    shape) receives (1/k)·Σ τ_i when given; `workspace` (uint8, at least
+    bitdelta_monosoup_workspace_bytes() + 256 bytes) may be passed in."""
+    _dev(w_base, torch.bfloat16, "w_base")
+    d_out, d_in = w_base.shape
+    k = len(w_fts)
+    for i, w in enumerate(w_fts):
+        _dev(w, torch.bfloat16, f"w_fts[{i}]")
+        if tuple(w.shape) != (d_out, d_in):
+            raise ValueError("every checkpoint must have the shape of w_base")
+    if out is None:
+        out = torch.empty_like(w_base)
+    if correction is not None:
+        _dev(correction, torch.float32, "correction")
+    need = bitdelta_monosoup_workspace_bytes(d_out, d_in, max(k, 1), rank)
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=w_base.device)
+    off = (-workspace.data_ptr()) % 256
+    table = (ctypes.c_void_p * max(k, 1))(*[w.data_ptr() for w in w_fts])
+    _check("bitdelta_monosoup", load().bitdelta_monosoup(
+        _ptr(w_base), ctypes.cast(table, ctypes.c_void_p), k, rank, power_iters, seed, d_out,
+        d_in, _ptr(out), _ptr(correction) if correction is not None else None,
+        ctypes.c_void_p(workspace.data_ptr() + off), workspace.numel() - off, _stream(stream)))
+    return out
 
 
 # --------------------------------------------------------------------------- delta cache

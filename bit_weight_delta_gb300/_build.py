@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", "bitdelta")
 LIB_PATH = os.path.join(HERE, "libbitdelta.so")
 
 SOURCES = ["abi.cu", "compress.cu", "reconstruct.cu", "gemv.cu", "gemm_tc.cu", "gemm_pair.cu",
-           "cache.cu", "similarity.cu"]
+           "cache.cu", "similarity.cu", "monosoup.cu"]
 HEADERS = ["common.cuh", "kernels.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -390,6 +390,46 @@ bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a
                                               best_out, workspace, vec, s));
 }
 
+size_t bitdelta_monosoup_workspace_bytes(int64_t d_out, int64_t d_in, int32_t k, int32_t rank) {
+  if (check_dims(d_out, d_in) != BD_OK || k < 1 || k > 64 || rank < 0 || rank > 64) return 0;
+  return bd::monosoup_workspace_bytes(d_out, d_in, k, rank);
+}
+
+bd_status bitdelta_monosoup(const uint16_t* w_base, const uint16_t* const* w_ft, int32_t k,
+                            int32_t rank, int32_t power_iters, uint64_t seed, int64_t d_out,
+                            int64_t d_in, uint16_t* w_merged, float* correction, void* workspace,
+                            size_t ws_bytes, bd_stream_t stream) {
+  if (!w_base || !w_ft || !w_merged || !workspace) return BD_ERR_INVALID_ARG;
+  bd_status st = check_dims(d_out, d_in);
+  if (st != BD_OK) return st;
+  if (k < 1 || k > 64 || rank < 0 || rank > 64 || rank > d_out || rank > d_in ||
+      power_iters < 0 || power_iters > 16)
+    return BD_ERR_UNSUPPORTED_SHAPE;
+  for (int32_t i = 0; i < k; ++i) {
+    if (!w_ft[i]) return BD_ERR_INVALID_ARG;
+    if (!aligned(w_ft[i], 16)) return BD_ERR_MISALIGNED;
+  }
+  if (!aligned(w_base, 16) || !aligned(w_merged, 16) || !aligned(correction, 16) ||
+      !aligned(workspace, 256))
+    return BD_ERR_MISALIGNED;
+  if (ws_bytes < bd::monosoup_workspace_bytes(d_out, d_in, k, rank)) return BD_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != BD_OK) return st;
+  bd::MonoSoupArgs a{};
+  a.w_base = w_base;
+  a.w_ft = w_ft;
+  a.k = k;
+  a.rank = rank;
+  a.power_iters = power_iters;
+  a.seed = seed;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.w_merged = w_merged;
+  a.correction = correction;
+  return from_cuda(bd::launch_monosoup(a, workspace, dev->num_sms,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bd_status bitdelta_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns < 1000 ? 1000 : ns);
   return BD_OK;

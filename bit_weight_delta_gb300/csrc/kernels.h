@@ -115,6 +115,20 @@ cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
                                    double* cos_out, int32_t* best_out, void* workspace,
                                    bool vec, cudaStream_t stream);
 
+// MonoSoup merge (monosoup.cu).  w_ft: host array of k device pointers.
+struct MonoSoupArgs {
+  const uint16_t* w_base;
+  const uint16_t* const* w_ft;
+  int k, rank, power_iters;
+  uint64_t seed;
+  int64_t d_out, d_in;
+  uint16_t* w_merged;
+  float* correction;  // nullable: fp32 (1/k)·Σ τ_i
+};
+size_t monosoup_workspace_bytes(int64_t d_out, int64_t d_in, int k, int rank);
+cudaError_t launch_monosoup(const MonoSoupArgs& a, void* workspace, int num_sms,
+                            cudaStream_t stream);
+
 // Test hook: one CTA waiting on an mbarrier nothing completes.
 cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream);
 

@@ -187,6 +187,35 @@ bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a
                                    double* cos_out, int32_t* best_out, void* workspace,
                                    size_t ws_bytes, bd_stream_t stream);
 
+/*
+ * MonoSoup merge of k fine-tuned checkpoints of one base (page section
+ * "MonoSoup: complementing the single checkpoint with SVD"):
+ *     W_merged = W_base + (1/k) · Σ_i τ_i,  τ_i = rank-r truncated SVD of
+ *     Δ_i = W_i − W_base.
+ * τ_i is computed by block subspace iteration on Δ_i (formed on the fly, never
+ * stored): a ±1 sketch drawn from `seed`, power_iters rounds of Δᵀ/Δ products
+ * each followed by a Cholesky-QR orthonormalisation, then τ_i = Y·Yᵀ·Δ_i.  It
+ * reaches the truncated SVD when Δ_i has a gap after its r-th singular value
+ * (error shrinking like (σ_{r+1}/σ_r)^(2·power_iters+1)); without a gap it
+ * returns a rank-r approximation close to it, not the exact truncation.
+ *   w_base       device bf16 [d_out, d_in].
+ *   w_ft         HOST array of k device pointers, each bf16 [d_out, d_in].
+ *   k            1..64 checkpoints;  rank 0..64 and <= min(d_out, d_in)
+ *                (rank 0: W_merged = W_base);  power_iters 0..16.
+ *   w_merged     device bf16 [d_out, d_in] (must not overlap the inputs):
+ *                bf16_rne(fp32(W_base) + fp32 correction).
+ *   correction   device fp32 [d_out, d_in] or NULL: the correction
+ *                (1/k)·Σ τ_i before rounding.
+ *   workspace    device, 256-byte aligned, >= bitdelta_monosoup_workspace_bytes.
+ * Errors as bitdelta_linear; BD_ERR_UNSUPPORTED_SHAPE for k, rank or
+ * power_iters out of range.
+ */
+size_t bitdelta_monosoup_workspace_bytes(int64_t d_out, int64_t d_in, int32_t k, int32_t rank);
+bd_status bitdelta_monosoup(const uint16_t* w_base, const uint16_t* const* w_ft, int32_t k,
+                            int32_t rank, int32_t power_iters, uint64_t seed, int64_t d_out,
+                            int64_t d_in, uint16_t* w_merged, float* correction, void* workspace,
+                            size_t ws_bytes, bd_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device error word
  * of the current device (BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_DEVICE_BOUNDS),
  * or BD_ERR_CUDA if the synchronisation itself failed. */
