@@ -942,6 +942,11 @@ def run_profile(kind: str):
         y = torch.empty((2048, 8192), dtype=torch.bfloat16, device="cuda")
         for _ in range(4):
             bd.bitdelta_linear(x, wb, p, a, per_row=True, out=y)
+    elif kind == "monosoup":
+        ms_wl = MonoSoupMerge(bd)
+        for _ in range(2):
+            bd.bitdelta_monosoup(ms_wl.wb, ms_wl.ws, ms_wl.rank, power_iters=ms_wl.q, seed=1,
+                                 out=ms_wl.out, workspace=ms_wl.ws_buf)
     else:
         raise SystemExit(f"unknown profile kind {kind}")
     torch.cuda.synchronize()

@@ -8,7 +8,7 @@
 // τ_i by block subspace iteration on Δ_i, which is formed on the fly in fp32
 // from the two bf16 matrices and never stored:
 //     Y = orth(Δ·Ω)                         Ω: d_in × r, entries ±1
-//     q times:  Z = orth(Δᵀ·Y),  Y = orth(Δ·Z)
+//     q times:  Z = Δᵀ·Y,  Y = orth(Δ·Z)
 //     Y = orth(Y);  R = Δᵀ·Y                τ_i = Y·Rᵀ = Y·Yᵀ·Δ
 // Y·Yᵀ·Δ is Δ projected onto the span of Y; once that span is the dominant
 // r-dimensional left singular subspace of Δ, it equals the truncated SVD.
@@ -33,10 +33,15 @@ namespace bd {
 namespace {
 
 constexpr int kMsThreads = 256;
-constexpr int kTileA = 64;   // rows of the long side per CTA
+constexpr int kMulThreads = 128;  // threads of a Δ-product CTA
+constexpr int kTileA = 128;  // rows of the long side per Δ-product CTA
 constexpr int kTileB = 32;   // contracted indices per step
-constexpr int kMaxSplit = 16;
-constexpr int kMaxGramParts = 256;
+constexpr int kMaxSplit = 32;
+
+constexpr int kMaxCkpt = 64;
+struct CkptTable {  // the checkpoints' W_i, passed by value
+  const uint16_t* p[kMaxCkpt];
+};
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -64,207 +69,296 @@ __global__ void sketch_fill_kernel(float* omega, int64_t d_in, int r, int rp, ui
 // out[a][j] = Σ_b Δ(a, b)·V[b][j] over b in this CTA's split.
 //   kT = false: a = row n of Δ, b = column c   (Y = Δ·V,  V: d_in × RP)
 //   kT = true:  a = column c,   b = row n      (Z = Δᵀ·V, V: d_out × RP)
-// Grid (ceil(A / 64), S); split s covers b in [s·b_chunk, (s+1)·b_chunk) and
-// writes part[s][a][j] (or out directly when S == 1).
+// Grid (ceil(A / 128), S, k); split s covers b in [s·b_chunk, (s+1)·b_chunk)
+// and writes part[s][a][j] (or the output directly when S == 1); blockIdx.z
+// picks the checkpoint.  128 threads; a thread
+// owns 8 a × RP/8 j.  The next step's Δ vectors and V values are loaded into
+// registers while the current step's products run.
 template <int RP, bool kT>
-__global__ void __launch_bounds__(kMsThreads) delta_mul_kernel(
-    const uint16_t* __restrict__ wft, const uint16_t* __restrict__ wb, int64_t d_out,
-    int64_t d_in, const float* __restrict__ v, float* __restrict__ out, int64_t b_chunk) {
-  constexpr int JW = RP / 16;  // output columns per thread
+__global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
+    CkptTable tab, const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
+    const float* __restrict__ v_all, int64_t v_stride, float* __restrict__ dst_all,
+    int64_t dst_stride, int64_t b_chunk) {
+  // checkpoint z: its W_i, its V (v_stride 0: one V for all) and its output
+  // (dst_stride apart; split s at dst + s·A·RP)
+  const uint16_t* __restrict__ wft = tab.p[blockIdx.z];
+  const float* __restrict__ v = v_all + blockIdx.z * v_stride;
+  constexpr int TJ = RP / 8;                  // j per thread
+  constexpr int VQ = kTileB * RP / 4 / kMulThreads;  // float4 of V per thread per step
   __shared__ __align__(16) float ds[kTileB][kTileA + 4];  // [b][a]
   __shared__ __align__(16) float vs[kTileB][RP];
   const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;
+  const int ty = tid >> 3, tx = tid & 7;      // 16 groups of 8 a, 8 groups of TJ j
   const int64_t A = kT ? d_in : d_out;
   const int64_t B = kT ? d_out : d_in;
   const int64_t a0 = static_cast<int64_t>(blockIdx.x) * kTileA;
   const int64_t b_lo = static_cast<int64_t>(blockIdx.y) * b_chunk;
   const int64_t b_hi = b_lo + b_chunk < B ? b_lo + b_chunk : B;
 
-  float acc[4][JW];
+  // loader geometry: 4 vectors of 8 bf16 per matrix per thread per step
+  //   !kT: rows a0 + (tid >> 2) + 32·u, columns b0 + 8·(tid & 3)
+  //    kT: rows b0 + (tid >> 4) + 8·u,  columns a0 + 8·(tid & 15)
+  uint4 pf[4], pb[4];
+  float4 pv[VQ];
+  auto load = [&](int64_t b0) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < JW; ++j) acc[i][j] = 0.f;
-
-  for (int64_t b0 = b_lo; b0 < b_hi; b0 += kTileB) {
-    // Δ tile: 64 a × 32 b, 256 vectors of 8 bf16 (one per thread)
-    if (!kT) {
-      const int row = tid >> 2, vec = tid & 3;
-      const int64_t n = a0 + row, c = b0 + 8 * vec;
-      float f[8];
-      if (n < d_out && c < b_hi) {
-        float fb[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(wft + n * d_in + c)), f);
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(wb + n * d_in + c)), fb);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] -= fb[e];
+    for (int u = 0; u < 4; ++u) {
+      int64_t n, c;
+      bool ok;
+      if (!kT) {
+        n = a0 + (tid >> 2) + 32 * u;
+        c = b0 + 8 * (tid & 3);
+        ok = n < d_out && c < b_hi;
       } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        n = b0 + (tid >> 4) + 8 * u;
+        c = a0 + 8 * (tid & 15);
+        ok = n < b_hi && c < d_in;
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ds[8 * vec + e][row] = f[e];
-    } else {
-      const int row = tid >> 3, vec = tid & 7;
-      const int64_t n = b0 + row, c = a0 + 8 * vec;
-      float f[8];
-      if (n < b_hi && c < d_in) {
-        float fb[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(wft + n * d_in + c)), f);
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(wb + n * d_in + c)), fb);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] -= fb[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = 0.f;
-      }
-      *reinterpret_cast<float4*>(&ds[row][8 * vec]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(&ds[row][8 * vec + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+      pf[u] = ok ? __ldg(reinterpret_cast<const uint4*>(wft + n * d_in + c)) : make_uint4(0, 0, 0, 0);
+      pb[u] = ok ? __ldg(reinterpret_cast<const uint4*>(wb + n * d_in + c)) : make_uint4(0, 0, 0, 0);
     }
-    // V tile: 32 b × RP
-    for (int q = tid; q < kTileB * RP / 4; q += kMsThreads) {
-      const int bb = q / (RP / 4), j4 = q % (RP / 4);
+#pragma unroll
+    for (int q = 0; q < VQ; ++q) {
+      const int idx = tid + q * kMulThreads;
+      const int bb = idx / (RP / 4), j4 = idx % (RP / 4);
       const int64_t b = b0 + bb;
-      *reinterpret_cast<float4*>(&vs[bb][4 * j4]) =
-          b < b_hi ? __ldg(reinterpret_cast<const float4*>(v + b * RP) + j4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      pv[q] = b < b_hi ? __ldg(reinterpret_cast<const float4*>(v + b * RP) + j4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float f[8], fb[8];
+      bf16x8_to_f32(pf[u], f);
+      bf16x8_to_f32(pb[u], fb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] -= fb[e];   // Δ, exact in fp32
+      if (!kT) {
+        const int row = (tid >> 2) + 32 * u, col = 8 * (tid & 3);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ds[col + e][row] = f[e];
+      } else {
+        const int row = (tid >> 4) + 8 * u, col = 8 * (tid & 15);
+        *reinterpret_cast<float4*>(&ds[row][col]) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(&ds[row][col + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < VQ; ++q) {
+      const int idx = tid + q * kMulThreads;
+      *reinterpret_cast<float4*>(&vs[idx / (RP / 4)][4 * (idx % (RP / 4))]) = pv[q];
+    }
+  };
+
+  float acc[8][TJ];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < TJ; ++j) acc[i][j] = 0.f;
+
+  if (b_lo < b_hi) load(b_lo);
+  for (int64_t b0 = b_lo; b0 < b_hi; b0 += kTileB) {
+    stash();
     __syncthreads();
-#pragma unroll 8
+    if (b0 + kTileB < b_hi) load(b0 + kTileB);   // in flight during the products
+#pragma unroll 4
     for (int bb = 0; bb < kTileB; ++bb) {
-      const float4 a4 = *reinterpret_cast<const float4*>(&ds[bb][4 * ty]);
-      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-      float vv[JW];
+      const float4 x0 = *reinterpret_cast<const float4*>(&ds[bb][8 * ty]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&ds[bb][8 * ty + 4]);
+      const float av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      float vv[TJ];
+      if constexpr (TJ % 4 == 0) {
 #pragma unroll
-      for (int j = 0; j < JW; ++j) vv[j] = vs[bb][JW * tx + j];
+        for (int j = 0; j < TJ; j += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(&vs[bb][TJ * tx + j]);
+          vv[j] = t4.x;
+          vv[j + 1] = t4.y;
+          vv[j + 2] = t4.z;
+          vv[j + 3] = t4.w;
+        }
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < TJ; j += 2) {
+          const float2 t2 = *reinterpret_cast<const float2*>(&vs[bb][TJ * tx + j]);
+          vv[j] = t2.x;
+          vv[j + 1] = t2.y;
+        }
+      }
 #pragma unroll
-        for (int j = 0; j < JW; ++j) acc[i][j] = fmaf(av[i], vv[j], acc[i][j]);
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TJ; ++j) acc[i][j] = fmaf(av[i], vv[j], acc[i][j]);
     }
     __syncthreads();
   }
-  float* dst = out + static_cast<int64_t>(blockIdx.y) * A * RP;
+  float* dst = dst_all + blockIdx.z * dst_stride + static_cast<int64_t>(blockIdx.y) * A * RP;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t a = a0 + 4 * ty + i;
+  for (int i = 0; i < 8; ++i) {
+    const int64_t a = a0 + 8 * ty + i;
     if (a >= A) continue;
 #pragma unroll
-    for (int j = 0; j < JW; ++j) dst[a * RP + JW * tx + j] = acc[i][j];
+    for (int j = 0; j < TJ; j += 2)
+      *reinterpret_cast<float2*>(dst + a * RP + TJ * tx + j) = make_float2(acc[i][j], acc[i][j + 1]);
   }
 }
 
-// out[i] = Σ_s part[s][i], s in order.
-__global__ void reduce_parts_kernel(const float* __restrict__ part, int n_part, int64_t n,
-                                    float* __restrict__ out) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float s = 0.f;
-    for (int p = 0; p < n_part; ++p) s += part[p * n + i];
-    out[i] = s;
-  }
-}
-
-// gpart[cta] = Σ over this CTA's rows of A[row]ᵀ·A[row]  (RP × RP).
+// Checkpoint blockIdx.y, rows [r_lo, r_lo + kSlab) (1024 threads): A[row] = Σ_s part[s][row]
+// (s in order; skipped when n_split == 0, A being complete already), then
+// gpart[cta] = Σ_rows A[row]ᵀ·A[row] (RP × RP).
+constexpr int kSlab = 128;
+constexpr int kRgThreads = 1024;
 template <int RP>
-__global__ void __launch_bounds__(kMsThreads) gram_partial_kernel(const float* __restrict__ a,
-                                                                  int64_t m, int64_t rows_per_cta,
-                                                                  float* __restrict__ gpart) {
-  constexpr int JW = RP / 16;
-  __shared__ __align__(16) float rows[32][RP];
+__global__ void __launch_bounds__(kRgThreads) reduce_gram_kernel(
+    const float* __restrict__ part_all, int n_split, float* __restrict__ a_all,
+    int64_t a_stride, int64_t m, float* __restrict__ gpart_all) {
+  __shared__ __align__(16) float rows[kSlab][RP];
   const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;
-  const int64_t r_lo = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
-  const int64_t r_hi = r_lo + rows_per_cta < m ? r_lo + rows_per_cta : m;
-  float acc[JW][JW];
+  const int64_t z = blockIdx.y;  // checkpoint
+  const float* __restrict__ part = part_all + z * n_split * m * RP;
+  float* __restrict__ a = a_all + z * a_stride;
+  float* __restrict__ gpart = gpart_all + z * gridDim.x * RP * RP;
+  const int64_t r_lo = static_cast<int64_t>(blockIdx.x) * kSlab;
+  for (int q = tid; q < kSlab * RP / 4; q += kRgThreads) {
+    const int rr = q / (RP / 4), j4 = q % (RP / 4);
+    const int64_t row = r_lo + rr;
+    float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < m) {
+      if (n_split > 0) {
+        for (int sp0 = 0; sp0 < n_split; sp0 += 8) {
+          float4 t[8];
 #pragma unroll
-  for (int i = 0; i < JW; ++i)
+          for (int u = 0; u < 8; ++u)
+            t[u] = sp0 + u < n_split
+                       ? __ldg(reinterpret_cast<const float4*>(part + ((sp0 + u) * m + row) * RP) + j4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < JW; ++j) acc[i][j] = 0.f;
-  for (int64_t r0 = r_lo; r0 < r_hi; r0 += 32) {
-    for (int q = tid; q < 32 * RP / 4; q += kMsThreads) {
-      const int rr = q / (RP / 4), j4 = q % (RP / 4);
-      const int64_t row = r0 + rr;
-      *reinterpret_cast<float4*>(&rows[rr][4 * j4]) =
-          row < r_hi ? __ldg(reinterpret_cast<const float4*>(a + row * RP) + j4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    for (int rr = 0; rr < 32; ++rr) {
-      float ai[JW], aj[JW];
-#pragma unroll
-      for (int i = 0; i < JW; ++i) {
-        ai[i] = rows[rr][JW * ty + i];
-        aj[i] = rows[rr][JW * tx + i];
+          for (int u = 0; u < 8; ++u) {
+            v4.x += t[u].x;
+            v4.y += t[u].y;
+            v4.z += t[u].z;
+            v4.w += t[u].w;
+          }
+        }
+        reinterpret_cast<float4*>(a + row * RP)[j4] = v4;
+      } else {
+        v4 = reinterpret_cast<const float4*>(a + row * RP)[j4];
       }
-#pragma unroll
-      for (int i = 0; i < JW; ++i)
-#pragma unroll
-        for (int j = 0; j < JW; ++j) acc[i][j] = fmaf(ai[i], aj[j], acc[i][j]);
     }
-    __syncthreads();
+    *reinterpret_cast<float4*>(&rows[rr][4 * j4]) = v4;
   }
-  float* g = gpart + static_cast<int64_t>(blockIdx.x) * RP * RP;
-#pragma unroll
-  for (int i = 0; i < JW; ++i)
-#pragma unroll
-    for (int j = 0; j < JW; ++j) g[(JW * ty + i) * RP + JW * tx + j] = acc[i][j];
+  __syncthreads();
+  float* gp = gpart + static_cast<int64_t>(blockIdx.x) * RP * RP;
+  for (int q = tid; q < RP * RP; q += kRgThreads) {
+    const int i = q / RP, j = q % RP;
+    float s0 = 0.f, s1 = 0.f;
+    for (int rr = 0; rr < kSlab; rr += 2) {
+      s0 = fmaf(rows[rr][i], rows[rr][j], s0);
+      s1 = fmaf(rows[rr + 1][i], rows[rr + 1][j], s1);
+    }
+    gp[q] = s0 + s1;
+  }
 }
 
 // One CTA: G = Σ gpart (in order), G = L·Lᵀ over the leading r × r block,
 // T = L⁻ᵀ (RP × RP, zero outside r × r and in the columns of dropped pivots).
+// Every thread takes part in the partial sums; warp 0 alone then factorises
+// (lane L owns rows L and L + 32, warp barriers only) and inverts row by row
+// (lane L owns columns L and L + 32: row i of L⁻¹ needs only the lane's own
+// column of the rows above it, so that phase needs no barrier at all).
 template <int RP>
-__global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(const float* __restrict__ gpart,
-                                                                  int n_part, int r,
-                                                                  float* __restrict__ t_out) {
-  __shared__ float g[RP][RP + 1];   // G, then L⁻¹ (lower) once L is complete
-  __shared__ float l[RP][RP + 1];
+__global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(
+    const float* __restrict__ gpart_all, int n_part, int r, float* __restrict__ t_all) {
+  constexpr int OWN = RP > 32 ? 2 : 1;  // rows / columns per lane
+  // one CTA per checkpoint
+  const float* __restrict__ gpart = gpart_all + static_cast<int64_t>(blockIdx.x) * n_part * RP * RP;
+  float* __restrict__ t_out = t_all + static_cast<int64_t>(blockIdx.x) * RP * RP;
+  __shared__ float g[RP][RP + 1];       // G (lower part), factorised in place into L
+  __shared__ float x[RP][RP + 1];       // L⁻¹
   __shared__ float inv_d[RP];
-  __shared__ float thr;
   const int tid = threadIdx.x;
-  for (int q = tid; q < RP * RP; q += kMsThreads) {
-    float s = 0.f;
-    for (int p = 0; p < n_part; ++p) s += gpart[static_cast<int64_t>(p) * RP * RP + q];
-    g[q / RP][q % RP] = s;
-    l[q / RP][q % RP] = 0.f;
+  const int lane = tid & 31;
+  // Σ_p gpart[p]: float4 columns, partials p ≡ u (mod 4) in chain u, the
+  // chains added in order at the end
+  for (int q4 = tid; q4 < RP * RP / 4; q4 += kMsThreads) {
+    float4 cs[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) cs[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int p0 = 0; p0 < n_part; p0 += 4) {
+      float4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        t[u] = p0 + u < n_part
+                   ? __ldg(reinterpret_cast<const float4*>(gpart + static_cast<int64_t>(p0 + u) * RP * RP) + q4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        cs[u].x += t[u].x;
+        cs[u].y += t[u].y;
+        cs[u].z += t[u].z;
+        cs[u].w += t[u].w;
+      }
+    }
+    const float sv[4] = {cs[0].x + cs[1].x + cs[2].x + cs[3].x, cs[0].y + cs[1].y + cs[2].y + cs[3].y,
+                         cs[0].z + cs[1].z + cs[2].z + cs[3].z, cs[0].w + cs[1].w + cs[2].w + cs[3].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int q = 4 * q4 + e;
+      g[q / RP][q % RP] = sv[e];
+      x[q / RP][q % RP] = 0.f;
+    }
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid < 32) {
     float mx = 0.f;
-    for (int j = 0; j < r; ++j) mx = fmaxf(mx, g[j][j]);
-    thr = 1e-6f * mx;
-  }
-  __syncthreads();
-  for (int j = 0; j < r; ++j) {
-    if (tid == 0) {
+#pragma unroll
+    for (int o = 0; o < OWN; ++o)
+      if (lane + 32 * o < r) mx = fmaxf(mx, g[lane + 32 * o][lane + 32 * o]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const float thr = 1e-6f * mx;
+    // right-looking Cholesky: column j of L replaces column j of G
+    for (int j = 0; j < r; ++j) {
       const float d = g[j][j];
       const bool live = d > thr && thr > 0.f;
       const float sd = live ? sqrtf(d) : 0.f;
-      l[j][j] = sd;
-      inv_d[j] = live ? 1.f / sd : 0.f;
+      const float id = live ? 1.f / sd : 0.f;
+      __syncwarp();
+#pragma unroll
+      for (int o = 0; o < OWN; ++o) {
+        const int i = lane + 32 * o;
+        if (i == j) g[j][j] = sd;
+        if (i > j && i < r) g[i][j] *= id;
+      }
+      if (lane == 0) inv_d[j] = id;
+      __syncwarp();
+#pragma unroll
+      for (int o = 0; o < OWN; ++o) {
+        const int i = lane + 32 * o;
+        if (i <= j || i >= r) continue;
+        const float lij = g[i][j];
+#pragma unroll 4
+        for (int k = j + 1; k <= i; ++k) g[i][k] = fmaf(-lij, g[k][j], g[i][k]);
+      }
+      __syncwarp();
     }
-    __syncthreads();
-    for (int i = j + 1 + tid; i < r; i += kMsThreads) l[i][j] = g[i][j] * inv_d[j];
-    __syncthreads();
-    const int w = r - j - 1;  // trailing block (i, k) with j < k <= i < r
-    for (int q = tid; q < w * w; q += kMsThreads) {
-      const int i = j + 1 + q / w, k = j + 1 + q % w;
-      if (k <= i) g[i][k] -= l[i][j] * l[k][j];
-    }
-    __syncthreads();
-  }
-  // X = L⁻¹ by forward substitution, one column per thread, into g
-  float (*x)[RP + 1] = g;
-  for (int q = tid; q < RP * RP; q += kMsThreads) x[q / RP][q % RP] = 0.f;
-  __syncthreads();
-  if (tid < r) {
-    const int c = tid;
-    x[c][c] = inv_d[c];
-    for (int i = c + 1; i < r; ++i) {
-      float s = 0.f;
-      for (int m = c; m < i; ++m) s = fmaf(l[i][m], x[m][c], s);
-      x[i][c] = -s * inv_d[i];
+    // X = L⁻¹: x[i][c] = (δ_ic − Σ_{c<=m<i} L[i][m]·x[m][c]) · inv_d[i]
+    for (int i = 0; i < r; ++i) {
+      const float di = inv_d[i];
+#pragma unroll
+      for (int o = 0; o < OWN; ++o) {
+        const int cc = lane + 32 * o;
+        if (cc > i) continue;
+        float s0 = cc == i ? 1.f : 0.f, s1 = 0.f;
+        int m = cc;
+        for (; m + 1 < i; m += 2) {
+          s0 = fmaf(-g[i][m], x[m][cc], s0);
+          s1 = fmaf(-g[i][m + 1], x[m + 1][cc], s1);
+        }
+        if (m < i) s0 = fmaf(-g[i][m], x[m][cc], s0);
+        x[i][cc] = (s0 + s1) * di;
+      }
     }
   }
   __syncthreads();
@@ -274,10 +368,14 @@ __global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(const float* _
   }
 }
 
-// A[row] ← A[row]·T in place, one warp per row.
+// A[row] ← A[row]·T in place, one warp per row, for every checkpoint.
 template <int RP>
-__global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restrict__ a, int64_t m,
-                                                                 const float* __restrict__ t) {
+__global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restrict__ a_all,
+                                                                 int64_t a_stride, int64_t m,
+                                                                 const float* __restrict__ t_all) {
+  // checkpoint blockIdx.y: its rows and its T
+  float* __restrict__ a = a_all + blockIdx.y * a_stride;
+  const float* __restrict__ t = t_all + static_cast<int64_t>(blockIdx.y) * RP * RP;
   __shared__ float ts[RP][RP];
   for (int q = threadIdx.x; q < RP * RP; q += kMsThreads) ts[q / RP][q % RP] = t[q];
   __syncthreads();
@@ -392,10 +490,15 @@ int padded_rank(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Workspace: Ω (d_in × RP), Z (k × d_in × RP), split partials (at most
+// kMaxSplit outputs of the longer side, over all checkpoints), Gram partials
+// (k × slabs × RP²), T (k × RP²), factors Y_i = P (k × d_out × RP) and
+// R_i (k × d_in × RP).
 MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
   MsLayout L;
   L.rp = padded_rank(r);
   const size_t rp = static_cast<size_t>(L.rp);
+  const size_t kk = static_cast<size_t>(k);
   const size_t a_max = static_cast<size_t>(d_out > d_in ? d_out : d_in);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -404,16 +507,17 @@ MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
     return o;
   };
   L.omega = take(static_cast<size_t>(d_in) * rp * 4);
-  L.z = take(static_cast<size_t>(d_in) * rp * 4);
+  L.z = take(kk * d_in * rp * 4);
   L.part = take(kMaxSplit * a_max * rp * 4);
-  L.gpart = take(static_cast<size_t>(kMaxGramParts) * rp * rp * 4);
-  L.t = take(rp * rp * 4);
-  L.p = take(static_cast<size_t>(k) * d_out * rp * 4);
-  L.r = take(static_cast<size_t>(k) * d_in * rp * 4);
+  L.gpart = take(kk * ((a_max + kSlab - 1) / kSlab) * rp * rp * 4);
+  L.t = take(kk * rp * rp * 4);
+  L.p = take(kk * d_out * rp * 4);
+  L.r = take(kk * d_in * rp * 4);
   L.total = off;
   return L;
 }
 
+// Every step below processes all k checkpoints in one launch.
 template <int RP>
 struct MsRunner {
   const MonoSoupArgs& a;
@@ -421,50 +525,84 @@ struct MsRunner {
   uint8_t* ws;
   MsLayout L;
   int num_sms;
+  CkptTable tab;
 
   float* f(size_t off) const { return reinterpret_cast<float*>(ws + off); }
 
-  cudaError_t delta_mul(bool trans, const uint16_t* wft, const float* v, float* out) const {
+  // CTAs of a Δ-product kernel that fit on one SM (queried once per kernel)
+  static int resident_ctas(bool trans) {
+    static int occ[2] = {0, 0};
+    int& o = occ[trans ? 1 : 0];
+    if (o == 0) {
+      int n = 0;
+      const cudaError_t e =
+          trans ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_mul_kernel<RP, true>,
+                                                                kMulThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_mul_kernel<RP, false>,
+                                                                kMulThreads, 0);
+      o = (e == cudaSuccess && n > 0) ? n : 2;
+    }
+    return o;
+  }
+
+  // out_i = Δ_i·V_i (trans: Δ_iᵀ·V_i) for every checkpoint i; V_i at
+  // v + i·v_stride, out_i at out + i·out_stride.  Split over the contracted
+  // side so that the grid is about one even wave; *n_split = 0 when the
+  // outputs are complete, else the number of partials left in L.part.
+  cudaError_t delta_mul(bool trans, const float* v, int64_t v_stride, float* out,
+                        int64_t out_stride, int* n_split) const {
     const int64_t A = trans ? a.d_in : a.d_out;
     const int64_t B = trans ? a.d_out : a.d_in;
     const int64_t a_blocks = (A + kTileA - 1) / kTileA;
-    const int64_t want = 2 * static_cast<int64_t>(num_sms);
-    int64_t split = (want + a_blocks - 1) / a_blocks;
+    const int64_t want = static_cast<int64_t>(resident_ctas(trans)) * num_sms;
+    int64_t split = want / (a_blocks * a.k);
+    const int64_t split_max = kMaxSplit / a.k > 1 ? kMaxSplit / a.k : 1;
+    if (split > split_max) split = split_max;
     if (split < 1) split = 1;
-    if (split > kMaxSplit) split = kMaxSplit;
     int64_t b_chunk = (B + split - 1) / split;
     if (b_chunk < 2 * kTileB) b_chunk = 2 * kTileB;
     b_chunk = (b_chunk + kTileB - 1) / kTileB * kTileB;
     split = (B + b_chunk - 1) / b_chunk;
     float* dst = split == 1 ? out : f(L.part);
-    const dim3 grid(static_cast<unsigned>(a_blocks), static_cast<unsigned>(split));
+    const int64_t dst_stride = split == 1 ? out_stride : split * A * RP;
+    const dim3 grid(static_cast<unsigned>(a_blocks), static_cast<unsigned>(split),
+                    static_cast<unsigned>(a.k));
     if (trans)
-      delta_mul_kernel<RP, true><<<grid, kMsThreads, 0, s>>>(wft, a.w_base, a.d_out, a.d_in, v,
-                                                             dst, b_chunk);
+      delta_mul_kernel<RP, true><<<grid, kMulThreads, 0, s>>>(tab, a.w_base, a.d_out, a.d_in, v,
+                                                              v_stride, dst, dst_stride, b_chunk);
     else
-      delta_mul_kernel<RP, false><<<grid, kMsThreads, 0, s>>>(wft, a.w_base, a.d_out, a.d_in, v,
-                                                              dst, b_chunk);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || split == 1) return e;
-    const int64_t n = A * RP;
-    const int64_t blocks = (n + kMsThreads - 1) / kMsThreads;
-    reduce_parts_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), kMsThreads, 0, s>>>(
-        f(L.part), static_cast<int>(split), n, out);
+      delta_mul_kernel<RP, false><<<grid, kMulThreads, 0, s>>>(tab, a.w_base, a.d_out, a.d_in, v,
+                                                               v_stride, dst, dst_stride, b_chunk);
+    *n_split = split == 1 ? 0 : static_cast<int>(split);
     return cudaGetLastError();
   }
 
-  cudaError_t orth(float* m_ptr, int64_t m) const {
-    int64_t rows_per_cta = (m + kMaxGramParts - 1) / kMaxGramParts;
-    if (rows_per_cta < 32) rows_per_cta = 32;
-    rows_per_cta = (rows_per_cta + 31) / 32 * 32;
-    const int64_t parts = (m + rows_per_cta - 1) / rows_per_cta;
-    gram_partial_kernel<RP><<<static_cast<unsigned>(parts), kMsThreads, 0, s>>>(
-        m_ptr, m, rows_per_cta, f(L.gpart));
-    chol_inverse_kernel<RP><<<1, kMsThreads, 0, s>>>(f(L.gpart), static_cast<int>(parts), a.rank,
-                                                     f(L.t));
-    const int64_t rows_blocks = (m + 7) / 8;
-    apply_right_kernel<RP><<<static_cast<unsigned>(rows_blocks < 4096 ? rows_blocks : 4096),
-                             kMsThreads, 0, s>>>(m_ptr, m, f(L.t));
+  // Σ of the split partials into the outputs (and their Gram partials)
+  cudaError_t reduce_gram(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
+    const int64_t parts = (m + kSlab - 1) / kSlab;
+    reduce_gram_kernel<RP><<<dim3(static_cast<unsigned>(parts), static_cast<unsigned>(a.k)),
+                             kRgThreads, 0, s>>>(f(L.part), n_split, m_ptr, stride, m,
+                                                 f(L.gpart));
+    last_parts = static_cast<int>(parts);
+    return cudaGetLastError();
+  }
+  mutable int last_parts = 0;
+
+  cudaError_t finish(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
+    if (n_split == 0) return cudaSuccess;
+    return reduce_gram(m_ptr, stride, m, n_split);
+  }
+
+  // orthonormalise the columns of every checkpoint's m × RP block
+  cudaError_t orth(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
+    cudaError_t e = reduce_gram(m_ptr, stride, m, n_split);
+    if (e != cudaSuccess) return e;
+    chol_inverse_kernel<RP><<<static_cast<unsigned>(a.k), kMsThreads, 0, s>>>(
+        f(L.gpart), last_parts, a.rank, f(L.t));
+    int64_t rows_blocks = (m + 7) / 8;
+    if (rows_blocks > 1024) rows_blocks = 1024;
+    apply_right_kernel<RP><<<dim3(static_cast<unsigned>(rows_blocks), static_cast<unsigned>(a.k)),
+                             kMsThreads, 0, s>>>(m_ptr, stride, m, f(L.t));
     return cudaGetLastError();
   }
 
@@ -476,22 +614,25 @@ struct MsRunner {
                                                                              : 4096),
                            256, 0, s>>>(f(L.omega), a.d_in, a.rank, RP, a.seed);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      for (int i = 0; i < a.k; ++i) {
-        const uint16_t* wft = a.w_ft[i];
-        float* y = f(L.p) + static_cast<int64_t>(i) * a.d_out * RP;
-        float* r = f(L.r) + static_cast<int64_t>(i) * a.d_in * RP;
-        float* z = f(L.z);
-        if ((e = delta_mul(false, wft, f(L.omega), y)) != cudaSuccess) return e;
-        if ((e = orth(y, a.d_out)) != cudaSuccess) return e;
-        for (int it = 0; it < a.power_iters; ++it) {
-          if ((e = delta_mul(true, wft, y, z)) != cudaSuccess) return e;
-          if ((e = orth(z, a.d_in)) != cudaSuccess) return e;
-          if ((e = delta_mul(false, wft, z, y)) != cudaSuccess) return e;
-          if ((e = orth(y, a.d_out)) != cudaSuccess) return e;
-        }
-        if ((e = orth(y, a.d_out)) != cudaSuccess) return e;  // second Cholesky QR pass
-        if ((e = delta_mul(true, wft, y, r)) != cudaSuccess) return e;
+      float* y = f(L.p);
+      float* z = f(L.z);
+      float* r = f(L.r);
+      const int64_t ys = a.d_out * RP, zs = a.d_in * RP;
+      int ns = 0;
+      if ((e = delta_mul(false, f(L.omega), 0, y, ys, &ns)) != cudaSuccess) return e;
+      if ((e = orth(y, ys, a.d_out, ns)) != cudaSuccess) return e;
+      for (int it = 0; it < a.power_iters; ++it) {
+        // Z = Δᵀ·Y needs no orthonormalisation of its own: only the span of
+        // Y matters, and Y = Δ·Z is orthonormalised (its condition number
+        // grows by at most (σ_1/σ_r)² per round)
+        if ((e = delta_mul(true, y, ys, z, zs, &ns)) != cudaSuccess) return e;
+        if ((e = finish(z, zs, a.d_in, ns)) != cudaSuccess) return e;
+        if ((e = delta_mul(false, z, zs, y, ys, &ns)) != cudaSuccess) return e;
+        if ((e = orth(y, ys, a.d_out, ns)) != cudaSuccess) return e;
       }
+      if ((e = orth(y, ys, a.d_out, 0)) != cudaSuccess) return e;  // second Cholesky QR pass
+      if ((e = delta_mul(true, y, ys, r, zs, &ns)) != cudaSuccess) return e;
+      if ((e = finish(r, zs, a.d_in, ns)) != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>((a.d_in + 63) / 64),
                     static_cast<unsigned>((a.d_out + 63) / 64));
@@ -516,13 +657,16 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, void* workspace, int num_sms,
   // factors start at zero: the padding columns stay zero and rank 0 merges nothing
   cudaError_t e = cudaMemsetAsync(ws + L.p, 0, L.total - L.p, stream);
   if (e != cudaSuccess) return e;
+  if (a.k < 1 || a.k > kMaxCkpt) return cudaErrorInvalidValue;
+  CkptTable tab{};
+  for (int i = 0; i < a.k; ++i) tab.p[i] = a.w_ft[i];
   switch (L.rp) {
     case 16:
-      return MsRunner<16>{a, stream, ws, L, num_sms}.run();
+      return MsRunner<16>{a, stream, ws, L, num_sms, tab}.run();
     case 32:
-      return MsRunner<32>{a, stream, ws, L, num_sms}.run();
+      return MsRunner<32>{a, stream, ws, L, num_sms, tab}.run();
     default:
-      return MsRunner<64>{a, stream, ws, L, num_sms}.run();
+      return MsRunner<64>{a, stream, ws, L, num_sms, tab}.run();
   }
 }
 
