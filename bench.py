@@ -942,6 +942,18 @@ def run_profile(kind: str):
         y = torch.empty((2048, 8192), dtype=torch.bfloat16, device="cuda")
         for _ in range(4):
             bd.bitdelta_linear(x, wb, p, a, per_row=True, out=y)
+    elif kind == "grouped":
+        grp = Grouped(bd)
+        for i in range(4):
+            grp.run_phase(f"set{i % grp.sets}")
+    elif kind == "kmerge":
+        km = KMergeSimilarity(bd)
+        n_b = km.n_var - 1
+        ws = torch.empty(bd.bitdelta_sign_similarity_workspace_bytes(km.d_out, n_b) + 256,
+                         dtype=torch.uint8, device="cuda")
+        for _ in range(4):
+            bd.bitdelta_sign_similarity(km.packs[0], km.alphas[0], km.pt, km.at, n_b, True,
+                                        workspace=ws)
     elif kind == "monosoup":
         ms_wl = MonoSoupMerge(bd)
         for _ in range(2):
@@ -965,7 +977,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--profile", default=None,
-                    help="decode|compress|reconstruct|prefill: a few eager launches for ncu")
+                    help="decode|compress|reconstruct|prefill|grouped|kmerge|monosoup: "
+                         "a few eager launches for ncu")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args.profile)
