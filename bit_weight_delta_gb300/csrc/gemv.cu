@@ -515,6 +515,7 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
 // product of variant v uses x fragments in which the rows of other variants
 // are zero, so each row collects exactly its own variant's α_v·(x·S_vᵀ).
 constexpr int kMaxGroupVars = 4;
+constexpr int kMixedAhead = 2;  // super-chunks of L2 prefetch ahead per warp
 
 struct MixedGroup {
   int32_t rows[kMaxGroupRows];     // x/y row per slot, −1 = empty
@@ -589,7 +590,30 @@ __device__ __forceinline__ void gemv_group_mixed(const GemvArgs& p, const MixedG
   };
 
   const int64_t n_sc = d_in / (32 * CPS);
+  // L2 prefetch of the super-chunk kMixedAhead steps ahead (this warp's next
+  // but one): lane L takes one 128-byte line of the 16 W row segments and of
+  // the x row segments, and the variants' sign words of rows 0..7 of each
+  // group of 8 rows
+  const int pr = lane >> 1, ph = lane & 1;  // row, half (line) of a 256-byte segment
+  const int64_t n_pf = n0 + pr;
+  const uint16_t* w_pf = n_pf < d_out && pr < 8 * NG ? p.w + n_pf * d_in + 64 * ph : nullptr;
+  const int xr_pf = pr < kMaxGroupRows ? grp.rows[pr] : -1;
+  const uint16_t* x_pf = xr_pf >= 0 ? p.x + static_cast<int64_t>(xr_pf) * d_in + 64 * ph : nullptr;
+  auto prefetch_sc = [&](int64_t sc_pf) {
+    if (sc_pf >= n_sc) return;
+    const int64_t kc = sc_pf * 32 * CPS;
+    if (w_pf != nullptr) prefetch_l2(w_pf + kc);
+    if (x_pf != nullptr) prefetch_l2(x_pf + kc);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int row = lane & 15, half = lane >> 4;  // row of group `half`
+      if (v < nv && half < NG && row < 8 && n0 + 8 * half + row < d_out)
+        prefetch_l2(p.packed_table[grp.vars[v] - 1] + (n0 + 8 * half + row) * row_bytes + kc / 8);
+    }
+  };
+  prefetch_sc(warp + kKW);
   for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+    prefetch_sc(sc + kMixedAhead * kKW);
     const int64_t kc0 = sc * 32 * CPS;
     uint4 w[CPS][NG];
     uint32_t sw[CPS][V][NG];
