@@ -347,8 +347,8 @@ __device__ __forceinline__ void chunk_mma_t(float (&acc_b)[NT][4], float (&acc_s
 
 // Warp 0 sums the KW warps' partial products (transposed fragments) in a
 // fixed order and writes y[token][n] (bf16, round to nearest even).
-template <int NT>
-__device__ __forceinline__ void store_group_rows_t(const GemvArgs& p, const RowGroup& grp,
+template <int NT, class Grp>
+__device__ __forceinline__ void store_group_rows_t(const GemvArgs& p, const Grp& grp,
                                                    const float* red, int64_t n0, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -784,14 +784,210 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_async_kernel(GemvArgs p)
   }
 }
 
+// Mixed groups through the deep queue: W_base rows, every variant's sign
+// words and the group's x rows travel by cp.async into a per-warp ring (as in
+// gemv_group_async), the W rows are the MMA's A operand and NT tiles of 8
+// tokens its B operand.  Each variant's sign product runs over all the
+// group's tokens; a token reads only its own variant's accumulator, so no
+// masking is needed.  Requires d_in % 128 == 0 and 16-byte aligned sign rows
+// for every variant of the group.
+template <int NT>
+__host__ __device__ constexpr int mixed_stage_bytes() {
+  return kStageRows * 256 + kMaxGroupVars * kStageRows * 16 + NT * 8 * 256;
+}
+template <int NT>
+__host__ __device__ constexpr int mixed_ring_stages() { return NT == 1 ? 3 : 2; }
+template <int NT>
+constexpr size_t mixed_ring_bytes() {
+  return static_cast<size_t>(mixed_ring_stages<NT>()) * kKW * mixed_stage_bytes<NT>();
+}
+
+template <int NT>
+__device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const MixedGroup& grp,
+                                                       float* red, uint8_t* ring) {
+  constexpr int CPS = kCPS;
+  constexpr int V = kMaxGroupVars;
+  constexpr int R = kStageRows;  // 16 W rows
+  static_assert(R == 16 && V % 2 == 0, "two 8-row halves; variants copied in pairs");
+  constexpr int D = mixed_ring_stages<NT>();
+  constexpr int kSB = mixed_stage_bytes<NT>();
+  constexpr int kSOff = R * 256;              // sign words: [variant][row] × 16 bytes
+  constexpr int kXOff = R * 256 + V * R * 16; // x segments of NT·8 token rows
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_in = p.d_in, d_out = p.d_out;
+  const int64_t row_bytes = d_in / 8;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int64_t rows_here = d_out - n0 < R ? d_out - n0 : R;
+  const int nv = grp.n_vars;
+
+  bool x_ok[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) x_ok[nt] = grp.rows[g + 8 * nt] >= 0;
+  bool row_ok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) row_ok[h] = 8 * h + g < rows_here;
+
+  float acc_b[NT][4], acc_s[V][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc_b[nt][e] = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc_s[v][nt][e] = 0.f;
+    }
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  uint8_t* const wring = ring + static_cast<size_t>(warp) * D * kSB;
+  const uint32_t wring_sa = smem_addr(wring);
+
+  // copy side (lane L): W word L & 15 of rows 2k + (L >> 4); the sign word of
+  // row L & 15 of variants 2k + (L >> 4); x word L & 15 of token rows 2k + (L >> 4)
+  const int cr = lane >> 4, cw = lane & 15;
+  const uint16_t* const wsrc0 = p.w + (n0 + cr) * d_in + 8 * cw;
+  const uint8_t* ssrc[V / 2];
+#pragma unroll
+  for (int k = 0; k < V / 2; ++k) {
+    const int v = 2 * k + cr;
+    ssrc[k] = (v < nv && cw < rows_here)
+                  ? p.packed_table[grp.vars[v] - 1] + (n0 + cw) * row_bytes
+                  : nullptr;
+  }
+  const uint16_t* xsrc[4 * NT];
+#pragma unroll
+  for (int k = 0; k < 4 * NT; ++k) {
+    const int row = grp.rows[2 * k + cr];
+    xsrc[k] = row >= 0 ? p.x + static_cast<int64_t>(row) * d_in + 8 * cw : nullptr;
+  }
+  const int64_t n_sc = d_in / (32 * CPS);
+  auto issue = [&](int s, int64_t sc) {
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * 32 * CPS;
+      const uint32_t st = wring_sa + s * kSB;
+#pragma unroll
+      for (int k = 0; k < R / 2; ++k) {
+        const int r = 2 * k + cr;
+        if (r < rows_here)
+          cp_async_16_cg(st + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), wsrc0 + 2 * k * d_in + kc0);
+      }
+#pragma unroll
+      for (int k = 0; k < V / 2; ++k)
+        if (ssrc[k] != nullptr)
+          cp_async_16_cg(st + kSOff + 16u * ((2 * k + cr) * R + cw), ssrc[k] + kc0 / 8);
+#pragma unroll
+      for (int k = 0; k < 4 * NT; ++k) {
+        const int r = 2 * k + cr;
+        if (xsrc[k] != nullptr)
+          cp_async_16_x(st + kXOff + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), xsrc[k] + kc0);
+      }
+    }
+    cp_async_commit();  // one group per stage, empty past the end
+  };
+
+  int64_t next = warp;
+#pragma unroll
+  for (int s = 0; s < D - 1; ++s) {
+    issue(s, next);
+    next += kKW;
+  }
+  int s_rd = 0;
+  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+    __syncwarp();  // every lane is done reading the slot refilled next
+    issue(s_rd == 0 ? D - 1 : s_rd - 1, next);
+    next += kKW;
+    cp_async_wait<D - 1>();
+    __syncwarp();
+    const uint8_t* st = wring + s_rd * kSB;
+    uint4 sw[V][2];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        sw[v][h] = (v < nv && row_ok[h])
+                       ? *reinterpret_cast<const uint4*>(st + kSOff + 16 * (v * R + 8 * h + g))
+                       : zero4;
+#pragma unroll
+    for (int j = 0; j < CPS; ++j) {
+      uint4 wv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = 8 * h + g;
+        wv[h] = row_ok[h] ? *reinterpret_cast<const uint4*>(
+                                st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
+                          : zero4;
+      }
+      uint4 xv[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r = 8 * nt + g;
+        xv[nt] = x_ok[nt] ? *reinterpret_cast<const uint4*>(
+                                st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
+                          : zero4;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_16816(acc_b[nt], wv[0].x, wv[1].x, wv[0].y, wv[1].y, xv[nt].x, xv[nt].y);
+        mma_16816(acc_b[nt], wv[0].z, wv[1].z, wv[0].w, wv[1].w, xv[nt].z, xv[nt].w);
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        if (v < nv) {
+          const uint32_t w0 = j == 0 ? sw[v][0].x : j == 1 ? sw[v][0].y : j == 2 ? sw[v][0].z : sw[v][0].w;
+          const uint32_t w1 = j == 0 ? sw[v][1].x : j == 1 ? sw[v][1].y : j == 2 ? sw[v][1].z : sw[v][1].w;
+          const uint32_t b0 = (w0 >> (8 * t)) & 0xFFu, b1 = (w1 >> (8 * t)) & 0xFFu;
+          uint32_t s0[4], s1[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            s0[i] = pm_one_pair(b0, i);
+            s1[i] = pm_one_pair(b1, i);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_16816(acc_s[v][nt], s0[0], s1[0], s0[1], s1[1], xv[nt].x, xv[nt].y);
+            mma_16816(acc_s[v][nt], s0[2], s1[2], s0[3], s1[3], xv[nt].z, xv[nt].w);
+          }
+        }
+      }
+    }
+    s_rd = s_rd == D - 1 ? 0 : s_rd + 1;
+  }
+  cp_async_wait<0>();
+
+  // y_part = acc_b + α_v[n]·acc_s[v], v the token's own variant (fragment
+  // rows: W rows n0+g, n0+8+g; columns: tokens 8nt + 2t, 8nt + 2t + 1)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = 8 * nt + 2 * t + (e & 1);
+      const int64_t n = n0 + g + 8 * (e >> 1);
+      const int mv = grp.slot_var[m];
+      float sv = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (v == mv) sv = acc_s[v][nt][e];
+      float val = acc_b[nt][e];
+      if (mv >= 0 && n < d_out) {
+        const float* al = p.alpha_table[grp.vars[mv] - 1];
+        val = fmaf(p.per_row ? __ldg(al + n) : __ldg(al), sv, val);
+      }
+      red[(warp * NT * 4 + nt * 4 + e) * 32 + lane] = val;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) store_group_rows_t<NT>(p, grp, red, n0, lane);
+  __syncthreads();
+}
+
 // Multi-tenant: rows of short segments, bucketed by variant, then taken in
 // groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
 // builds the same grouping in shared memory, then covers its 8·NG output
 // columns for every group.
-template <int NG>
-__global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
+template <int NG, int kAsyncNT>
+__global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p, int ring_off) {
   __shared__ float red[kKW * NG * 4 * 32];
-  extern __shared__ int32_t dyn[];
+  extern __shared__ __align__(16) int32_t dyn[];
   griddep_launch_dependents();
   griddep_wait();
   // dyn: [n_var+2] bucket counts | [n_var+2] bucket starts | [max_rows] rows
@@ -884,6 +1080,13 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p) {
       bucket = bk;
     }
     __syncthreads();
+    if constexpr (kAsyncNT > 0) {
+      if (mg_vec) {
+        gemv_group_mixed_async<kAsyncNT>(p, mg, red,
+                                         reinterpret_cast<uint8_t*>(dyn) + ring_off);
+        continue;
+      }
+    }
     if (mg_vec)
       gemv_group_mixed<NG, true>(p, mg, red);
     else
@@ -939,10 +1142,9 @@ cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream) {
   return launch_single<kNG>(p, sign_vec, stream);
 }
 
-cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream) {
-  const size_t smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
-  const int64_t n_blocks = (p.d_out + 8 * kNG - 1) / (8 * kNG);
-  dim3 grid(static_cast<unsigned>(n_blocks));
+template <int NT>
+cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off, dim3 grid,
+                                    cudaStream_t stream) {
   // Raise the dynamic shared-memory limit only when a call needs more than
   // any earlier call on this device (so captured calls make no attribute call).
   static size_t smem_set[64] = {};
@@ -951,12 +1153,32 @@ cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > 48 * 1024 && smem > smem_set[dev]) {
-    e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     smem_set[dev] = smem;
   }
-  return launch_pdl(gemv_grouped_kernel<kNG>, grid, dim3(kKW * 32), smem, stream, p);
+  return launch_pdl(gemv_grouped_kernel<kNG, NT>, grid, dim3(kKW * 32), smem, stream, p,
+                    ring_off);
+}
+
+cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream) {
+  const size_t group_smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
+  const int64_t n_blocks = (p.d_out + 8 * kNG - 1) / (8 * kNG);
+  const dim3 grid(static_cast<unsigned>(n_blocks));
+  // The deep-queue pass (d_in % 128 == 0) with one token tile when no group
+  // can hold more than 8 rows, else two; its ring follows the grouping lists.
+  const size_t ring_off = (group_smem + 15) / 16 * 16;
+  const size_t kMaxDyn = 200 * 1024;
+  if (p.d_in % 128 == 0) {
+    if (max_rows <= 8 && ring_off + mixed_ring_bytes<1>() <= kMaxDyn)
+      return launch_grouped_instance<1>(p, ring_off + mixed_ring_bytes<1>(),
+                                        static_cast<int>(ring_off), grid, stream);
+    if (ring_off + mixed_ring_bytes<2>() <= kMaxDyn)
+      return launch_grouped_instance<2>(p, ring_off + mixed_ring_bytes<2>(),
+                                        static_cast<int>(ring_off), grid, stream);
+  }
+  return launch_grouped_instance<0>(p, group_smem, 0, grid, stream);
 }
 
 }  // namespace bd
