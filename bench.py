@@ -48,7 +48,7 @@ METRIC = "bitdelta_linear TFLOP/s (prefill) & GB/s (decode) as % of GB300 roofli
 # capture of `python bench.py --profile decode`, summarised in the file named by
 # DECODE_PROFILE.  Valid for the kernel build that capture was taken on; reset
 # to None whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 35_762_176
+DECODE_TRAFFIC_BYTES = 35_761_152
 DECODE_PROFILE = "profiles/gemv_single_async_decode_4096x4096_M8.md"
 
 # --------------------------------------------------------------------------- peaks
