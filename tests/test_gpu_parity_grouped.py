@@ -103,3 +103,52 @@ def test_grouped_bad_variant_id_is_reported():
                                n_var=1, max_seg_len=2, per_row=True)
     assert bd.bitdelta_check_error() == 7   # BD_ERR_DEVICE_BOUNDS
     assert bd.bitdelta_check_error() == 0
+
+
+@pytest.mark.parametrize("per_row", [True, False])
+def test_grouped_at_most_eight_short_rows(per_row):
+    """At most 8 short rows in the whole batch (here 8 one-row segments that
+    alternate two variants, as in a decode step of two tenants): the short
+    rows run through the ring with a single token tile."""
+    lengths = [1] * 8
+    wb, packs, alphas, off, var, x = _setup(17, 320, 1024, 2, lengths, per_row,
+                                            variants=[1, 2, 1, 2, 1, 2, 1, 2])
+    y = _run(wb, packs, alphas, off, var, x, per_row)
+    ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, per_row)
+    assert_linear_close(y, ref)
+    for s in range(len(var)):
+        assert_linear_close(y[s:s + 1], ref[s:s + 1], f"row {s}")
+
+
+def test_grouped_few_rows_with_base_and_ragged_d_out():
+    """Seven short rows (base and three variants) on a d_out that is not a
+    multiple of 16: single token tile, partial last row group."""
+    lengths = [2, 1, 3, 1]
+    wb, packs, alphas, off, var, x = _setup(18, 250, 512, 3, lengths,
+                                            variants=[3, 0, 1, 2])
+    y = _run(wb, packs, alphas, off, var, x, True)
+    ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
+    assert_linear_close(y, ref)
+
+
+def test_grouped_unaligned_sign_rows_take_the_register_pass():
+    """d_in % 128 == 0 but one variant's packed signs start 8 bytes past a
+    16-byte boundary: groups holding that variant take the register-pipelined
+    pass (byte-wise sign loads), the others the ring; both match the oracle."""
+    lengths = [1, 3, 1, 2, 1, 5]
+    d_out, d_in = 192, 512
+    wb, packs, alphas, off, var, x = _setup(19, d_out, d_in, 3, lengths,
+                                            variants=[1, 2, 3, 1, 0, 2])
+    dp = [to_dev(p) for p in packs]
+    raw = torch.empty(packs[1].size + 8, dtype=torch.uint8, device="cuda")
+    shifted = raw[8:8 + packs[1].size].view(packs[1].shape)
+    shifted.copy_(dp[1])
+    assert shifted.data_ptr() % 16 == 8
+    dp[1] = shifted
+    da = [to_dev(a) for a in alphas]
+    pt, at = bd.variant_tables(dp, da, "cuda")
+    y = bd.bitdelta_linear_grouped(to_dev_bf16(x), to_dev(off), to_dev(var), to_dev_bf16(wb), pt,
+                                   at, n_var=3, max_seg_len=int(np.diff(off).max()), per_row=True)
+    assert bd.bitdelta_check_error() == 0
+    ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
+    assert_linear_close(bf16_values(y), ref)
