@@ -20,10 +20,11 @@
 //     W_merged = bf16_rne(W_base + (1/k)·Σ_i Y_i·R_iᵀ).
 //
 // Factor matrices are fp32, row-major with RP columns (r padded to 16, 32 or
-// 64; the padding columns stay zero).  Products with Δ are tall-skinny
-// (64 rows of the long side × RP per CTA, split over the contracted side with
-// a fixed-order reduction of the partial results); they run on the CUDA
-// cores in fp32.
+// 64; the padding columns stay zero).  Products with Δ are tall-skinny (64
+// rows of the long side × RP per CTA, split over the contracted side with a
+// fixed-order reduction of the partial results); they run on the tensor
+// cores as W_i·V − W_base·V with V split into two bf16 terms (four bf16
+// products per tile, fp32 accumulation).
 #include <cstdint>
 
 #include "common.cuh"
@@ -34,7 +35,7 @@ namespace {
 
 constexpr int kMsThreads = 256;
 constexpr int kMulThreads = 128;  // threads of a Δ-product CTA
-constexpr int kTileA = 128;  // rows of the long side per Δ-product CTA
+constexpr int kTileA = 64;   // rows of the long side per Δ-product CTA (16 per warp)
 constexpr int kTileB = 32;   // contracted indices per step
 constexpr int kMaxSplit = 32;
 
@@ -42,6 +43,16 @@ constexpr int kMaxCkpt = 64;
 struct CkptTable {  // the checkpoints' W_i, passed by value
   const uint16_t* p[kMaxCkpt];
 };
+
+// D += A·B, mma.sync m16n8k16 (bf16 A row-major, bf16 B column-major, fp32).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -66,140 +77,231 @@ __global__ void sketch_fill_kernel(float* omega, int64_t d_in, int r, int rp, ui
   }
 }
 
-// out[a][j] = Σ_b Δ(a, b)·V[b][j] over b in this CTA's split.
+// V split for the tensor-core Δ products: V (B × RP fp32, one per checkpoint
+// at v_stride, or one for all when v_stride is 0) → kVTerms bf16 terms
+// V ≈ hi + lo (relative error 2^-18 per element), stored transposed as
+// vs[z][term][j][b] with rows of bp = B rounded up to 8 (zero padding), so
+// that a B fragment is two adjacent b of one j and every row is 16-byte
+// aligned.  A thread converts 8 consecutive b of one j and writes one
+// 16-byte vector per term.
+constexpr int kVTerms = 2;
+__global__ void vsplit_kernel(const float* __restrict__ v_all, int64_t v_stride, int64_t B,
+                              int64_t bp, int rp, uint16_t* __restrict__ out) {
+  const int64_t z = blockIdx.y;
+  const float* __restrict__ v = v_all + z * v_stride;
+  uint16_t* __restrict__ o = out + z * kVTerms * rp * bp;
+  const int64_t nb8 = bp / 8;
+  const int64_t n = nb8 * rp;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(i / nb8);
+    const int64_t b0 = 8 * (i - static_cast<int64_t>(j) * nb8);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float x[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) x[u] = b0 + e + u < B ? __ldg(v + (b0 + e + u) * rp + j) : 0.f;
+      const uint32_t h = pack_bf16x2_rn(x[0], x[1]);
+      const float r0 = x[0] - __uint_as_float(h << 16);
+      const float r1 = x[1] - __uint_as_float(h & 0xFFFF0000u);
+      hw[e / 2] = h;
+      lw[e / 2] = pack_bf16x2_rn(r0, r1);
+    }
+    *reinterpret_cast<uint4*>(o + static_cast<int64_t>(j) * bp + b0) =
+        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(o + static_cast<int64_t>(rp + j) * bp + b0) =
+        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Shared-memory geometry of one pipeline stage of the Δ-product kernel.
+template <int RP, bool kT>
+struct MulStage {
+  // W tiles (W_i and W_base): !kT [64 a][32 b + 8], kT [32 b][64 a + 8] (bf16)
+  static constexpr int kWRow = kT ? kTileA + 8 : kTileB + 8;
+  static constexpr int kWRows = kT ? kTileB : kTileA;
+  static constexpr int kWBytes = kWRows * kWRow * 2;
+  // V terms: [kVTerms][RP j][32 b + 8] (bf16)
+  static constexpr int kVRow = kTileB + 8;
+  static constexpr int kVBytes = kVTerms * RP * kVRow * 2;
+  static constexpr int kBytes = 2 * kWBytes + kVBytes;
+};
+constexpr int kMulStages = 3;
+
+template <int RP, bool kT>
+constexpr size_t mul_smem_bytes() {
+  return static_cast<size_t>(kMulStages) * MulStage<RP, kT>::kBytes;
+}
+
+// out[a][j] = Σ_b Δ(a, b)·V[b][j] over b in this CTA's split, on the tensor
+// cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 //   kT = false: a = row n of Δ, b = column c   (Y = Δ·V,  V: d_in × RP)
 //   kT = true:  a = column c,   b = row n      (Z = Δᵀ·V, V: d_out × RP)
-// Grid (ceil(A / 128), S, k); split s covers b in [s·b_chunk, (s+1)·b_chunk)
-// and writes part[s][a][j] (or the output directly when S == 1); blockIdx.z
-// picks the checkpoint.  128 threads; a thread
-// owns 8 a × RP/8 j.  The next step's Δ vectors and V values are loaded into
-// registers while the current step's products run.
+// Δ·V = W_i·V − W_base·V with both weights as exact bf16 operands and V as
+// the sum of two bf16 terms (vsplit_kernel): four products per tile, the
+// W_base ones with the V fragments' sign bits flipped, all into one fp32
+// accumulator.  With V's columns orthonormal (as in the iteration), the
+// result stays within about 1e-6 of Δ·V relative to its largest entry
+// (fp64 emulation: 5e-7), despite the cancellation of the two products.  Grid
+// (ceil(A / 64), S, k); split s covers b in [s·b_chunk, (s+1)·b_chunk) and
+// writes part[s][a][j] (or the output directly when S == 1); blockIdx.z picks
+// the checkpoint.  128 threads; warp w owns rows a0 + 16w .. +15 and all RP
+// columns.  Tiles arrive by cp.async through a kMulStages-deep ring; A
+// fragments come from ldmatrix (.trans for Δᵀ).
 template <int RP, bool kT>
 __global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
     CkptTable tab, const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
-    const float* __restrict__ v_all, int64_t v_stride, float* __restrict__ dst_all,
-    int64_t dst_stride, int64_t b_chunk) {
-  // checkpoint z: its W_i, its V (v_stride 0: one V for all) and its output
-  // (dst_stride apart; split s at dst + s·A·RP)
+    const uint16_t* __restrict__ vs_all, int64_t vs_stride, int64_t bp,
+    float* __restrict__ dst_all, int64_t dst_stride, int64_t b_chunk) {
+  using G = MulStage<RP, kT>;
+  constexpr int JT = RP / 8;
+  extern __shared__ __align__(16) uint8_t sm[];
   const uint16_t* __restrict__ wft = tab.p[blockIdx.z];
-  const float* __restrict__ v = v_all + blockIdx.z * v_stride;
-  constexpr int TJ = RP / 8;                  // j per thread
-  constexpr int VQ = kTileB * RP / 4 / kMulThreads;  // float4 of V per thread per step
-  __shared__ __align__(16) float ds[kTileB][kTileA + 4];  // [b][a]
-  __shared__ __align__(16) float vs[kTileB][RP];
-  const int tid = threadIdx.x;
-  const int ty = tid >> 3, tx = tid & 7;      // 16 groups of 8 a, 8 groups of TJ j
   const int64_t A = kT ? d_in : d_out;
   const int64_t B = kT ? d_out : d_in;
+  const uint16_t* __restrict__ vsz = vs_all + blockIdx.z * vs_stride;  // [kVTerms][RP][bp]
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
   const int64_t a0 = static_cast<int64_t>(blockIdx.x) * kTileA;
   const int64_t b_lo = static_cast<int64_t>(blockIdx.y) * b_chunk;
   const int64_t b_hi = b_lo + b_chunk < B ? b_lo + b_chunk : B;
+  const uint32_t sm_sa = smem_addr(sm);
+  const int n_steps = static_cast<int>((b_hi - b_lo + kTileB - 1) / kTileB);
 
-  // loader geometry: 4 vectors of 8 bf16 per matrix per thread per step
-  //   !kT: rows a0 + (tid >> 2) + 32·u, columns b0 + 8·(tid & 3)
-  //    kT: rows b0 + (tid >> 4) + 8·u,  columns a0 + 8·(tid & 15)
-  uint4 pf[4], pb[4];
-  float4 pv[VQ];
-  auto load = [&](int64_t b0) {
+  // One stage: W_i and W_base tiles (256 vectors of 16 bytes each, 2 per
+  // thread per matrix) and the V-term tiles (kVTerms·RP rows of 64 bytes).
+  // Elements past the matrix edge are zero-filled by plain stores.
+  auto issue = [&](int stage, int step) {
+    if (step < n_steps) {
+      const int64_t b0 = b_lo + static_cast<int64_t>(step) * kTileB;
+      const uint32_t st = sm_sa + stage * G::kBytes;
+      uint8_t* stp = sm + stage * G::kBytes;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      int64_t n, c;
-      bool ok;
-      if (!kT) {
-        n = a0 + (tid >> 2) + 32 * u;
-        c = b0 + 8 * (tid & 3);
-        ok = n < d_out && c < b_hi;
-      } else {
-        n = b0 + (tid >> 4) + 8 * u;
-        c = a0 + 8 * (tid & 15);
-        ok = n < b_hi && c < d_in;
-      }
-      pf[u] = ok ? __ldg(reinterpret_cast<const uint4*>(wft + n * d_in + c)) : make_uint4(0, 0, 0, 0);
-      pb[u] = ok ? __ldg(reinterpret_cast<const uint4*>(wb + n * d_in + c)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int q = 0; q < VQ; ++q) {
-      const int idx = tid + q * kMulThreads;
-      const int bb = idx / (RP / 4), j4 = idx % (RP / 4);
-      const int64_t b = b0 + bb;
-      pv[q] = b < b_hi ? __ldg(reinterpret_cast<const float4*>(v + b * RP) + j4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  auto stash = [&]() {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float f[8], fb[8];
-      bf16x8_to_f32(pf[u], f);
-      bf16x8_to_f32(pb[u], fb);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] -= fb[e];   // Δ, exact in fp32
-      if (!kT) {
-        const int row = (tid >> 2) + 32 * u, col = 8 * (tid & 3);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ds[col + e][row] = f[e];
-      } else {
-        const int row = (tid >> 4) + 8 * u, col = 8 * (tid & 15);
-        *reinterpret_cast<float4*>(&ds[row][col]) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4*>(&ds[row][col + 4]) = make_float4(f[4], f[5], f[6], f[7]);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < VQ; ++q) {
-      const int idx = tid + q * kMulThreads;
-      *reinterpret_cast<float4*>(&vs[idx / (RP / 4)][4 * (idx % (RP / 4))]) = pv[q];
-    }
-  };
-
-  float acc[8][TJ];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < TJ; ++j) acc[i][j] = 0.f;
-
-  if (b_lo < b_hi) load(b_lo);
-  for (int64_t b0 = b_lo; b0 < b_hi; b0 += kTileB) {
-    stash();
-    __syncthreads();
-    if (b0 + kTileB < b_hi) load(b0 + kTileB);   // in flight during the products
-#pragma unroll 4
-    for (int bb = 0; bb < kTileB; ++bb) {
-      const float4 x0 = *reinterpret_cast<const float4*>(&ds[bb][8 * ty]);
-      const float4 x1 = *reinterpret_cast<const float4*>(&ds[bb][8 * ty + 4]);
-      const float av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      float vv[TJ];
-      if constexpr (TJ % 4 == 0) {
-#pragma unroll
-        for (int j = 0; j < TJ; j += 4) {
-          const float4 t4 = *reinterpret_cast<const float4*>(&vs[bb][TJ * tx + j]);
-          vv[j] = t4.x;
-          vv[j + 1] = t4.y;
-          vv[j + 2] = t4.z;
-          vv[j + 3] = t4.w;
+      for (int u = 0; u < 2; ++u) {
+        const int q = tid + kMulThreads * u;
+        int row, col;
+        int64_t n, c;
+        bool ok;
+        if (!kT) {
+          row = q >> 2;
+          col = 8 * (q & 3);
+          n = a0 + row;
+          c = b0 + col;
+          ok = n < d_out && c < b_hi;
+        } else {
+          row = q >> 3;
+          col = 8 * (q & 7);
+          n = b0 + row;
+          c = a0 + col;
+          ok = n < b_hi && c < d_in;
         }
-      } else {
+        const uint32_t off = static_cast<uint32_t>((row * G::kWRow + col) * 2);
+        if (ok) {
+          cp16(st + off, wft + n * d_in + c);
+          cp16(st + G::kWBytes + off, wb + n * d_in + c);
+        } else {
+          *reinterpret_cast<uint4*>(stp + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(stp + G::kWBytes + off) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // V terms: rows (term, j), 4 vectors of 8 b each
+      for (int q = tid; q < kVTerms * RP * 4; q += kMulThreads) {
+        const int row = q >> 2, col = 8 * (q & 3);
+        const int64_t b = b0 + col;
+        const uint32_t off = static_cast<uint32_t>(2 * G::kWBytes + (row * G::kVRow + col) * 2);
+        if (b < b_hi)  // b_hi < B only at split boundaries (multiples of 32)
+          cp16(st + off, vsz + static_cast<int64_t>(row) * bp + b);
+        else
+          *reinterpret_cast<uint4*>(stp + off) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[JT][4];
 #pragma unroll
-        for (int j = 0; j < TJ; j += 2) {
-          const float2 t2 = *reinterpret_cast<const float2*>(&vs[bb][TJ * tx + j]);
-          vv[j] = t2.x;
-          vv[j + 1] = t2.y;
+  for (int jt = 0; jt < JT; ++jt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[jt][e] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < kMulStages - 1; ++s) issue(s, s);
+  for (int step = 0; step < n_steps; ++step) {
+    cp_async_wait<kMulStages - 2>();
+    __syncthreads();  // the stage is complete for every thread; the oldest slot is free
+    issue((step + kMulStages - 1) % kMulStages, step + kMulStages - 1);
+    const int stage = step % kMulStages;
+    const uint32_t st = sm_sa + stage * G::kBytes;
+#pragma unroll
+    for (int kk = 0; kk < kTileB; kk += 16) {
+      uint32_t af[2][4];  // [W_i, W_base] A fragments of rows 16w .. +15, k kk .. +15
+#pragma unroll
+      for (int mtx = 0; mtx < 2; ++mtx) {
+        const uint32_t base = st + mtx * G::kWBytes;
+        if (!kT) {
+          const int m = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int k = kk + 8 * (lane >> 4);
+          ldsm_x4(base + (m * G::kWRow + k) * 2, af[mtx][0], af[mtx][1], af[mtx][2], af[mtx][3]);
+        } else {
+          const int k = kk + (lane & 7) + 8 * (lane >> 4);
+          const int m = 16 * warp + 8 * ((lane >> 3) & 1);
+          ldsm_x4_t(base + (k * G::kWRow + m) * 2, af[mtx][0], af[mtx][1], af[mtx][2], af[mtx][3]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int jp = 0; jp < JT; jp += 2) {
+        // B fragments of tiles jp, jp+1 for each V term: [term][b0 jp, b1 jp, b0 jp+1, b1 jp+1]
+        uint32_t bf[kVTerms][4];
 #pragma unroll
-        for (int j = 0; j < TJ; ++j) acc[i][j] = fmaf(av[i], vv[j], acc[i][j]);
+        for (int term = 0; term < kVTerms; ++term) {
+          const int j = 8 * (jp + (lane >> 4)) + (lane & 7);
+          const int k = kk + 8 * ((lane >> 3) & 1);
+          ldsm_x4(st + 2 * G::kWBytes + ((term * RP + j) * G::kVRow + k) * 2, bf[term][0],
+                  bf[term][1], bf[term][2], bf[term][3]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (jp + h >= JT) break;
+          float (&c)[4] = acc[jp + h];
+#pragma unroll
+          for (int term = 0; term < kVTerms; ++term) {
+            const uint32_t b0 = bf[term][2 * h], b1 = bf[term][2 * h + 1];
+            mma_bf16_16816(c, af[0][0], af[0][1], af[0][2], af[0][3], b0, b1);
+            mma_bf16_16816(c, af[1][0], af[1][1], af[1][2], af[1][3], b0 ^ 0x80008000u,
+                           b1 ^ 0x80008000u);
+          }
+        }
+      }
     }
-    __syncthreads();
   }
+  cp_async_wait<0>();
   float* dst = dst_all + blockIdx.z * dst_stride + static_cast<int64_t>(blockIdx.y) * A * RP;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t a = a0 + 8 * ty + i;
+  for (int h = 0; h < 2; ++h) {
+    const int64_t a = a0 + 16 * warp + g + 8 * h;
     if (a >= A) continue;
 #pragma unroll
-    for (int j = 0; j < TJ; j += 2)
-      *reinterpret_cast<float2*>(dst + a * RP + TJ * tx + j) = make_float2(acc[i][j], acc[i][j + 1]);
+    for (int jt = 0; jt < JT; ++jt)
+      *reinterpret_cast<float2*>(dst + a * RP + 8 * jt + 2 * t) =
+          make_float2(acc[jt][2 * h], acc[jt][2 * h + 1]);
   }
 }
 
@@ -310,6 +412,67 @@ __global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(
     }
   }
   __syncthreads();
+  if constexpr (RP <= 32) {
+    // Register form (rank <= 32): lane i holds row i of G, then column i of
+    // L⁻¹; pivots and multipliers travel by shuffles.
+    if (tid < 32) {
+      const unsigned full = 0xFFFFFFFFu;
+      float gr[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) gr[k] = (lane < r && k < r) ? g[lane][k] : 0.f;
+      float diag = 0.f;
+#pragma unroll
+      for (int k = 0; k < RP; ++k)
+        if (k == lane) diag = gr[k];
+      float mx = diag;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(full, mx, o));
+      const float thr = 1e-6f * mx;
+      float my_inv = 0.f;  // inv_d of this lane's row
+#pragma unroll
+      for (int j = 0; j < RP; ++j) {
+        const float d = __shfl_sync(full, gr[j], j);  // G[j][j] after the updates
+        const bool live = d > thr && thr > 0.f && j < r;
+        const float sd = live ? sqrtf(d) : 0.f;
+        const float id = live ? 1.f / sd : 0.f;
+        const float lij = lane > j ? gr[j] * id : 0.f;  // L[lane][j]
+        if (lane == j) {
+          gr[j] = sd;
+          my_inv = id;
+        }
+        if (lane > j) gr[j] = lij;
+#pragma unroll
+        for (int k = j + 1; k < RP; ++k) {
+          const float lkj = __shfl_sync(full, lij, k);  // L[k][j]
+          if (lane >= k) gr[k] = fmaf(-lij, lkj, gr[k]);
+        }
+      }
+      // X = L⁻¹, column `lane`: x[i] = (δ_i,lane − Σ_{m<i} L[i][m]·x[m]) · inv_d[i]
+      float xc[RP];
+#pragma unroll
+      for (int i = 0; i < RP; ++i) {
+        float s0 = lane == i ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < i; ++m) {
+          const float lim = __shfl_sync(full, gr[m], i);  // L[i][m]
+          if (m & 1)
+            s1 = fmaf(-lim, xc[m], s1);
+          else
+            s0 = fmaf(-lim, xc[m], s0);
+        }
+        const float di = __shfl_sync(full, my_inv, i);
+        xc[i] = lane <= i ? (s0 + s1) * di : 0.f;
+      }
+      // T = Xᵀ: row `lane` of T is column `lane` of X
+      if (lane < RP) {
+#pragma unroll
+        for (int i = 0; i < RP; ++i) x[lane][i] = (lane < r && i < r) ? xc[i] : 0.f;
+      }
+    }
+    __syncthreads();
+    for (int q = tid; q < RP * RP; q += kMsThreads) t_out[q] = x[q / RP][q % RP];
+    return;
+  }
   if (tid < 32) {
     float mx = 0.f;
 #pragma unroll
@@ -483,7 +646,7 @@ __global__ void __launch_bounds__(kMsThreads) merge_kernel(
 
 struct MsLayout {
   int rp = 0;
-  size_t omega = 0, z = 0, part = 0, gpart = 0, t = 0, p = 0, r = 0, total = 0;
+  size_t omega = 0, z = 0, part = 0, gpart = 0, t = 0, vsplit = 0, p = 0, r = 0, total = 0;
 };
 
 int padded_rank(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
@@ -492,7 +655,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace: Ω (d_in × RP), Z (k × d_in × RP), split partials (at most
 // kMaxSplit outputs of the longer side, over all checkpoints), Gram partials
-// (k × slabs × RP²), T (k × RP²), factors Y_i = P (k × d_out × RP) and
+// (k × slabs × RP²), T (k × RP²), the bf16 terms of V (k × 2 × RP × the
+// longer side rounded up to 8), factors Y_i = P (k × d_out × RP) and
 // R_i (k × d_in × RP).
 MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
   MsLayout L;
@@ -511,6 +675,7 @@ MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
   L.part = take(kMaxSplit * a_max * rp * 4);
   L.gpart = take(kk * ((a_max + kSlab - 1) / kSlab) * rp * rp * 4);
   L.t = take(kk * rp * rp * 4);
+  L.vsplit = take(kk * kVTerms * rp * ((a_max + 7) / 8 * 8) * 2);
   L.p = take(kk * d_out * rp * 4);
   L.r = take(kk * d_in * rp * 4);
   L.total = off;
@@ -529,32 +694,60 @@ struct MsRunner {
 
   float* f(size_t off) const { return reinterpret_cast<float*>(ws + off); }
 
-  // CTAs of a Δ-product kernel that fit on one SM (queried once per kernel)
-  static int resident_ctas(bool trans) {
-    static int occ[2] = {0, 0};
-    int& o = occ[trans ? 1 : 0];
-    if (o == 0) {
+  // CTAs of a Δ-product kernel that fit on one SM (queried once per kernel,
+  // after its dynamic shared-memory limit is raised)
+  template <bool kT>
+  static int resident_ctas() {
+    static int occ = 0;
+    if (occ == 0) {
+      const size_t smem = mul_smem_bytes<RP, kT>();
       int n = 0;
-      const cudaError_t e =
-          trans ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_mul_kernel<RP, true>,
-                                                                kMulThreads, 0)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_mul_kernel<RP, false>,
-                                                                kMulThreads, 0);
-      o = (e == cudaSuccess && n > 0) ? n : 2;
+      if (cudaFuncSetAttribute(delta_mul_kernel<RP, kT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_mul_kernel<RP, kT>,
+                                                        kMulThreads, smem) == cudaSuccess &&
+          n > 0)
+        occ = n;
+      else
+        occ = -1;
     }
-    return o;
+    return occ;
   }
 
   // out_i = Δ_i·V_i (trans: Δ_iᵀ·V_i) for every checkpoint i; V_i at
-  // v + i·v_stride, out_i at out + i·out_stride.  Split over the contracted
-  // side so that the grid is about one even wave; *n_split = 0 when the
-  // outputs are complete, else the number of partials left in L.part.
+  // v + i·v_stride (one V for all when v_stride is 0), out_i at
+  // out + i·out_stride.  V is first split into three bf16 terms; the product
+  // is split over the contracted side so that the grid is about one even
+  // wave; *n_split = 0 when the outputs are complete, else the number of
+  // partials left in L.part.
   cudaError_t delta_mul(bool trans, const float* v, int64_t v_stride, float* out,
                         int64_t out_stride, int* n_split) const {
-    const int64_t A = trans ? a.d_in : a.d_out;
-    const int64_t B = trans ? a.d_out : a.d_in;
+    return trans ? delta_mul_t<true>(v, v_stride, out, out_stride, n_split)
+                 : delta_mul_t<false>(v, v_stride, out, out_stride, n_split);
+  }
+
+  template <bool kT>
+  cudaError_t delta_mul_t(const float* v, int64_t v_stride, float* out, int64_t out_stride,
+                          int* n_split) const {
+    const int64_t A = kT ? a.d_in : a.d_out;
+    const int64_t B = kT ? a.d_out : a.d_in;
+    const int64_t bp = (B + 7) / 8 * 8;
+    const int nz = v_stride == 0 ? 1 : a.k;
+    uint16_t* vs = reinterpret_cast<uint16_t*>(ws + L.vsplit);
+    {
+      const int64_t n = bp / 8 * RP;
+      int64_t blocks = (n + 255) / 256;
+      if (blocks > 2048) blocks = 2048;
+      vsplit_kernel<<<dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(nz)), 256, 0,
+                      s>>>(v, v_stride, B, bp, RP, vs);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    const int occ = resident_ctas<kT>();
+    if (occ < 0) return cudaErrorInvalidConfiguration;
     const int64_t a_blocks = (A + kTileA - 1) / kTileA;
-    const int64_t want = static_cast<int64_t>(resident_ctas(trans)) * num_sms;
+    const int64_t want = static_cast<int64_t>(occ) * num_sms;
     int64_t split = want / (a_blocks * a.k);
     const int64_t split_max = kMaxSplit / a.k > 1 ? kMaxSplit / a.k : 1;
     if (split > split_max) split = split_max;
@@ -567,12 +760,9 @@ struct MsRunner {
     const int64_t dst_stride = split == 1 ? out_stride : split * A * RP;
     const dim3 grid(static_cast<unsigned>(a_blocks), static_cast<unsigned>(split),
                     static_cast<unsigned>(a.k));
-    if (trans)
-      delta_mul_kernel<RP, true><<<grid, kMulThreads, 0, s>>>(tab, a.w_base, a.d_out, a.d_in, v,
-                                                              v_stride, dst, dst_stride, b_chunk);
-    else
-      delta_mul_kernel<RP, false><<<grid, kMulThreads, 0, s>>>(tab, a.w_base, a.d_out, a.d_in, v,
-                                                               v_stride, dst, dst_stride, b_chunk);
+    delta_mul_kernel<RP, kT><<<grid, kMulThreads, mul_smem_bytes<RP, kT>(), s>>>(
+        tab, a.w_base, a.d_out, a.d_in, vs, v_stride == 0 ? 0 : kVTerms * RP * bp, bp, dst,
+        dst_stride, b_chunk);
     *n_split = split == 1 ? 0 : static_cast<int>(split);
     return cudaGetLastError();
   }
