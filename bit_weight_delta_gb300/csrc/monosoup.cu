@@ -16,7 +16,7 @@
 // gap after σ_r a few iterations reach the truncation to fp32 accuracy.
 // orth() is Cholesky QR: G = AᵀA (r × r), G = L·Lᵀ, A ← A·L⁻ᵀ; a column whose
 // pivot falls below 1e-6 of the largest diagonal entry is dependent and is
-// dropped (zeroed).  The merge is one pass over W_base:
+// dropped (zeroed).  The merge is one tensor-core pass over W_base:
 //     W_merged = bf16_rne(W_base + (1/k)·Σ_i Y_i·R_iᵀ).
 //
 // Factor matrices are fp32, row-major with RP columns (r padded to 16, 32 or
@@ -570,75 +570,147 @@ __global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restri
   }
 }
 
-// W_merged = bf16_rne(W_base + inv_k·Σ_i P_i·R_iᵀ) over 64 × 64 tiles.
-template <int RP>
-__global__ void __launch_bounds__(kMsThreads) merge_kernel(
-    const uint16_t* __restrict__ wb, const float* __restrict__ p_fac,
-    const float* __restrict__ r_fac, int k, int64_t d_out, int64_t d_in, float inv_k,
+// Factor split for the tensor-core merge: the k checkpoints' factors
+// F_i (rows × RP fp32, rows·RP apart), scaled by `scale`, side by side as
+// two bf16 terms hi + lo of rows × kp (kp = k·RP; column i·RP + j holds
+// F_i[row][j]).  A thread converts 8 consecutive columns of one row.
+__global__ void fsplit_kernel(const float* __restrict__ f, int64_t rows, int rp, int k,
+                              float scale, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+  const int64_t kp = static_cast<int64_t>(k) * rp;
+  const int64_t n8 = rows * (kp / 8);
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = q / (kp / 8);
+    const int64_t col = 8 * (q - row * (kp / 8));
+    const int64_t i = col / rp, j = col - i * rp;
+    const float4* src = reinterpret_cast<const float4*>(f + (i * rows + row) * rp + j);
+    const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float a = xv[e] * scale, b = xv[e + 1] * scale;
+      const uint32_t h = pack_bf16x2_rn(a, b);
+      hw[e / 2] = h;
+      lw[e / 2] = pack_bf16x2_rn(a - __uint_as_float(h << 16), b - __uint_as_float(h & 0xFFFF0000u));
+    }
+    *reinterpret_cast<uint4*>(hi + row * kp + col) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo + row * kp + col) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+constexpr int kMergeTile = 64;   // output rows and columns per CTA
+constexpr int kMergeK = 64;      // K per stage
+constexpr int kMergeRow = kMergeK + 8;  // bf16 per smem row (conflict-free ldmatrix)
+constexpr int kMergeStageBytes = 4 * kMergeTile * kMergeRow * 2;  // P hi, P lo, R hi, R lo
+constexpr size_t kMergeSmem = 2 * static_cast<size_t>(kMergeStageBytes);
+
+// W_merged = bf16_rne(W_base + Σ_K P'[n][K]·R[c][K]) with P' = P/k, on the
+// tensor cores: P' = Phi + Plo and R = Rhi + Rlo (bf16, fsplit_kernel), three
+// products per tile (Phi·Rhi + Phi·Rlo + Plo·Rhi; the dropped Plo·Rlo is
+// 2^-18 relative), fp32 accumulation.  CTA: 64 × 64 outputs, 4 warps of
+// 16 rows × 64 columns; K in stages of 64 through a two-deep cp.async ring.
+__global__ void __launch_bounds__(kMulThreads) merge_kernel(
+    const uint16_t* __restrict__ wb, const uint16_t* __restrict__ phi,
+    const uint16_t* __restrict__ plo, const uint16_t* __restrict__ rhi,
+    const uint16_t* __restrict__ rlo, int64_t kp, int64_t d_out, int64_t d_in,
     uint16_t* __restrict__ out, float* __restrict__ corr) {
-  __shared__ __align__(16) float ps[16][64 + 4];  // [j][n]
-  __shared__ __align__(16) float rs[16][64 + 4];  // [j][c]
+  constexpr int JT = kMergeTile / 8;
+  extern __shared__ __align__(16) uint8_t sm[];
   const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 64;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  const int lr = tid >> 2, lj = tid & 3;  // loader: row of the tile, 4 columns of the step
-  for (int i = 0; i < k; ++i) {
-    const float* pi = p_fac + static_cast<int64_t>(i) * d_out * RP;
-    const float* ri = r_fac + static_cast<int64_t>(i) * d_in * RP;
-    for (int j0 = 0; j0 < RP; j0 += 16) {
-      const int64_t n = n0 + lr, c = c0 + lr;
-      const float4 pv = n < d_out ? __ldg(reinterpret_cast<const float4*>(pi + n * RP + j0) + lj)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 rv = c < d_in ? __ldg(reinterpret_cast<const float4*>(ri + c * RP + j0) + lj)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-      ps[4 * lj + 0][lr] = pv.x;
-      ps[4 * lj + 1][lr] = pv.y;
-      ps[4 * lj + 2][lr] = pv.z;
-      ps[4 * lj + 3][lr] = pv.w;
-      rs[4 * lj + 0][lr] = rv.x;
-      rs[4 * lj + 1][lr] = rv.y;
-      rs[4 * lj + 2][lr] = rv.z;
-      rs[4 * lj + 3][lr] = rv.w;
-      __syncthreads();
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const float4 p4 = *reinterpret_cast<const float4*>(&ps[jj][4 * ty]);
-        const float4 r4 = *reinterpret_cast<const float4*>(&rs[jj][4 * tx]);
-        const float pv4[4] = {p4.x, p4.y, p4.z, p4.w};
-        const float rv4[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(pv4[a], rv4[b], acc[a][b]);
+  const int lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kMergeTile;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kMergeTile;
+  const uint32_t sm_sa = smem_addr(sm);
+  const int n_steps = static_cast<int>((kp + kMergeK - 1) / kMergeK);
+  constexpr int kMat = kMergeTile * kMergeRow * 2;  // bytes of one matrix tile
+
+  auto issue = [&](int stage, int step) {
+    if (step < n_steps) {
+      const int64_t k0 = static_cast<int64_t>(step) * kMergeK;
+      const uint32_t st = sm_sa + stage * kMergeStageBytes;
+      uint8_t* stp = sm + stage * kMergeStageBytes;
+      // 4 matrices × 64 rows × 8 vectors of 8 bf16
+      for (int q = tid; q < 4 * kMergeTile * (kMergeK / 8); q += kMulThreads) {
+        const int mtx = q / (kMergeTile * (kMergeK / 8));
+        const int rem = q - mtx * kMergeTile * (kMergeK / 8);
+        const int row = rem >> 3, col = 8 * (rem & 7);
+        const bool is_p = mtx < 2;
+        const int64_t grow = (is_p ? n0 : c0) + row;
+        const int64_t gk = k0 + col;
+        const uint16_t* src = mtx == 0 ? phi : mtx == 1 ? plo : mtx == 2 ? rhi : rlo;
+        const uint32_t off = static_cast<uint32_t>(mtx * kMat + (row * kMergeRow + col) * 2);
+        if (grow < (is_p ? d_out : d_in) && gk < kp)
+          cp16(st + off, src + grow * kp + gk);
+        else
+          *reinterpret_cast<uint4*>(stp + off) = make_uint4(0, 0, 0, 0);
       }
-      __syncthreads();
+    }
+    cp_async_commit();
+  };
+
+  float acc[JT][4];
+#pragma unroll
+  for (int jt = 0; jt < JT; ++jt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[jt][e] = 0.f;
+
+  issue(0, 0);
+  for (int step = 0; step < n_steps; ++step) {
+    cp_async_wait<0>();
+    __syncthreads();  // stage `step` complete everywhere; the other slot is free
+    issue((step + 1) & 1, step + 1);
+    const uint32_t st = sm_sa + (step & 1) * kMergeStageBytes;
+#pragma unroll
+    for (int kk = 0; kk < kMergeK; kk += 16) {
+      uint32_t ap[2][4];
+#pragma unroll
+      for (int term = 0; term < 2; ++term) {
+        const int m = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int k = kk + 8 * (lane >> 4);
+        ldsm_x4(st + term * kMat + (m * kMergeRow + k) * 2, ap[term][0], ap[term][1], ap[term][2],
+                ap[term][3]);
+      }
+#pragma unroll
+      for (int jp = 0; jp < JT; jp += 2) {
+        uint32_t bq[2][4];
+#pragma unroll
+        for (int term = 0; term < 2; ++term) {
+          const int j = 8 * (jp + (lane >> 4)) + (lane & 7);
+          const int k = kk + 8 * ((lane >> 3) & 1);
+          ldsm_x4(st + (2 + term) * kMat + (j * kMergeRow + k) * 2, bq[term][0], bq[term][1],
+                  bq[term][2], bq[term][3]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float (&c)[4] = acc[jp + h];
+          const uint32_t bh0 = bq[0][2 * h], bh1 = bq[0][2 * h + 1];
+          const uint32_t bl0 = bq[1][2 * h], bl1 = bq[1][2 * h + 1];
+          mma_bf16_16816(c, ap[0][0], ap[0][1], ap[0][2], ap[0][3], bh0, bh1);
+          mma_bf16_16816(c, ap[0][0], ap[0][1], ap[0][2], ap[0][3], bl0, bl1);
+          mma_bf16_16816(c, ap[1][0], ap[1][1], ap[1][2], ap[1][3], bh0, bh1);
+        }
+      }
     }
   }
-  const int64_t c = c0 + 4 * tx;
-  if (c >= d_in) return;  // d_in % 8 == 0: the 4 columns are wholly inside or outside
+  cp_async_wait<0>();
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int64_t n = n0 + 4 * ty + a;
+  for (int h = 0; h < 2; ++h) {
+    const int64_t n = n0 + 16 * warp + g + 8 * h;
     if (n >= d_out) continue;
-    const uint2 w = *reinterpret_cast<const uint2*>(wb + n * d_in + c);
-    const float base[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
-                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)};
-    float cv[4], mv[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      cv[b] = inv_k * acc[a][b];
-      mv[b] = base[b] + cv[b];
+    for (int jt = 0; jt < JT; ++jt) {
+      const int64_t c = c0 + 8 * jt + 2 * t;
+      if (c >= d_in) continue;  // d_in % 8 == 0: c and c + 1 are inside together
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(wb + n * d_in + c);
+      const float cv0 = acc[jt][2 * h], cv1 = acc[jt][2 * h + 1];
+      const float m0 = __uint_as_float(w << 16) + cv0;
+      const float m1 = __uint_as_float(w & 0xFFFF0000u) + cv1;
+      *reinterpret_cast<uint32_t*>(out + n * d_in + c) = pack_bf16x2_rn(m0, m1);
+      if (corr != nullptr)
+        *reinterpret_cast<float2*>(corr + n * d_in + c) = make_float2(cv0, cv1);
     }
-    *reinterpret_cast<uint2*>(out + n * d_in + c) =
-        make_uint2(pack_bf16x2_rn(mv[0], mv[1]), pack_bf16x2_rn(mv[2], mv[3]));
-    if (corr != nullptr)
-      *reinterpret_cast<float4*>(corr + n * d_in + c) = make_float4(cv[0], cv[1], cv[2], cv[3]);
   }
 }
 
@@ -646,7 +718,8 @@ __global__ void __launch_bounds__(kMsThreads) merge_kernel(
 
 struct MsLayout {
   int rp = 0;
-  size_t omega = 0, z = 0, part = 0, gpart = 0, t = 0, vsplit = 0, p = 0, r = 0, total = 0;
+  size_t omega = 0, z = 0, part = 0, gpart = 0, t = 0, vsplit = 0, fsplit = 0, p = 0, r = 0,
+         total = 0;
 };
 
 int padded_rank(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
@@ -656,7 +729,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // Workspace: Ω (d_in × RP), Z (k × d_in × RP), split partials (at most
 // kMaxSplit outputs of the longer side, over all checkpoints), Gram partials
 // (k × slabs × RP²), T (k × RP²), the bf16 terms of V (k × 2 × RP × the
-// longer side rounded up to 8), factors Y_i = P (k × d_out × RP) and
+// longer side rounded up to 8), the bf16 terms of the factors for the merge
+// (2 × k·RP × (d_out + d_in)), factors Y_i = P (k × d_out × RP) and
 // R_i (k × d_in × RP).
 MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
   MsLayout L;
@@ -676,6 +750,7 @@ MsLayout ms_layout(int64_t d_out, int64_t d_in, int k, int r) {
   L.gpart = take(kk * ((a_max + kSlab - 1) / kSlab) * rp * rp * 4);
   L.t = take(kk * rp * rp * 4);
   L.vsplit = take(kk * kVTerms * rp * ((a_max + 7) / 8 * 8) * 2);
+  L.fsplit = take(2 * kk * rp * (static_cast<size_t>(d_out) + d_in) * 2);
   L.p = take(kk * d_out * rp * 4);
   L.r = take(kk * d_in * rp * 4);
   L.total = off;
@@ -824,12 +899,34 @@ struct MsRunner {
       if ((e = delta_mul(true, y, ys, r, zs, &ns)) != cudaSuccess) return e;
       if ((e = finish(r, zs, a.d_in, ns)) != cudaSuccess) return e;
     }
-    const dim3 grid(static_cast<unsigned>((a.d_in + 63) / 64),
-                    static_cast<unsigned>((a.d_out + 63) / 64));
-    merge_kernel<RP><<<grid, kMsThreads, 0, s>>>(a.w_base, f(L.p), f(L.r),
-                                                 a.rank > 0 ? a.k : 0, a.d_out, a.d_in,
-                                                 1.0f / static_cast<float>(a.k), a.w_merged,
-                                                 a.correction);
+    // merge: split the factors (P scaled by 1/k) into bf16 terms, then one
+    // tensor-core pass over W_base
+    const int64_t kp = a.rank > 0 ? static_cast<int64_t>(a.k) * RP : 0;
+    uint16_t* fs = reinterpret_cast<uint16_t*>(ws + L.fsplit);
+    uint16_t* phi = fs;
+    uint16_t* plo = phi + a.d_out * kp;
+    uint16_t* rhi = plo + a.d_out * kp;
+    uint16_t* rlo = rhi + a.d_in * kp;
+    if (kp > 0) {
+      const int64_t np = a.d_out * (kp / 8), nr = a.d_in * (kp / 8);
+      fsplit_kernel<<<static_cast<unsigned>((np + 255) / 256 < 4096 ? (np + 255) / 256 : 4096),
+                      256, 0, s>>>(f(L.p), a.d_out, RP, a.k, 1.0f / static_cast<float>(a.k),
+                                   phi, plo);
+      fsplit_kernel<<<static_cast<unsigned>((nr + 255) / 256 < 4096 ? (nr + 255) / 256 : 4096),
+                      256, 0, s>>>(f(L.r), a.d_in, RP, a.k, 1.0f, rhi, rlo);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    static bool merge_attr = false;
+    if (!merge_attr) {
+      if ((e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kMergeSmem))) != cudaSuccess)
+        return e;
+      merge_attr = true;
+    }
+    const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
+                    static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));
+    merge_kernel<<<grid, kMulThreads, kMergeSmem, s>>>(a.w_base, phi, plo, rhi, rlo, kp, a.d_out,
+                                                       a.d_in, a.w_merged, a.correction);
     return cudaGetLastError();
   }
 };
