@@ -773,7 +773,10 @@ struct MsRunner {
   // after its dynamic shared-memory limit is raised)
   template <bool kT>
   static int resident_ctas() {
-    static int occ = 0;
+    static int occ_dev[64] = {};  // per device: the attribute is per context
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    int& occ = occ_dev[dev];
     if (occ == 0) {
       const size_t smem = mul_smem_bytes<RP, kT>();
       int n = 0;
@@ -916,12 +919,15 @@ struct MsRunner {
                       256, 0, s>>>(f(L.r), a.d_in, RP, a.k, 1.0f, rhi, rlo);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    static bool merge_attr = false;
-    if (!merge_attr) {
+    static bool merge_attr[64] = {};  // per device
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!merge_attr[dev]) {
       if ((e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kMergeSmem))) != cudaSuccess)
         return e;
-      merge_attr = true;
+      merge_attr[dev] = true;
     }
     const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
                     static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));

@@ -70,6 +70,7 @@ def _check_against_oracle(wb, ws, rank, power_iters=2):
     (512, 384, 16, 2),    # d_out > d_in
     (640, 1000, 64, 2),   # the largest rank
     (96, 64, 20, 1),      # one checkpoint, rank padded to 32
+    (203, 256, 12, 2),    # d_out not a multiple of 8 (padded rows of V's bf16 terms)
 ])
 def test_merge_matches_oracle(d_out, d_in, rank, k):
     wb = synth.base_weight(d_out + d_in, d_out, d_in)
