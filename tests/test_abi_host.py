@@ -117,3 +117,63 @@ def test_grouped_rejects_bad_arguments(lib):
     assert call(y=BAD) == MISALIGNED
     assert call(M=0, x=NULL, so=NULL) == OK      # empty batch is a no-op
     assert call(n_seg=0, so=NULL) == OK
+
+
+def test_monosoup_rejects_bad_arguments(lib):
+    f = lib.bitdelta_monosoup
+    table = (ctypes.c_void_p * 2)(GOOD.value, GOOD.value)
+    ws_need = lib.bitdelta_monosoup_workspace_bytes(64, 128, 2, 8)
+    assert ws_need > 0
+    args = dict(wb=GOOD, wft=ctypes.cast(table, ctypes.c_void_p), k=2, rank=8, q=2, d_out=64,
+                d_in=128, out=GOOD, corr=NULL, ws=GOOD, ws_bytes=ws_need)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return f(a["wb"], a["wft"], a["k"], a["rank"], a["q"], 7, a["d_out"], a["d_in"],
+                 a["out"], a["corr"], a["ws"], a["ws_bytes"], NULL)
+
+    assert call(wb=NULL) == INVALID
+    assert call(wft=NULL) == INVALID
+    assert call(out=NULL) == INVALID
+    assert call(d_in=100) == SHAPE           # d_in % 8 != 0
+    assert call(k=0) == SHAPE
+    assert call(k=65) == SHAPE
+    assert call(rank=65) == SHAPE
+    assert call(rank=-1) == SHAPE
+    assert call(rank=65, d_out=64) == SHAPE
+    assert call(d_out=4, rank=8) == SHAPE     # rank above min(d_out, d_in)
+    assert call(q=17) == SHAPE
+    assert call(out=BAD) == MISALIGNED
+    assert call(corr=BAD) == MISALIGNED
+    assert call(ws=BAD) == MISALIGNED
+    assert call(ws_bytes=ws_need - 1) == WORKSPACE
+    bad_table = (ctypes.c_void_p * 2)(GOOD.value, BAD.value)
+    assert call(wft=ctypes.cast(bad_table, ctypes.c_void_p)) == MISALIGNED
+    null_table = (ctypes.c_void_p * 2)(GOOD.value, 0)
+    assert call(wft=ctypes.cast(null_table, ctypes.c_void_p)) == INVALID
+    assert lib.bitdelta_monosoup_workspace_bytes(64, 100, 2, 8) == 0   # bad shape: 0
+
+
+def test_sign_similarity_rejects_bad_arguments(lib):
+    f = lib.bitdelta_sign_similarity
+    ws_need = lib.bitdelta_sign_similarity_workspace_bytes(64, 3)
+    assert ws_need > 0
+    args = dict(pa=GOOD, aa=GOOD, pt=GOOD, at=GOOD, n_b=3, mode=1, d_out=64, d_in=128, cos=GOOD,
+                best=GOOD, ws=GOOD, ws_bytes=ws_need)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return f(a["pa"], a["aa"], a["pt"], a["at"], a["n_b"], a["mode"], a["d_out"], a["d_in"],
+                 a["cos"], a["best"], a["ws"], a["ws_bytes"], NULL)
+
+    assert call(pa=NULL) == INVALID
+    assert call(pt=NULL) == INVALID
+    assert call(cos=NULL) == INVALID
+    assert call(mode=5) == INVALID
+    assert call(d_in=12) == SHAPE
+    assert call(n_b=0) == SHAPE
+    assert call(n_b=257) == SHAPE
+    assert call(cos=BAD) == MISALIGNED
+    assert call(ws=BAD) == MISALIGNED
+    assert call(ws_bytes=ws_need - 1) == WORKSPACE
+    assert lib.bitdelta_sign_similarity_workspace_bytes(64, 0) == 0
