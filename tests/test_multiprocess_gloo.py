@@ -38,7 +38,7 @@ def _worker(rank, world, port, times, out):
 def test_max_over_ranks_two_processes():
     times = [3.25, 7.5]
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(2, port, times, out), nprocs=2, join=True)
         assert dict(out) == {0: 7.5, 1: 7.5}
