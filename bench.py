@@ -773,7 +773,11 @@ def timed_run(cudart, wl, steps, warmup, dist, clock=None, graph_steps=None):
 def e2e_decode(bd, steps: int):
     """End to end through the public API: per step, pinned host -> device copy
     of one layer's inputs (W_base, W_ft, x), compress, reconstruct, fused
-    linear at M = 1..16, device -> host copy of the results."""
+    linear at M = 1..16, device -> host copy of the results.  Steps are
+    pipelined the way a server streams layers: two buffer sets, copies in on
+    one stream, compute on a second, copies out on a third, ordered by events
+    (step i's upload overlaps step i-1's compute and step i-2's download).
+    Every step's own copies lie inside the timed region."""
     import synth
     d = 4096
     Ms = (1, 2, 4, 8, 16)
@@ -781,53 +785,78 @@ def e2e_decode(bd, steps: int):
     x_h = synth.activations(21, max(Ms), d)
 
     def pinned(a):
-        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
-        return t
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
     hb, hf, hx = pinned(wb_h), pinned(wf_h), pinned(x_h)
-    db = torch.empty_like(hb, device="cuda")
-    df = torch.empty_like(hf, device="cuda")
-    dx = torch.empty_like(hx, device="cuda")
-    packed = torch.empty((d, d // 8), dtype=torch.uint8, device="cuda")
-    alpha = torch.empty((d,), dtype=torch.float32, device="cuda")
-    w_eff = torch.empty((d, d), dtype=torch.bfloat16, device="cuda")
-    ys = {M: torch.empty((M, d), dtype=torch.bfloat16, device="cuda") for M in Ms}
-    o_packed = torch.empty(packed.shape, dtype=torch.uint8).pin_memory()
-    o_alpha = torch.empty(alpha.shape, dtype=torch.float32).pin_memory()
-    o_weff = torch.empty(w_eff.shape, dtype=torch.bfloat16).pin_memory()
-    o_ys = {M: torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for M in Ms}
+    sets = []
+    for _ in range(2):
+        st = {
+            "db": torch.empty_like(hb, device="cuda"), "df": torch.empty_like(hf, device="cuda"),
+            "dx": torch.empty_like(hx, device="cuda"),
+            "packed": torch.empty((d, d // 8), dtype=torch.uint8, device="cuda"),
+            "alpha": torch.empty((d,), dtype=torch.float32, device="cuda"),
+            "w_eff": torch.empty((d, d), dtype=torch.bfloat16, device="cuda"),
+            "ys": {M: torch.empty((M, d), dtype=torch.bfloat16, device="cuda") for M in Ms},
+            "o_packed": torch.empty((d, d // 8), dtype=torch.uint8).pin_memory(),
+            "o_alpha": torch.empty((d,), dtype=torch.float32).pin_memory(),
+            "o_weff": torch.empty((d, d), dtype=torch.bfloat16).pin_memory(),
+            "o_ys": {M: torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for M in Ms},
+            "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
+            "ev_out": torch.cuda.Event(),
+        }
+        sets.append(st)
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def step():
-        db.copy_(hb, non_blocking=True)
-        df.copy_(hf, non_blocking=True)
-        dx.copy_(hx, non_blocking=True)
-        bd.bitdelta_compress(db, df, per_row=True, packed_out=packed, alpha_out=alpha)
-        bd.bitdelta_reconstruct(db, packed, alpha, per_row=True, out=w_eff)
-        for M in Ms:
-            bd.bitdelta_linear(dx[:M], db, packed, alpha, per_row=True, out=ys[M])
-        o_packed.copy_(packed, non_blocking=True)
-        o_alpha.copy_(alpha, non_blocking=True)
-        o_weff.copy_(w_eff, non_blocking=True)
-        for M in Ms:
-            o_ys[M].copy_(ys[M], non_blocking=True)
+    def step(i):
+        st = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(st["ev_comp"])          # step i-2 has finished reading this set
+            st["db"].copy_(hb, non_blocking=True)
+            st["df"].copy_(hf, non_blocking=True)
+            st["dx"].copy_(hx, non_blocking=True)
+            st["ev_in"].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(st["ev_in"])
+            s_comp.wait_event(st["ev_out"])         # step i-2's results have left
+            bd.bitdelta_compress(st["db"], st["df"], per_row=True, packed_out=st["packed"],
+                                 alpha_out=st["alpha"], stream=s_comp)
+            bd.bitdelta_reconstruct(st["db"], st["packed"], st["alpha"], per_row=True,
+                                    out=st["w_eff"], stream=s_comp)
+            for M in Ms:
+                bd.bitdelta_linear(st["dx"][:M], st["db"], st["packed"], st["alpha"],
+                                   per_row=True, out=st["ys"][M], stream=s_comp)
+            st["ev_comp"].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(st["ev_comp"])
+            st["o_packed"].copy_(st["packed"], non_blocking=True)
+            st["o_alpha"].copy_(st["alpha"], non_blocking=True)
+            st["o_weff"].copy_(st["w_eff"], non_blocking=True)
+            for M in Ms:
+                st["o_ys"][M].copy_(st["ys"][M], non_blocking=True)
+            st["ev_out"].record(s_out)
 
-    for _ in range(3):
-        step()
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    s_comp.wait_event(start)
+    s_out.wait_event(start)
+    for i in range(steps):
+        step(i)
+    s_in.wait_stream(s_comp)
+    s_in.wait_stream(s_out)
+    end.record(s_in)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    ms = start.elapsed_time(end) / steps
     h2d = hb.numel() * 2 + hf.numel() * 2 + hx.numel() * 2
-    d2h = packed.numel() + alpha.numel() * 4 + w_eff.numel() * 2 + sum(
-        M * d * 2 for M in Ms)
+    d2h = d * (d // 8) + d * 4 + d * d * 2 + sum(M * d * 2 for M in Ms)
     n = d * d
     alg = 2 * (n * (4 + 1 / 8) + 4 * d) + sum(n * (2 + 1 / 8) + 4 * d + 2 * M * 2 * d for M in Ms)
     return {"value": alg / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
-            "note": "one 4096x4096 layer per step, inputs copied from pinned host memory"}
+            "note": "one 4096x4096 layer per step, inputs copied from pinned host memory; "
+                    "steps pipelined on copy-in / compute / copy-out streams with two "
+                    "buffer sets"}
 
 
 # --------------------------------------------------------------------------- main
