@@ -326,6 +326,34 @@ class Prefill:
                 times.append(s.elapsed_time(e))
             t = statistics.median(times[2:])
             out[mode] = {"ms_per_step": t, "tflops": self.flops_per_step() / (t * 1e-3) / 1e12}
+        # fused against unfused at fewer tokens (same four shapes, eager launches
+        # for both): the unfused path pays its reconstruct once per weight, the
+        # fused kernel its transform once per 256-token tile
+        out["fused_vs_unfused_by_tokens"] = {}
+        for m in (512, 1024):
+            res = {}
+            for mode in ("fused", "unfused"):
+                times = []
+                for _ in range(reps + 2):
+                    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s.record()
+                    for nm, d_out, d_in in self.shapes:
+                        wb, packed, alpha = self.mats[nm]
+                        x = self.x[d_in][:m]
+                        y = self.y[nm][:m]
+                        if mode == "unfused":
+                            self.bd.bitdelta_reconstruct(wb, packed, alpha, per_row=True,
+                                                         out=w_eff[nm])
+                            torch.matmul(x, w_eff[nm].T, out=y)
+                        else:
+                            self.bd.bitdelta_linear(x, wb, packed, alpha, per_row=True, out=y)
+                    e.record()
+                    torch.cuda.synchronize()
+                    times.append(s.elapsed_time(e))
+                t = statistics.median(times[2:])
+                fl = self.flops_per_step() * m / self.M
+                res[mode] = {"ms_per_step": t, "tflops": fl / (t * 1e-3) / 1e12}
+            out["fused_vs_unfused_by_tokens"][f"M{m}"] = res
         del w_eff
         return out
 
@@ -1070,6 +1098,7 @@ def main():
                                for p in pre.phases},
             "cublas_bf16_gemm_same_shapes": ref["cublas_plain"],
             "unfused_reconstruct_plus_cublas": ref["unfused"],
+            "fused_vs_unfused_by_tokens": ref["fused_vs_unfused_by_tokens"],
             "frac_of_cublas": ref["cublas_plain"]["ms_per_step"] / pms,
         }
         del pre
