@@ -53,7 +53,7 @@ def test_weak_scaling_value_counts_every_rank():
 
 
 def test_reference_arm_under_torchrun_two_ranks():
-    """bench.py --impl reference launched like the driver launches N > 1:
+    """bench.py --impl reference launched by torchrun with N > 1 ranks:
     rank 0 times the oracle and prints one JSON line, rank 1 exits 0."""
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
