@@ -161,3 +161,36 @@ def test_wait_timeout_is_reported():
     x = synth.activations(0, 2, 128)
     assert_linear_close(bf16_values(_run(x, wb, packed, alpha, True)),
                         oracle.linear(x, wb, packed, alpha, True))
+
+
+@pytest.mark.parametrize("shape", [(37, 256), (250, 1024), (1, 128), (17, 384)])
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_decode_ring_ragged_d_out(shape, M):
+    """d_in a multiple of 128 (the cp.async ring for M <= 8) with a d_out that
+    leaves the last CTA a partial group of 16 rows, and empty token slots."""
+    d_out, d_in = shape
+    wb, packed, alpha = _layer(3, d_out, d_in, True)
+    x = synth.activations(3, M, d_in)
+    y = _run(x, wb, packed, alpha, True)
+    assert bd.bitdelta_check_error() == 0
+    assert_linear_close(bf16_values(y), oracle.linear(x, wb, packed, alpha, True),
+                        f"{shape} M={M}")
+
+
+@pytest.mark.parametrize("M", [2, 8, 16])
+def test_decode_unaligned_sign_rows(M):
+    """Packed signs starting 8 bytes past a 16-byte boundary on a d_in that
+    the ring could take: the register kernel with byte-wise sign loads runs
+    instead, and matches the oracle."""
+    import torch
+    d_out, d_in = 96, 512
+    wb, packed, alpha = _layer(4, d_out, d_in, True)
+    raw = torch.empty(packed.size + 8, dtype=torch.uint8, device="cuda")
+    shifted = raw[8:8 + packed.size].view(packed.shape)
+    shifted.copy_(bd_tensor(packed))
+    assert shifted.data_ptr() % 16 == 8
+    x = synth.activations(4, M, d_in)
+    y = bd.bitdelta_linear(to_dev_bf16(x), to_dev_bf16(wb), shifted, bd_tensor(alpha),
+                           per_row=True)
+    assert bd.bitdelta_check_error() == 0
+    assert_linear_close(bf16_values(y), oracle.linear(x, wb, packed, alpha, True), f"M={M}")
