@@ -32,6 +32,7 @@ EXPORTED = (
     "bitdelta_packed_bytes", "bitdelta_compress_workspace_bytes", "bitdelta_compress",
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
+    "bitdelta_set_prefill_tile",
     "bitdelta_status_string", "bitdelta_compress_noalloc", "bitdelta_sign_similarity",
     "bitdelta_sign_similarity_workspace_bytes", "bitdelta_monosoup",
     "bitdelta_monosoup_workspace_bytes",
@@ -86,6 +87,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_check_error.restype = st
     lib.bitdelta_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.bitdelta_set_wait_limit_ns.restype = st
+    lib.bitdelta_set_prefill_tile.argtypes = [ctypes.c_int]
+    lib.bitdelta_set_prefill_tile.restype = st
     lib.bitdelta_debug_wait_timeout.argtypes = [p]
     lib.bitdelta_debug_wait_timeout.restype = st
     lib.bitdelta_status_string.argtypes = [st]
@@ -262,6 +265,16 @@ def bitdelta_check_error(stream=None) -> int:
 
 def bitdelta_set_wait_limit_ns(ns: int) -> None:
     _check("bitdelta_set_wait_limit_ns", load().bitdelta_set_wait_limit_ns(int(ns)))
+
+
+PREFILL_TILES = {"auto": 0, 256: 1, 512: 2}
+
+
+def bitdelta_set_prefill_tile(tile="auto") -> None:
+    """Token width of the tensor-core kernel's pair tiles: "auto", 256 or 512."""
+    if tile not in PREFILL_TILES:
+        raise ValueError(f"prefill tile must be one of {list(PREFILL_TILES)}, not {tile!r}")
+    _check("bitdelta_set_prefill_tile", load().bitdelta_set_prefill_tile(PREFILL_TILES[tile]))
 
 
 def bitdelta_debug_wait_timeout(stream=None) -> None:

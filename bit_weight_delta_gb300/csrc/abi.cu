@@ -19,6 +19,7 @@ namespace {
 __device__ uint32_t g_error_word;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_prefill_tile{BD_PREFILL_TILE_AUTO};
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDecodeMaxRows = 16;
@@ -108,24 +109,55 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
 #ifndef BD_GEMM_PAIR
 #define BD_GEMM_PAIR 1
 #endif
+// Cost of one 512-token pair tile in 256-token pair tiles, in quarters: the
+// steady state of the two kernels on 8192 x 57344 at M = 2048 measured 1454
+// and 1266 TFLOP/s, 2 x 1266 / 1454 = 1.74.
+constexpr int64_t kWideTileCost4 = 7;
 
-// Launch the tensor-core kernel on g (x has rows_x rows; at most
-// token_tiles_bound 256-token tiles per row tile).  The pair kernel
-// (cta_group::2, 256 output rows per tile) unless built with BD_GEMM_PAIR=0,
-// or when the device cannot place a cluster of two of its CTAs: then the
-// one-CTA kernel.  Returns false, launching nothing, when a tensor map cannot
-// be encoded.
+// 512-token pair tiles for this call?  Under BD_PREFILL_TILE_AUTO the width
+// whose rounds of tiles over the device's pairs cost less: ceil(tiles /
+// pairs) x the cost of one tile.  Token tiles per row tile: ceil(rows_x /
+// width) + extra_tiles (one ragged tile per segment in grouped mode);
+// long_tokens <= 256 (no segment fills half a wide tile) keeps 256.
+bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens, int64_t extra_tiles) {
+  const int policy = g_prefill_tile.load();
+  if (policy == BD_PREFILL_TILE_256) return false;
+  if (policy == BD_PREFILL_TILE_512) return true;
+  if (long_tokens <= bd::gemm_pair_tokens(false)) return false;
+  const int pairs = bd::gemm_pair_capacity(true);
+  if (pairs < 1) return false;  // the launch reports why
+  const int64_t row_tiles = (d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows());
+  auto rounds = [&](bool wide) {
+    const int64_t tok = bd::gemm_pair_tokens(wide);
+    const int64_t tiles = row_tiles * ((rows_x + tok - 1) / tok + extra_tiles);
+    return (tiles + pairs - 1) / pairs;
+  };
+  return rounds(true) * kWideTileCost4 < rounds(false) * 4;
+}
+
+// Launch the tensor-core kernel on g (x has rows_x rows, of which the
+// longest run of one tile schedule — M, or the longest segment — has
+// long_tokens; extra_tiles bounds the ragged token tiles beyond
+// ceil(rows_x / tile tokens), one per segment in grouped mode).  The pair
+// kernel (cta_group::2, 256 output rows by 256 or 512 tokens per tile,
+// use_wide_tiles) unless built with BD_GEMM_PAIR=0, or when the device cannot
+// place a cluster of two of its CTAs: then the one-CTA kernel.  Returns
+// false, launching nothing, when a tensor map cannot be encoded.
 bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t rows_x,
-               int64_t token_tiles_bound, int num_sms, cudaStream_t s, cudaError_t* err) {
+               int64_t long_tokens, int64_t extra_tiles, int num_sms, cudaStream_t s,
+               cudaError_t* err) {
   CUtensorMap tw, tx;
   if (BD_GEMM_PAIR) {
-    const int bk = bd::gemm_pair_block_k();
+    const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens, extra_tiles);
+    const int bk = wide ? bd::gemm_pair_wide_block_k() : bd::gemm_pair_block_k();
+    const int64_t tok = bd::gemm_pair_tokens(wide);
     if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
         !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_pair_x_rows()))
       return false;
     const int64_t pair_tiles = ((g.d_out + 2 * bd::gemm_block_rows() - 1) /
-                                (2 * bd::gemm_block_rows())) * token_tiles_bound;
-    *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, s);
+                                (2 * bd::gemm_block_rows())) *
+                               ((rows_x + tok - 1) / tok + extra_tiles);
+    *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, wide, s);
     if (*err != cudaErrorInvalidConfiguration) return true;
     (void)cudaGetLastError();  // no cluster fits: fall through to one CTA per tile
   }
@@ -133,8 +165,9 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
   if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
       !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_block_tokens()))
     return false;
-  const int64_t tiles =
-      ((g.d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) * token_tiles_bound;
+  const int64_t tok = bd::gemm_block_tokens();
+  const int64_t tiles = ((g.d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
+                        ((rows_x + tok - 1) / tok + extra_tiles);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   *err = bd::launch_gemm(g, tw, tx, grid, s);
   return true;
@@ -240,7 +273,6 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
   const bd::DevCtx ctx = make_ctx(dev);
 
   if (M > kDecodeMaxRows && tc_shape_ok(M, d_out, d_in) && aligned(packed, 16)) {
-    const int64_t t_total = (M + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens();
     bd::GemmArgs g{};
     g.M = M;
     g.d_out = d_out;
@@ -251,7 +283,7 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
     g.y = y;
     g.ctx = ctx;
     cudaError_t e = cudaSuccess;
-    if (launch_tc(g, w_base, x, M, t_total, dev->num_sms, s, &e)) return from_cuda(e);
+    if (launch_tc(g, w_base, x, M, M, 0, dev->num_sms, s, &e)) return from_cuda(e);
   }
   bd::GemvArgs a{};
   a.x = x;
@@ -310,10 +342,8 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
     g.ctx = ctx;
     // token tiles over all segments <= total tiles of M_total + one ragged
     // tile per segment
-    const int64_t token_tiles =
-        (M_total + bd::gemm_block_tokens() - 1) / bd::gemm_block_tokens() + n_seg;
     cudaError_t e = cudaSuccess;
-    use_tc = launch_tc(g, w_base, x, M_total, token_tiles, dev->num_sms, s, &e);
+    use_tc = launch_tc(g, w_base, x, M_total, max_seg_len, n_seg, dev->num_sms, s, &e);
     if (use_tc && (st = from_cuda(e)) != BD_OK) return st;
   }
   const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
@@ -432,6 +462,13 @@ bd_status bitdelta_monosoup(const uint16_t* w_base, const uint16_t* const* w_ft,
 
 bd_status bitdelta_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns < 1000 ? 1000 : ns);
+  return BD_OK;
+}
+
+bd_status bitdelta_set_prefill_tile(bd_prefill_tile tile) {
+  if (tile != BD_PREFILL_TILE_AUTO && tile != BD_PREFILL_TILE_256 && tile != BD_PREFILL_TILE_512)
+    return BD_ERR_INVALID_ARG;
+  g_prefill_tile.store(static_cast<int>(tile));
   return BD_OK;
 }
 

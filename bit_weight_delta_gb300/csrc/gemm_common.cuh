@@ -320,6 +320,17 @@ __device__ __forceinline__ void umma_bf16_tmem_a_pair(uint32_t d_tmem, uint32_t 
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with A in shared memory: each CTA's 128 rows of A at the same
+// shared-memory offset (descriptor a_desc), read by that CTA's tensor core.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on `bar` (same offset) in both CTAs of the pair when the MMAs this
 // thread issued so far complete.
 __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {

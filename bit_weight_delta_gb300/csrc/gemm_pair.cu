@@ -7,22 +7,33 @@
 // and multiplies in the same pass (conceptual fused_bitdelta_linear:
 // F.linear(x, W_base + α·unpack(bits))).
 //
-// Pair tile: 256 output rows x 256 tokens x 64 K per stage.  CTA rank r of the
-// pair owns output rows n0 + 128r .. +127: it loads those W_base rows, builds
-// their W_eff in its own tensor memory (the MMA's A operand) and holds their
-// fp32 accumulator (128 lanes x 256 token columns).  Each CTA loads half of
-// the x tile (tokens tok0 + 128r .. +127, the MMA's B operand, split in N).
-// Rank 0 issues one 256x256x16 MMA that reads both CTAs' operands.  Against
-// the one-CTA kernel, x moves half the bytes per SM through L2 and shared
-// memory for the same FLOPs, and the ring holds six 32 KB stages.
+// Two tile widths share this file.
+//
+// Narrow pair tile: 256 output rows x 256 tokens x 64 K per stage.  CTA rank
+// r of the pair owns output rows n0 + 128r .. +127: it loads those W_base
+// rows, builds their W_eff in its own tensor memory (the MMA's A operand) and
+// holds their fp32 accumulator (128 lanes x 256 token columns).  Each CTA
+// loads half of the x tile (tokens tok0 + 128r .. +127, the MMA's B operand,
+// split in N).  Rank 0 issues one 256x256x16 MMA that reads both CTAs'
+// operands.  Six 32 KB stages.
+//
+// Wide pair tile: 256 output rows x 512 tokens.  The two accumulators (tokens
+// tok0 .. +255 and tok0 + 256 .. +511) fill the 512 tensor-memory columns, so
+// W_eff is written back over the W_base stage in shared memory, in the same
+// swizzled layout the TMA wrote, and both N = 256 MMAs of a K step read it
+// from there.  Each W_eff value then feeds 512 tokens: half the transform
+// work per FLOP of the narrow tile.  Each CTA loads two 128-token x boxes
+// per stage (tok0 + 128r and tok0 + 256 + 128r); eight 24 KB stages of
+// 32 K (64-byte swizzle).
 //
 // Warp roles per CTA (448 threads, one CTA per SM, persistent over tiles):
 //   warps 0-7   transform: two warpgroups take the stages in turn; thread i
 //               of a warpgroup owns W row i (TMEM lane i), forms 64 W_eff
-//               values per stage and tcgen05.st's them to the stage's A
-//               slot, then its warp arrives on rank 0's xform barrier.
+//               values per stage and stores them to the stage's A slot
+//               (tcgen05.st, narrow) or back to shared memory (wide), then
+//               its warp arrives on rank 0's xform barrier.
 //   warps 8-11  epilogue: tcgen05.ld this CTA's accumulator, store bf16 y.
-//   warp 12     TMA producer for this CTA's W_base rows and half of x.
+//   warp 12     TMA producer for this CTA's W_base rows and its x rows.
 //   warp 13     rank 0: MMA issuer; rank 1: waits for the pair's last MMA.
 // Barriers: full[s] (TMA -> transform, local), xform[s] (both CTAs'
 // transforms -> rank 0's MMA), empty[s] and accfull (rank 0's MMA commits,
@@ -36,33 +47,25 @@ namespace bd {
 namespace {
 using namespace gemm_detail;
 
-constexpr int kBM = 128;            // output rows per CTA
-constexpr int kPairM = 2 * kBM;     // output rows per pair tile (UMMA M)
-constexpr int kBN = 256;            // tokens per pair tile (UMMA N)
-constexpr int kHalfN = kBN / 2;     // tokens loaded by each CTA
 #ifndef BD_PAIR_BK
 #define BD_PAIR_BK 64
 #endif
-// K per stage: one row of a swizzle atom, 128 bytes of bf16 (BK = 64, 128-byte
-// swizzle, 6 stages of 32 KB) or 64 bytes (BK = 32, 64-byte swizzle, 12
-// stages of 16 KB).
-constexpr int kBK = BD_PAIR_BK;
-static_assert(kBK == 32 || kBK == 64, "BK is one 64- or 128-byte swizzle row");
-constexpr int kStages = 384 / kBK;
-constexpr int kABytes = kBM * kBK * 2;     // W_base per stage
-constexpr int kBBytes = kHalfN * kBK * 2;  // x per stage
-constexpr int kChunks = kBK / 8;           // 16-byte chunks per W row per stage
-constexpr int kSwzShift = kBK == 64 ? 0 : 1;  // row bits that select the chunk XOR
-constexpr int kSignBytes = kBK / 8;        // sign bytes per row per stage
-constexpr int kPrefetch = 2;               // sign/α prefetch distance (own stages)
-constexpr int kRing = kPrefetch + 2;       // private ring slots per thread
-constexpr int kDCols = kBN;                // accumulator columns
-constexpr int kACol0 = kDCols;             // first column of the A slots
-constexpr int kAColsPerStage = kBK / 2;    // two bf16 per 32-bit column
-constexpr int kTmemCols = 512;             // D (256) + 6 A slots (192), power of two
 #ifndef BD_PAIR_XF_GROUPS
 #define BD_PAIR_XF_GROUPS 2
 #endif
+// K per stage of the wide tile: 32 (eight 24 KB stages) measured 4-7%
+// faster than 64 (four 48 KB stages) on M = 2048 projections.
+#ifndef BD_PAIR_WIDE_BK
+#define BD_PAIR_WIDE_BK 32
+#endif
+
+constexpr int kBM = 128;         // output rows per CTA
+constexpr int kPairM = 2 * kBM;  // output rows per pair tile (UMMA M)
+constexpr int kMmaN = 256;       // tokens per MMA (UMMA N)
+constexpr int kXBox = kMmaN / 2; // x rows per TMA box (one CTA's half of an MMA's N)
+constexpr int kPrefetch = 2;     // sign/α prefetch distance (own stages)
+constexpr int kRing = kPrefetch + 2;  // private ring slots per thread
+constexpr int kTmemCols = 512;
 constexpr int kXfGroups = BD_PAIR_XF_GROUPS;  // transform warpgroups, stages in turn
 constexpr int kXfWarps = 4 * kXfGroups;
 constexpr int kEpiWarp0 = kXfWarps;
@@ -70,25 +73,46 @@ constexpr int kTmaWarp = kEpiWarp0 + 4;
 constexpr int kMmaWarp = kTmaWarp + 1;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start a warpgroup");
-static_assert(kACol0 + kStages * kAColsPerStage <= kTmemCols, "tensor memory budget");
-static_assert(kXfGroups <= kStages, "a warpgroup's stages must not alias in the ring");
-constexpr uint32_t kIdesc = idesc_bf16_f32(kPairM, kBN);
-constexpr uint32_t kXformArrivals = 2 * 4;   // 4 transform warps per stage, both CTAs
+constexpr uint32_t kIdesc = idesc_bf16_f32(kPairM, kMmaN);
+constexpr uint32_t kXformArrivals = 2 * 4;     // 4 transform warps per stage, both CTAs
 constexpr uint32_t kAccEmptyArrivals = 2 * 4;  // 4 epilogue warps, both CTAs
 
-// Shared memory layout (offsets from a 1024-byte aligned base; identical in
-// both CTAs, so one offset names the same buffer in either).
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128] x 8 B
-constexpr int kOffAlpha = kOffSign + kXfGroups * kRing * kBM * 8;  // [G][kRing][128] floats
-constexpr int kOffBar = kOffAlpha + kXfGroups * kRing * kBM * 4;
-constexpr int kNumBars = 3 * kStages + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, counts
-constexpr int kOffSeg = kOffMisc + 64;            // grouped-mode tables
-constexpr int kSegBytes = (3 * kGemmMaxSegs + 2) * 4;
-constexpr int kSmemBytes = kOffSeg + kSegBytes + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+template <bool kWide>
+struct Cfg {
+  static constexpr int kNMma = kWide ? 2 : 1;  // N = 256 MMAs per K step
+  static constexpr int kBN = kNMma * kMmaN;    // tokens per pair tile
+  // K per stage: one row of a swizzle atom, 128 bytes of bf16 (BK = 64,
+  // 128-byte swizzle) or 64 bytes (BK = 32, 64-byte swizzle).
+  static constexpr int kBK = kWide ? BD_PAIR_WIDE_BK : BD_PAIR_BK;
+  static constexpr int kStages = kWide ? 256 / kBK : 384 / kBK;
+  static constexpr int kABytes = kBM * kBK * 2;             // W_base (W_eff) per stage
+  static constexpr int kXBoxBytes = kXBox * kBK * 2;        // one x box
+  static constexpr int kBBytes = kNMma * kXBoxBytes;        // x per stage
+  static constexpr int kChunks = kBK / 8;                   // 16-byte chunks per W row
+  static constexpr int kSwzShift = kBK == 64 ? 0 : 1;       // row bits that select the XOR
+  static constexpr int kSignBytes = kBK / 8;                // sign bytes per row per stage
+  static constexpr int kACol0 = kBN;                        // narrow: first A slot column
+  static constexpr int kAColsPerStage = kBK / 2;            // narrow: two bf16 per column
+  // Shared memory layout (offsets from a 1024-byte aligned base; identical
+  // in both CTAs, so one offset names the same buffer in either).
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSign = kOffB + kStages * kBBytes;                // [G][kRing][128] x 8 B
+  static constexpr int kOffAlpha = kOffSign + kXfGroups * kRing * kBM * 8;  // [G][kRing][128] f32
+  static constexpr int kOffBar = kOffAlpha + kXfGroups * kRing * kBM * 4;
+  static constexpr int kNumBars = 3 * kStages + 3;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, counts
+  static constexpr int kOffSeg = kOffMisc + 64;            // grouped-mode tables
+  static constexpr int kSegBytes = (3 * kGemmMaxSegs + 2) * 4;
+  static constexpr int kSmemBytes = kOffSeg + kSegBytes + 1024;  // + alignment slack
+  static_assert(kBK == 32 || kBK == 64, "BK is one 64- or 128-byte swizzle row");
+  static_assert(kXfGroups <= kStages, "a warpgroup's stages must not alias in the ring");
+  static_assert(kWide ? kNMma * kMmaN <= kTmemCols
+                      : kACol0 + kStages * kAColsPerStage <= kTmemCols,
+                "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kABytes % 1024 == 0 && kXBoxBytes % 1024 == 0, "swizzle atoms stay aligned");
+};
 
 struct Misc {
   uint32_t tmem_base;
@@ -96,21 +120,26 @@ struct Misc {
   int64_t t_total;  // token tiles over all segments
 };
 
+template <bool kWide>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bitdelta_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                               const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
+  using C = Cfg<kWide>;
+  constexpr int kStages = C::kStages;
+  constexpr int kBK = C::kBK;
+  constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full_bar = bars;                 // own TMA -> own transform
   uint64_t* xform_bar = bars + kStages;      // both transforms -> rank 0's MMA (rank 0 only)
   uint64_t* empty_bar = bars + 2 * kStages;  // rank 0's MMA -> both TMA producers
   uint64_t* accfull_bar = bars + 3 * kStages;
   uint64_t* accempty_bar = accfull_bar + 1;  // both epilogues -> rank 0's MMA (rank 0 only)
   uint64_t* drain_bar = accempty_bar + 1;
-  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
-  int32_t* s_seg_off = reinterpret_cast<int32_t*>(smem + kOffSeg);
+  Misc* misc = reinterpret_cast<Misc*>(smem + C::kOffMisc);
+  int32_t* s_seg_off = reinterpret_cast<int32_t*>(smem + C::kOffSeg);
   int32_t* s_seg_var = s_seg_off + (kGemmMaxSegs + 1);
   int32_t* s_prefix = s_seg_var + kGemmMaxSegs;
   volatile int* abort = &misc->abort;
@@ -166,15 +195,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 s_prefix);
   };
   const int64_t row0 = static_cast<int64_t>(rank) * kBM;     // this CTA's rows in the tile
-  const int64_t tok_half = static_cast<int64_t>(rank) * kHalfN;  // this CTA's x rows
+  const int64_t tok_half = static_cast<int64_t>(rank) * kXBox;  // this CTA's x rows per MMA
 
   if (warp < kXfWarps) {
     // ============================================================ transform
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;  // the W row (and TMEM lane) of this thread
     const int quarter = warp & 3;     // TMEM lane quarter of this warp
-    uint8_t* sign_ring = smem + kOffSign + wg * (kRing * kBM * 8);
-    float* alpha_ring = reinterpret_cast<float*>(smem + kOffAlpha) + wg * (kRing * kBM);
+    uint8_t* sign_ring = smem + C::kOffSign + wg * (kRing * kBM * 8);
+    float* alpha_ring = reinterpret_cast<float*>(smem + C::kOffAlpha) + wg * (kRing * kBM);
     const int64_t row_bytes = p.d_in / 8;
 
     const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
@@ -203,7 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int64_t row = t.n0 + row0 + r;
       row = row < p.d_out ? row : p.d_out - 1;
       pf_alpha = p.per_row ? al + row : al;
-      if ((reinterpret_cast<uintptr_t>(pk) & (kSignBytes - 1)) == 0) {
+      if ((reinterpret_cast<uintptr_t>(pk) & (C::kSignBytes - 1)) == 0) {
         pf_src = pk + row * row_bytes;
         pf_mode = 1;
       } else {
@@ -219,10 +248,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto prefetch_next = [&]() {
       uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
       if (pf_mode == 1) {
-        if constexpr (kSignBytes == 8)
-          cp_async_8(dst, pf_src + pf_kb * kSignBytes);
+        if constexpr (C::kSignBytes == 8)
+          cp_async_8(dst, pf_src + pf_kb * C::kSignBytes);
         else
-          cp_async_4(dst, pf_src + pf_kb * kSignBytes);
+          cp_async_4(dst, pf_src + pf_kb * C::kSignBytes);
       } else if (pf_mode == 2) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
       }
@@ -268,38 +297,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool has_delta = tl.variant > 0;
       uint2 sg = make_uint2(0u, 0u);
       if (has_delta) {
-        if constexpr (kSignBytes == 8)
+        if constexpr (C::kSignBytes == 8)
           sg = *reinterpret_cast<const uint2*>(sign_ring + (slot * kBM + r) * 8);
         else
           sg.x = *reinterpret_cast<const uint32_t*>(sign_ring + (slot * kBM + r) * 8);
       }
-      const uint8_t* w_row = smem + kOffA + s * kABytes + r * (kBK * 2);
-      const int swz = (r >> kSwzShift) & (kChunks - 1);
-      uint4 wv[kChunks];
+      uint8_t* w_row = smem + C::kOffA + s * C::kABytes + r * (kBK * 2);
+      const int swz = (r >> C::kSwzShift) & (C::kChunks - 1);
+      if constexpr (kWide) {
+        // W_eff over W_base in place (same swizzled chunk positions); base
+        // rows are already the operand.  The fence makes these generic-proxy
+        // writes visible to the tensor core's reads of the stage.
+        if (has_delta) {
+          uint4 wv[C::kChunks];
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        // logical 16-byte chunk c sits at physical chunk c ^ swz: the TMA's
-        // 128-byte (64-byte) swizzle XORs the chunk index with address bits
-        // 7-9 (7-8), i.e. with row bits 0-2 (1-2)
-        wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
-      }
-      uint32_t packed[kBK / 2];
-      if (has_delta) {
-        weff_chunks<kChunks>(wv, sg, alpha_bits, packed);
-      } else {
+          for (int c = 0; c < C::kChunks; ++c)
+            wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
+          uint32_t packed[kBK / 2];
+          weff_chunks<C::kChunks>(wv, sg, alpha_bits, packed);
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          packed[4 * c + 0] = wv[c].x;
-          packed[4 * c + 1] = wv[c].y;
-          packed[4 * c + 2] = wv[c].z;
-          packed[4 * c + 3] = wv[c].w;
+          for (int c = 0; c < C::kChunks; ++c)
+            *reinterpret_cast<uint4*>(w_row + ((c ^ swz) << 4)) =
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          fence_proxy_async_smem();
         }
+        __syncwarp();
+      } else {
+        uint4 wv[C::kChunks];
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          // logical 16-byte chunk c sits at physical chunk c ^ swz: the TMA's
+          // 128-byte (64-byte) swizzle XORs the chunk index with address bits
+          // 7-9 (7-8), i.e. with row bits 0-2 (1-2)
+          wv[c] = *reinterpret_cast<const uint4*>(w_row + ((c ^ swz) << 4));
+        }
+        uint32_t packed[kBK / 2];
+        if (has_delta) {
+          weff_chunks<C::kChunks>(wv, sg, alpha_bits, packed);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c) {
+            packed[4 * c + 0] = wv[c].x;
+            packed[4 * c + 1] = wv[c].y;
+            packed[4 * c + 2] = wv[c].z;
+            packed[4 * c + 3] = wv[c].w;
+          }
+        }
+        tmem_st_32x32b(a_lane + static_cast<uint32_t>(C::kACol0 + C::kAColsPerStage * s), packed);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
       }
-      tmem_st_32x32b(a_lane + static_cast<uint32_t>(kACol0 + kAColsPerStage * s), packed);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      // the A slot is written and this CTA's x half of the stage has landed
+      // the A operand is written and this CTA's x of the stage has landed
       if (lane == 0) mbar_arrive_cluster(xform_rank0 + static_cast<uint32_t>(8 * s));
       s += kXfGroups;
       if (s >= kStages) {
@@ -352,11 +401,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[s], kABytes + kBBytes);
-          tma_load_2d(smem + kOffA + s * kABytes, &tmap_w, &full_bar[s], kb * kBK,
+          mbar_arrive_expect_tx(&full_bar[s], C::kABytes + C::kBBytes);
+          tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, &full_bar[s], kb * kBK,
                       static_cast<int32_t>(tl.n0 + row0), pol_w);
-          tma_load_2d(smem + kOffB + s * kBBytes, &tmap_x, &full_bar[s], kb * kBK,
-                      static_cast<int32_t>(tl.tok0 + tok_half), pol_x);
+#pragma unroll
+          for (int j = 0; j < C::kNMma; ++j)
+            tma_load_2d(smem + C::kOffB + s * C::kBBytes + j * C::kXBoxBytes, &tmap_x,
+                        &full_bar[s], kb * kBK,
+                        static_cast<int32_t>(tl.tok0 + j * kMmaN + tok_half), pol_x);
         }
       }
       // Drain: wait (bounded, ignoring abort) until every issued copy landed.
@@ -368,11 +420,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
     if (lane == 0 && rank == 0) {
-      const uint32_t b_base = smem_addr(smem + kOffB);
+      const uint32_t a_base = smem_addr(smem + C::kOffA);
+      const uint32_t b_base = smem_addr(smem + C::kOffB);
       int64_t q = 0;
       bool ok = true;
       bool issued = false;
       for (int64_t i = 0; i < my_tiles && ok; ++i) {
+        // N = 256 MMAs with at least one output token (the wide tile's second
+        // half is skipped when the tile ends in its first half)
+        int n_mma = 1;
+        if constexpr (kWide) {
+          const Tile tl = my_tile(i);
+          n_mma = tl.tok0 + kMmaN < tl.tok_end ? 2 : 1;
+        }
         // both CTAs' accumulators must have been drained by their epilogues
         if (!mbar_wait_cluster(accempty_bar, static_cast<uint32_t>((i & 1) ^ 1), p.ctx, abort))
           break;
@@ -385,14 +445,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kACol0 + kAColsPerStage * s);
-          const uint64_t b_desc = kBK == 64 ? sdesc_k_sw128(b_base + s * kBBytes)
-                                            : sdesc_k_sw64(b_base + s * kBBytes);
+          const uint64_t b_desc = kBK == 64 ? sdesc_k_sw128(b_base + s * C::kBBytes)
+                                            : sdesc_k_sw64(b_base + s * C::kBBytes);
+          if constexpr (kWide) {
+            const uint64_t a_desc = kBK == 64 ? sdesc_k_sw128(a_base + s * C::kABytes)
+                                              : sdesc_k_sw64(a_base + s * C::kABytes);
+            constexpr uint64_t kBoxStep = C::kXBoxBytes >> 4;  // descriptor address units
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
-            umma_bf16_tmem_a_pair(tmem_base, a_tmem + 8 * k, b_desc + 2 * k, kIdesc,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k) {
+              // K step 16: +32 bytes inside both operands' swizzle atoms
+              const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+              umma_bf16_pair(tmem_base, a_desc + 2 * k, b_desc + 2 * k, kIdesc, acc);
+              if (n_mma > 1)
+                umma_bf16_pair(tmem_base + kMmaN, a_desc + 2 * k, b_desc + kBoxStep + 2 * k,
+                               kIdesc, acc);
+            }
+          } else {
+            const uint32_t a_tmem =
+                tmem_base + static_cast<uint32_t>(C::kACol0 + C::kAColsPerStage * s);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
+              umma_bf16_tmem_a_pair(tmem_base, a_tmem + 8 * k, b_desc + 2 * k, kIdesc,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+            }
           }
           issued = true;
           umma_commit_pair(&empty_bar[s]);
@@ -417,39 +493,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-}  // namespace
-
-int gemm_pair_x_rows() { return kHalfN; }
-int gemm_pair_block_k() { return kBK; }
-
-cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
-                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
-                             cudaStream_t stream) {
-  static bool attr_done[64] = {};
+// Per device: kernel attributes set and the number of pairs that fit at once
+// (occupancy query), once per instantiation.
+template <bool kWide>
+cudaError_t pair_capacity(int* pairs) {
+  static bool done[64] = {};
   static int max_pairs[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel<kWide>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kWide>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<kWide>::kSmemBytes;
+    cfg.gridDim = dim3(2);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, bitdelta_gemm_pair_kernel<kWide>, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[dev] = n;
+    done[dev] = true;
+  }
+  *pairs = max_pairs[dev];
+  return cudaSuccess;
+}
+
+template <bool kWide>
+cudaError_t launch_pair_instance(const GemmArgs& p, const CUtensorMap& tmap_w,
+                                 const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
+                                 cudaStream_t stream) {
+  int max_pairs = 0;
+  cudaError_t e = pair_capacity<kWide>(&max_pairs);
+  if (e != cudaSuccess) return e;
+  if (max_pairs < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<kWide>::kSmemBytes;
   cfg.stream = stream;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    cfg.gridDim = dim3(2);
-    e = cudaOccupancyMaxActiveClusters(&n, bitdelta_gemm_pair_kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_pairs[dev] = n;
-    attr_done[dev] = true;
-  }
-  const int64_t pairs = pair_tiles_bound < max_pairs[dev] ? pair_tiles_bound : max_pairs[dev];
+  const int64_t pairs = pair_tiles_bound < max_pairs ? pair_tiles_bound : max_pairs;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (pairs > 0 ? pairs : 1)));
-  return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel, tmap_w, tmap_x, p);
+  return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel<kWide>, tmap_w, tmap_x, p);
+}
+
+}  // namespace
+
+int gemm_pair_x_rows() { return kXBox; }
+int gemm_pair_block_k() { return Cfg<false>::kBK; }
+int gemm_pair_wide_block_k() { return Cfg<true>::kBK; }
+int gemm_pair_tokens(bool wide) { return wide ? Cfg<true>::kBN : Cfg<false>::kBN; }
+int gemm_pair_capacity(bool wide) {
+  int n = 0;
+  const cudaError_t e = wide ? pair_capacity<true>(&n) : pair_capacity<false>(&n);
+  return e == cudaSuccess ? n : -static_cast<int>(e);
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
+                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound, bool wide,
+                             cudaStream_t stream) {
+  return wide ? launch_pair_instance<true>(p, tmap_w, tmap_x, pair_tiles_bound, stream)
+              : launch_pair_instance<false>(p, tmap_w, tmap_x, pair_tiles_bound, stream);
 }
 
 }  // namespace bd

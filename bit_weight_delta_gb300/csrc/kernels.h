@@ -97,13 +97,20 @@ cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUte
                         int grid, cudaStream_t stream);
 
 // Prefill-size linear on CTA pairs (tcgen05 cta_group::2): tiles of
-// 2 * gemm_block_rows() output rows x gemm_block_tokens() tokens; tmap_w's box
-// has gemm_block_rows() rows, tmap_x's box gemm_pair_x_rows() (half a tile),
-// both gemm_pair_block_k() columns.  pair_tiles_bound caps the pairs launched.
+// 2 * gemm_block_rows() output rows x gemm_pair_tokens(wide) tokens (256, or
+// 512 for the wide tile); tmap_w's box has gemm_block_rows() rows, tmap_x's
+// box gemm_pair_x_rows() (half of one MMA's 256 tokens), both
+// gemm_pair_block_k() (narrow) or gemm_pair_wide_block_k() (wide) columns.
+// pair_tiles_bound caps the pairs launched.
 int gemm_pair_x_rows();
 int gemm_pair_block_k();
+int gemm_pair_wide_block_k();
+int gemm_pair_tokens(bool wide);
+// CTA pairs of that kernel the current device holds at once (0 if none fits;
+// negative cudaError_t on a failed query).
+int gemm_pair_capacity(bool wide);
 cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
-                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound,
+                             const CUtensorMap& tmap_x, int64_t pair_tiles_bound, bool wide,
                              cudaStream_t stream);
 
 // Cosine similarity of 1-bit task vectors (K-Merge); grid and workspace:

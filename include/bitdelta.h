@@ -104,7 +104,9 @@ bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, co
  * (fp32 accumulation, one RNE rounding at the end), no bias.
  * Dispatch: M <= 16 takes the bandwidth-bound decode kernel; larger M the
  * tcgen05 tensor-core kernel when d_in % 128 == 0 and every pointer allows
- * TMA, else the decode kernel over 16-row chunks.
+ * TMA, else the decode kernel over 16-row chunks.  The tensor-core kernel
+ * runs on CTA pairs with tiles of 256 output rows by 256 or 512 tokens
+ * (bitdelta_set_prefill_tile).
  * y must not overlap the inputs.
  */
 bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
@@ -225,6 +227,26 @@ bd_status bitdelta_check_error(bd_stream_t stream);
  * (default 2e9).  Values below 1000 are raised to 1000.  Host-side setting
  * read at each launch. */
 bd_status bitdelta_set_wait_limit_ns(uint64_t ns);
+
+/* Token width of the tensor-core kernel's CTA-pair tiles (bitdelta_linear
+ * with M > 16 and the long segments of bitdelta_linear_grouped).  A 512-token
+ * tile builds each W_eff tile once for twice the tokens of a 256-token tile
+ * (half the transform work per FLOP) but makes half as many tiles.
+ *   BD_PREFILL_TILE_AUTO  (default) per call, the width whose predicted time
+ *                         is lower: rounds of tiles over the GPU's CTA pairs
+ *                         (ceil(tiles / pairs)) times the measured cost of
+ *                         one tile, a 512-token tile costing 1.75 256-token
+ *                         tiles; grouped calls use M_total and n_seg for the
+ *                         tile counts and take 256 when max_seg_len <= 256.
+ *   BD_PREFILL_TILE_256, BD_PREFILL_TILE_512  always that width.
+ * Process-wide host setting read at each launch; BD_ERR_INVALID_ARG for any
+ * other value. */
+typedef enum {
+  BD_PREFILL_TILE_AUTO = 0,
+  BD_PREFILL_TILE_256 = 1,
+  BD_PREFILL_TILE_512 = 2
+} bd_prefill_tile;
+bd_status bitdelta_set_prefill_tile(bd_prefill_tile tile);
 
 /* Test hook: launches one CTA that waits on an mbarrier nothing will complete,
  * with the current wait limit.  The wait gives up, records

@@ -177,3 +177,16 @@ def test_sign_similarity_rejects_bad_arguments(lib):
     assert call(ws=BAD) == MISALIGNED
     assert call(ws_bytes=ws_need - 1) == WORKSPACE
     assert lib.bitdelta_sign_similarity_workspace_bytes(64, 0) == 0
+
+
+def test_prefill_tile_setting(lib):
+    """The pair-tile width setting is host state: the three named values are
+    accepted, anything else rejected; the binding maps 'auto', 256, 512."""
+    for v in (1, 2, 0):
+        assert lib.bitdelta_set_prefill_tile(v) == OK
+    for v in (3, -1, 512):
+        assert lib.bitdelta_set_prefill_tile(v) == INVALID
+    with pytest.raises(ValueError):
+        bd.bitdelta_set_prefill_tile(128)
+    bd.bitdelta_set_prefill_tile(512)
+    bd.bitdelta_set_prefill_tile("auto")
