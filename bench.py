@@ -975,12 +975,13 @@ def run_reference(args, rank, world):
     return 0
 
 
-def run_profile(kind: str):
+def run_profile(kind: str, prefill_tile: str = "auto"):
     """A few eager launches of one kernel on a small case, for ncu captures."""
     import bit_weight_delta_gb300 as bd
     import synth.device as sd
     bd.load()
     torch.cuda.set_device(0)
+    bd.bitdelta_set_prefill_tile(prefill_tile if prefill_tile == "auto" else int(prefill_tile))
     if kind in ("decode", "compress", "reconstruct"):
         layers = []
         for l in range(4):
@@ -1043,9 +1044,11 @@ def main():
     ap.add_argument("--profile", default=None,
                     help="decode|compress|reconstruct|prefill|grouped|kmerge|monosoup: "
                          "a few eager launches for ncu")
+    ap.add_argument("--prefill-tile", default="auto", choices=["auto", "256", "512"],
+                    help="token width of the tensor-core kernel's pair tiles (profile runs)")
     args = ap.parse_args()
     if args.profile:
-        return run_profile(args.profile)
+        return run_profile(args.profile, args.prefill_tile)
 
     dist, rank, world, local = init_dist(args)
     if args.impl == "reference":
