@@ -115,11 +115,15 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
 constexpr int64_t kWideTileCost4 = 7;
 
 // 512-token pair tiles for this call?  Under BD_PREFILL_TILE_AUTO the width
-// whose rounds of tiles over the device's pairs cost less: ceil(tiles /
-// pairs) x the cost of one tile.  Token tiles per row tile: ceil(rows_x /
-// width) + extra_tiles (one ragged tile per segment in grouped mode);
-// long_tokens <= 256 (no segment fills half a wide tile) keeps 256.
-bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens, int64_t extra_tiles) {
+// whose rounds of tiles over the device's pairs cost less, ceil(tiles /
+// pairs) x the cost of one tile, with ceil(rows_x / width) token tiles per
+// row tile (exact for one run of M rows; for a grouped batch, whose long
+// segments the host cannot see, the same estimate over M_total); on a tie
+// the 512-token tile (half the transform work).  long_tokens <= 256 (no
+// segment fills half a wide tile) keeps 256.  Measured on the grouped
+// workload (64 one-row and four 512-row segments over 4096 -> 14336): 0.462
+// ms with 512-token tiles, 0.499 with 256.
+bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens) {
   const int policy = g_prefill_tile.load();
   if (policy == BD_PREFILL_TILE_256) return false;
   if (policy == BD_PREFILL_TILE_512) return true;
@@ -129,10 +133,10 @@ bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens, int64_t 
   const int64_t row_tiles = (d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows());
   auto rounds = [&](bool wide) {
     const int64_t tok = bd::gemm_pair_tokens(wide);
-    const int64_t tiles = row_tiles * ((rows_x + tok - 1) / tok + extra_tiles);
+    const int64_t tiles = row_tiles * ((rows_x + tok - 1) / tok);
     return (tiles + pairs - 1) / pairs;
   };
-  return rounds(true) * kWideTileCost4 < rounds(false) * 4;
+  return rounds(true) * kWideTileCost4 <= rounds(false) * 4;
 }
 
 // Launch the tensor-core kernel on g (x has rows_x rows, of which the
@@ -148,7 +152,7 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
                cudaError_t* err) {
   CUtensorMap tw, tx;
   if (BD_GEMM_PAIR) {
-    const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens, extra_tiles);
+    const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens);
     const int bk = wide ? bd::gemm_pair_wide_block_k() : bd::gemm_pair_block_k();
     const int64_t tok = bd::gemm_pair_tokens(wide);
     if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||

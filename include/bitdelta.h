@@ -233,11 +233,11 @@ bd_status bitdelta_set_wait_limit_ns(uint64_t ns);
  * tile builds each W_eff tile once for twice the tokens of a 256-token tile
  * (half the transform work per FLOP) but makes half as many tiles.
  *   BD_PREFILL_TILE_AUTO  (default) per call, the width whose predicted time
- *                         is lower: rounds of tiles over the GPU's CTA pairs
- *                         (ceil(tiles / pairs)) times the measured cost of
- *                         one tile, a 512-token tile costing 1.75 256-token
- *                         tiles; grouped calls use M_total and n_seg for the
- *                         tile counts and take 256 when max_seg_len <= 256.
+ *                         is lower (512 on a tie): rounds of tiles over the
+ *                         GPU's CTA pairs (ceil(tiles / pairs)) times the
+ *                         measured cost of one tile, a 512-token tile costing
+ *                         1.75 256-token tiles; grouped calls count tiles
+ *                         over M_total and take 256 when max_seg_len <= 256.
  *   BD_PREFILL_TILE_256, BD_PREFILL_TILE_512  always that width.
  * Process-wide host setting read at each launch; BD_ERR_INVALID_ARG for any
  * other value. */
