@@ -113,8 +113,10 @@ cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
                              const CUtensorMap& tmap_x, int64_t pair_tiles_bound, bool wide,
                              cudaStream_t stream);
 
-// Cosine similarity of 1-bit task vectors (K-Merge); grid and workspace:
-// 256 bytes (a counter) + grid · (2·n_b + 1) doubles.
+// Cosine similarity of 1-bit task vectors (K-Merge).  sign_similarity_grid
+// bounds the CTAs of a launch (the launch takes at most one wave of the
+// device); workspace: 256 bytes (a counter) + that bound · (2·n_b + 1)
+// doubles.
 int sign_similarity_grid(int64_t d_out);
 cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
                                    const uint8_t* const* pb_table, const float* const* ab_table,

@@ -14,7 +14,10 @@
 // HBM-bound: the candidate's signs are read once, each member's once
 // ((1 + n_b)/16 bytes per weight).  A warp takes one row of the candidate at
 // a time into registers (16 bytes per lane per 4096 columns) and streams the
-// pool members' same row, eight members per round of loads.  Per-CTA partial
+// pool members' same row, sixteen members per round of loads.  The lanes'
+// disagreement counts are summed by a transposing butterfly that leaves
+// member j's row total in lanes 2j and 2j+1 (16 shuffles for 16 members),
+// and the even lanes do the fp64 α arithmetic side by side.  Per-CTA partial
 // sums go to the caller's workspace; the last CTA to finish reduces them in a
 // fixed order (deterministic) and writes the cosines and the argmax.
 #include <cstdint>
@@ -27,7 +30,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRound = 8;  // pool members whose row loads are in flight together
+constexpr int kRound = 16;  // pool members whose row loads are in flight together
+constexpr int kMaxGrid = 512;  // CTAs (partials per lane in the final sum: kMaxGrid / 32)
 
 struct SimArgs {
   const uint8_t* pa;
@@ -48,10 +52,26 @@ __device__ __forceinline__ int popc4(uint4 a, uint4 b) {
   return __popc(a.x ^ b.x) + __popc(a.y ^ b.y) + __popc(a.z ^ b.z) + __popc(a.w ^ b.w);
 }
 
-__device__ __forceinline__ int warp_sum(int v) {
+// c[j]: this lane's count for member j of the round.  Each level halves the
+// members a lane keeps (lanes with the level's bit set keep the upper half)
+// and adds the partner's half it does not keep; after xor 16, 8, 4, 2 lane L
+// holds its pair's share of member L >> 1, and xor 1 completes the total.
+__device__ __forceinline__ int transpose_sum16(int (&c)[kRound], int lane) {
+  static_assert(kRound == 16, "four halving levels");
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
+  for (int lvl = 0; lvl < 4; ++lvl) {
+    const int x = 16 >> lvl, half = 8 >> lvl;
+    const bool up = (lane & x) != 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < half) {
+        const int send = up ? c[k] : c[k + half];
+        const int keep = up ? c[k + half] : c[k];
+        c[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, x);
+      }
+    }
+  }
+  return c[0] + __shfl_xor_sync(0xFFFFFFFFu, c[0], 1);
 }
 
 __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
@@ -80,44 +100,41 @@ __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
     for (int b0 = 0; b0 < n_b; b0 += kRound) {
       int cnt[kRound];
 #pragma unroll
-      for (int j = 0; j < kRound; ++j) cnt[j] = 0;
-      // lane j fetches member b0 + j's α for this row while the signs stream
-      const bool mine_j = lane < kRound && b0 + lane < n_b;
-      const float ab_j = mine_j ? (p.per_row ? __ldg(s_ab[b0 + lane] + r) : __ldg(s_ab[b0 + lane]))
+      for (int q = 0; q < kRound; ++q) cnt[q] = 0;
+      // lane pair (2j, 2j+1) ends with member b0 + j; the even lane fetches
+      // its α for this row while the signs stream
+      const int jm = lane >> 1;
+      const bool mine_j = (lane & 1) == 0 && b0 + jm < n_b;
+      const float ab_j = mine_j ? (p.per_row ? __ldg(s_ab[b0 + jm] + r) : __ldg(s_ab[b0 + jm]))
                                 : 0.f;
       bool v4 = p.vec != 0;  // 16-byte loads when every member row is 16-byte aligned
 #pragma unroll
-      for (int j = 0; j < kRound; ++j)
-        if (b0 + j < n_b) v4 = v4 && (reinterpret_cast<uintptr_t>(s_pb[b0 + j]) & 15u) == 0;
+      for (int q = 0; q < kRound; ++q)
+        if (b0 + q < n_b) v4 = v4 && (reinterpret_cast<uintptr_t>(s_pb[b0 + q]) & 15u) == 0;
       if (v4) {
         for (int64_t off = 16 * lane; off < row_bytes; off += 512) {
           const uint4 va = ldg_stream_v4(ra + off);
           uint4 vb[kRound];
 #pragma unroll
-          for (int j = 0; j < kRound; ++j)
-            vb[j] = b0 + j < n_b ? ldg_stream_v4(s_pb[b0 + j] + r * row_bytes + off) : va;
+          for (int q = 0; q < kRound; ++q)
+            vb[q] = b0 + q < n_b ? ldg_stream_v4(s_pb[b0 + q] + r * row_bytes + off) : va;
 #pragma unroll
-          for (int j = 0; j < kRound; ++j) cnt[j] += popc4(va, vb[j]);
+          for (int q = 0; q < kRound; ++q) cnt[q] += popc4(va, vb[q]);
         }
       } else {
         for (int64_t off = lane; off < row_bytes; off += 32) {
           const uint32_t a = __ldg(ra + off);
 #pragma unroll
-          for (int j = 0; j < kRound; ++j)
-            if (b0 + j < n_b) cnt[j] += __popc(a ^ __ldg(s_pb[b0 + j] + r * row_bytes + off));
+          for (int q = 0; q < kRound; ++q)
+            if (b0 + q < n_b) cnt[q] += __popc(a ^ __ldg(s_pb[b0 + q] + r * row_bytes + off));
         }
       }
-      // every lane ends with every member's total; lane j keeps member b0 + j
-      int d_mine = 0;
-#pragma unroll
-      for (int j = 0; j < kRound; ++j) {
-        const int d = warp_sum(cnt[j]);  // disagreeing signs of row r with member b0 + j
-        if (lane == j) d_mine = d;
-      }
+      // disagreeing signs of row r with member b0 + jm
+      const int d_mine = transpose_sum16(cnt, lane);
       if (mine_j) {
         const double alpha_b = static_cast<double>(ab_j);
-        mine[b0 + lane] += alpha_a * alpha_b * (d_in - 2.0 * d_mine);
-        mine[n_b + b0 + lane] += alpha_b * alpha_b * d_in;
+        mine[b0 + jm] += alpha_a * alpha_b * (d_in - 2.0 * d_mine);
+        mine[n_b + b0 + jm] += alpha_b * alpha_b * d_in;
       }
     }
     if (lane == 0) mine[2 * n_b] += alpha_a * alpha_a * d_in;
@@ -137,30 +154,40 @@ __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
   if (!last) return;
   __threadfence();
   // The last CTA: totals over CTAs, then cosines and argmax.  Warp w takes
-  // the values i ≡ w (mod kWarps); lane l sums CTAs c ≡ l (mod 32) with
-  // independent loads, then a butterfly over the lanes: a fixed order for a
-  // given grid, so the result is deterministic.
+  // the values i ≡ w (mod kWarps); lane l loads the partials of CTAs
+  // c ≡ l (mod 32) all at once, sums them in c order, then a butterfly over
+  // the lanes: a fixed order for a given grid, so the result is
+  // deterministic.
   double* tot = sm;  // reuse: [stride_w]
+  const unsigned int n_cta = gridDim.x;
   for (int i = warp; i < stride_w; i += kWarps) {
+    double v[kMaxGrid / 32];
+#pragma unroll
+    for (int q = 0; q < kMaxGrid / 32; ++q) {
+      const unsigned int c = lane + 32u * q;
+      v[q] = c < n_cta ? p.partial[static_cast<int64_t>(c) * stride_w + i] : 0.0;
+    }
     double s = 0.0;
-#pragma unroll 4
-    for (unsigned int c = lane; c < gridDim.x; c += 32)
-      s += p.partial[static_cast<int64_t>(c) * stride_w + i];
+#pragma unroll
+    for (int q = 0; q < kMaxGrid / 32; ++q) s += v[q];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
     if (lane == 0) tot[i] = s;
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < n_b; b += kThreads)
-    p.cos_out[b] = tot[b] / sqrt(tot[2 * n_b] * tot[n_b + b]);
+  double* cosv = tot + stride_w;  // [n_b]
+  for (int b = threadIdx.x; b < n_b; b += kThreads) {
+    const double c = tot[b] / sqrt(tot[2 * n_b] * tot[n_b + b]);
+    cosv[b] = c;
+    p.cos_out[b] = c;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     int best = 0;
     double bv = -2.0;
     for (int b = 0; b < n_b; ++b) {
-      const double c = p.cos_out[b];
-      if (c > bv) {  // ties keep the lower index
-        bv = c;
+      if (cosv[b] > bv) {  // ties keep the lower index
+        bv = cosv[b];
         best = b;
       }
     }
@@ -173,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
 
 int sign_similarity_grid(int64_t d_out) {
   const int64_t want = (d_out + kWarps - 1) / kWarps;
-  return static_cast<int>(want < 512 ? want : 512);
+  return static_cast<int>(want < kMaxGrid ? want : kMaxGrid);
 }
 
 cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
@@ -195,8 +222,21 @@ cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
   a.counter = static_cast<unsigned int*>(workspace);
   a.partial = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + 256);
   a.vec = vec ? 1 : 0;
-  const int grid = sign_similarity_grid(d_out);
   const size_t smem = static_cast<size_t>(kWarps) * (2 * n_b + 1) * sizeof(double);
+  // One wave: at most the CTAs the device holds at once (a second, partial
+  // wave of 56 CTAs made a third of the SMs idle for half of a 4096 x 14336
+  // call), and rows spread evenly over the warps by the kernel's stride.
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sign_similarity_kernel, kThreads,
+                                                    smem);
+  if (e != cudaSuccess) return e;
+  int grid = sign_similarity_grid(d_out);
+  const int wave = sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > wave) grid = wave;
   return launch_pdl(sign_similarity_kernel, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
