@@ -394,8 +394,7 @@ bd_status bitdelta_check_error(bd_stream_t stream) {
 
 size_t bitdelta_sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b) {
   if (d_out <= 0 || n_b < 1 || n_b > 256) return 0;
-  return 256 + static_cast<size_t>(bd::sign_similarity_grid(d_out)) *
-                   (2 * static_cast<size_t>(n_b) + 1) * sizeof(double);
+  return bd::sign_similarity_workspace_bytes(d_out, n_b);
 }
 
 bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a,
@@ -417,7 +416,7 @@ bd_status bitdelta_sign_similarity(const uint8_t* packed_a, const float* alpha_a
   DeviceState* dev = nullptr;
   if ((st = current_device(&dev)) != BD_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s) != cudaSuccess) return BD_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return BD_ERR_CUDA;  // counters
   const bool vec = d_in % 128 == 0 && aligned(packed_a, 16);
   return from_cuda(bd::launch_sign_similarity(packed_a, alpha_a, packed_table, alpha_table, n_b,
                                               mode == BD_ALPHA_PER_ROW, d_out, d_in, cos_out,

@@ -115,9 +115,11 @@ cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
 
 // Cosine similarity of 1-bit task vectors (K-Merge).  sign_similarity_grid
 // bounds the CTAs of a launch (the launch takes at most one wave of the
-// device); workspace: 256 bytes (a counter) + that bound · (2·n_b + 1)
-// doubles.
+// device); workspace (sign_similarity_workspace_bytes): 256 bytes of
+// counters, zeroed before the first call, then (2·n_b + 1) doubles per CTA
+// of that bound and per group of 16 of them.
 int sign_similarity_grid(int64_t d_out);
+size_t sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b);
 cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
                                    const uint8_t* const* pb_table, const float* const* ab_table,
                                    int32_t n_b, bool per_row, int64_t d_out, int64_t d_in,

@@ -18,8 +18,11 @@
 // disagreement counts are summed by a transposing butterfly that leaves
 // member j's row total in lanes 2j and 2j+1 (16 shuffles for 16 members),
 // and the even lanes do the fp64 α arithmetic side by side.  Per-CTA partial
-// sums go to the caller's workspace; the last CTA to finish reduces them in a
-// fixed order (deterministic) and writes the cosines and the argmax.
+// sums go to the caller's workspace; the last CTA of each group of kGroup
+// CTAs sums its group's partials, and the last group to finish sums the
+// group partials and writes the cosines and the argmax: fixed orders
+// (deterministic), and the fp64 reduction spread over many SMs instead of
+// one.
 #include <cstdint>
 
 #include "common.cuh"
@@ -31,7 +34,10 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRound = 16;  // pool members whose row loads are in flight together
-constexpr int kMaxGrid = 512;  // CTAs (partials per lane in the final sum: kMaxGrid / 32)
+constexpr int kMaxGrid = 512;  // CTAs of a launch at most
+constexpr int kGroup = 16;     // CTA partials summed by one group reducer
+constexpr int kMaxGroups = kMaxGrid / kGroup;
+static_assert(4 * (1 + kMaxGroups) <= 256, "counters fit the workspace's first 256 bytes");
 
 struct SimArgs {
   const uint8_t* pa;
@@ -44,7 +50,9 @@ struct SimArgs {
   double* cos_out;
   int32_t* best_out;
   double* partial;         // [gridDim.x][2·n_b + 1]: dot[b], norm_b[b], norm_a
-  unsigned int* counter;   // CTAs finished (reset by the last one)
+  double* group_partial;   // [groups][2·n_b + 1]
+  unsigned int* counter;   // [0]: groups finished; [1 + g]: CTAs of group g finished
+                           // (each reset by the one that completes it)
   int vec;                 // 16-byte loads allowed (d_in % 128 == 0, candidate aligned)
 };
 
@@ -149,30 +157,50 @@ __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
   __threadfence();
   __syncthreads();
   __shared__ unsigned int last;
-  if (threadIdx.x == 0) last = atomicAdd(p.counter, 1u) == gridDim.x - 1 ? 1u : 0u;
+  const unsigned int n_cta = gridDim.x;
+  const unsigned int grp = blockIdx.x / kGroup, g0 = grp * kGroup;
+  const unsigned int g_size = n_cta - g0 < kGroup ? n_cta - g0 : kGroup;
+  if (threadIdx.x == 0) last = atomicAdd(p.counter + 1 + grp, 1u) == g_size - 1 ? 1u : 0u;
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // The last CTA: totals over CTAs, then cosines and argmax.  Warp w takes
-  // the values i ≡ w (mod kWarps); lane l loads the partials of CTAs
-  // c ≡ l (mod 32) all at once, sums them in c order, then a butterfly over
-  // the lanes: a fixed order for a given grid, so the result is
-  // deterministic.
-  double* tot = sm;  // reuse: [stride_w]
-  const unsigned int n_cta = gridDim.x;
-  for (int i = warp; i < stride_w; i += kWarps) {
-    double v[kMaxGrid / 32];
+  // The last CTA of the group: its CTAs' partials in CTA order, value i by
+  // thread i (loads bypass L1: other SMs wrote them).
+  for (int i = threadIdx.x; i < stride_w; i += kThreads) {
+    double v[kGroup];
 #pragma unroll
-    for (int q = 0; q < kMaxGrid / 32; ++q) {
-      const unsigned int c = lane + 32u * q;
-      v[q] = c < n_cta ? p.partial[static_cast<int64_t>(c) * stride_w + i] : 0.0;
-    }
+    for (int q = 0; q < kGroup; ++q)
+      v[q] = q < static_cast<int>(g_size)
+                 ? __ldcg(p.partial + static_cast<int64_t>(g0 + q) * stride_w + i)
+                 : 0.0;
     double s = 0.0;
 #pragma unroll
-    for (int q = 0; q < kMaxGrid / 32; ++q) s += v[q];
+    for (int q = 0; q < kGroup; ++q) s += v[q];
+    p.group_partial[static_cast<int64_t>(grp) * stride_w + i] = s;
+  }
+  if (threadIdx.x == 0) p.counter[1 + grp] = 0u;
+  __threadfence();
+  __syncthreads();
+  const unsigned int n_grp = (n_cta + kGroup - 1) / kGroup;
+  if (threadIdx.x == 0) last = atomicAdd(p.counter, 1u) == n_grp - 1 ? 1u : 0u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // The last group: totals over the groups in group order, value i by
+  // thread i, eight loads in flight at a time; then cosines and argmax.
+  double* tot = sm;  // reuse: [stride_w]
+  for (int i = threadIdx.x; i < stride_w; i += kThreads) {
+    double s = 0.0;
+    for (unsigned int q0 = 0; q0 < n_grp; q0 += 8) {
+      double v[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    if (lane == 0) tot[i] = s;
+      for (int q = 0; q < 8; ++q)
+        v[q] = q0 + q < n_grp ? __ldcg(p.group_partial + static_cast<int64_t>(q0 + q) * stride_w + i)
+                              : 0.0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += v[q];
+    }
+    tot[i] = s;
   }
   __syncthreads();
   double* cosv = tot + stride_w;  // [n_b]
@@ -203,6 +231,12 @@ int sign_similarity_grid(int64_t d_out) {
   return static_cast<int>(want < kMaxGrid ? want : kMaxGrid);
 }
 
+size_t sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b) {
+  const size_t grid = static_cast<size_t>(sign_similarity_grid(d_out));
+  const size_t groups = (grid + kGroup - 1) / kGroup;
+  return 256 + (grid + groups) * (2 * static_cast<size_t>(n_b) + 1) * sizeof(double);
+}
+
 cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
                                    const uint8_t* const* pb_table, const float* const* ab_table,
                                    int32_t n_b, bool per_row, int64_t d_out, int64_t d_in,
@@ -221,6 +255,7 @@ cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,
   a.best_out = best_out;
   a.counter = static_cast<unsigned int*>(workspace);
   a.partial = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + 256);
+  a.group_partial = a.partial + static_cast<int64_t>(sign_similarity_grid(d_out)) * (2 * n_b + 1);
   a.vec = vec ? 1 : 0;
   const size_t smem = static_cast<size_t>(kWarps) * (2 * n_b + 1) * sizeof(double);
   // One wave: at most the CTAs the device holds at once (a second, partial

@@ -176,8 +176,8 @@ bd_status bitdelta_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft
  *   cos_out                device double [n_b]
  *   best_out               device int32 [1]: argmax of cos_out (ties: lowest b)
  *   workspace              device, bitdelta_sign_similarity_workspace_bytes()
- *                          bytes, 256-byte aligned; its first word is zeroed by
- *                          the call (deterministic reduction in a fixed order;
+ *                          bytes, 256-byte aligned; its first 256 bytes are
+ *                          zeroed by the call (deterministic reduction in a fixed order;
  *                          the grid follows the device's SM count, so results
  *                          repeat bit for bit on the same device model)
  * Reads (1 + n_b) · d_out · d_in / 8 sign bytes.  Errors as bitdelta_linear
