@@ -63,6 +63,22 @@ def test_grouped_decode_only_ragged_d_in():
     assert_linear_close(y, oracle.linear_grouped(x, off, var, wb, packs, alphas, True))
 
 
+def test_grouped_empty_segments():
+    """Zero-length segments (offsets repeat) at the start, between short and
+    long segments and at the end: they produce no rows and no tiles, and the
+    rows around them keep their own variants."""
+    lengths = [0, 3, 0, 300, 0, 1, 0, 40, 0]
+    wb, packs, alphas, off, var, x = _setup(19, 256, 512, 3, lengths,
+                                            variants=[2, 1, 3, 2, 1, 3, 2, 1, 3])
+    y = _run(wb, packs, alphas, off, var, x, True)
+    ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
+    assert_linear_close(y, ref)
+    for s in range(len(lengths)):
+        if lengths[s] > 0:
+            rows = slice(off[s], off[s + 1])
+            assert_linear_close(y[rows], ref[rows], f"segment {s}")
+
+
 def test_grouped_long_segments_without_tma_shape():
     """Long segments with d_in % 128 != 0 run through the decode kernel."""
     lengths = [33, 1, 20]
