@@ -317,6 +317,21 @@ def test_grouped_equals_per_segment_linear():
             assert np.array_equal(y[rows], ref)
 
 
+def test_grouped_empty_segments_change_nothing():
+    """Zero-length segments (repeated offsets) inserted anywhere leave every
+    row's output as it was without them."""
+    x, off, var, wb, packs, alphas = _grouped_case()
+    y = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
+    lengths = np.diff(off)
+    ins_len, ins_var = [0], [2]
+    for L, v in zip(lengths, var):
+        ins_len += [int(L), 0]
+        ins_var += [int(v), 3]
+    off2 = np.concatenate([[0], np.cumsum(ins_len)]).astype(np.int32)
+    y2 = oracle.linear_grouped(x, off2, np.array(ins_var, np.int32), wb, packs, alphas, True)
+    assert np.array_equal(y, y2)
+
+
 def test_grouped_at_matches_full():
     x, off, var, wb, packs, alphas = _grouped_case()
     y = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
