@@ -328,7 +328,7 @@ class Prefill:
             out[mode] = {"ms_per_step": t, "tflops": self.flops_per_step() / (t * 1e-3) / 1e12}
         # fused against unfused at fewer tokens (same four shapes, eager launches
         # for both): the unfused path pays its reconstruct once per weight, the
-        # fused kernel its transform once per 256-token tile
+        # fused kernel its transform once per token tile (256 or 512 tokens)
         out["fused_vs_unfused_by_tokens"] = {}
         for m in (512, 1024):
             res = {}
