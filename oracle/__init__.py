@@ -55,6 +55,8 @@ def _load():
         lib.orc_reconstruct.restype = None
         lib.orc_linear.argtypes = [p, i64, p, p, p, ctypes.c_int, i64, i64, p]
         lib.orc_linear.restype = None
+        lib.orc_linear_split.argtypes = [p, i64, p, p, p, ctypes.c_int, i64, i64, p]
+        lib.orc_linear_split.restype = None
         lib.orc_linear_at.argtypes = [p, i64, p, p, p, ctypes.c_int, i64, i64, p, p, i64, p]
         lib.orc_linear_at.restype = None
         lib.orc_linear_grouped.argtypes = [p, i64, p, p, i32, p, p, p, i32, ctypes.c_int,
@@ -121,6 +123,21 @@ def linear(x, w_base, packed, alpha, per_row: bool):
     y = np.empty((M, d_out), np.float64)
     _load().orc_linear(_ptr(xx), M, _ptr(wb), _ptr(pk), _ptr(al), int(per_row), d_out, d_in,
                        _ptr(y))
+    return y
+
+
+def linear_split(x, w_base, packed, alpha, per_row: bool):
+    """fp64 y [M, d_out] = x·W_baseᵀ + α ⊙ (x·Sᵀ): the effective weight
+    W_base + α·sign(Δ) as a real number, not rounded to bf16."""
+    xx = _c(x, np.uint16)
+    wb = _c(w_base, np.uint16)
+    pk = _c(packed, np.uint8)
+    al = _c(alpha, np.float32)
+    M = xx.shape[0]
+    d_out, d_in = wb.shape
+    y = np.empty((M, d_out), np.float64)
+    _load().orc_linear_split(_ptr(xx), M, _ptr(wb), _ptr(pk), _ptr(al), int(per_row), d_out, d_in,
+                             _ptr(y))
     return y
 
 

@@ -189,6 +189,28 @@ void orc_linear(const uint16_t* x, int64_t M, const uint16_t* w_base, const uint
   delete[] w_row;
 }
 
+// [Math] the effective weight as the real number W_base + α·sign(Δ), before
+// any rounding to a storage dtype: y = x·W_baseᵀ + α ⊙ (x·Sᵀ) with S = ±1 from
+// the packed bits, every product and sum in fp64 (x·W_base products of two
+// bf16 values and α·(±1) are exact in fp64).  The decode kernels compute this
+// split form; it differs from orc_linear only by the bf16 rounding of W_eff.
+void orc_linear_split(const uint16_t* x, int64_t M, const uint16_t* w_base,
+                      const uint8_t* packed, const float* alpha, int per_row, int64_t d_out,
+                      int64_t d_in, double* y) {
+  for (int64_t n = 0; n < d_out; ++n) {
+    const double a = static_cast<double>(alpha_for_row(alpha, per_row, n));
+    for (int64_t m = 0; m < M; ++m) {
+      double base = 0.0, signs = 0.0;
+      for (int64_t k = 0; k < d_in; ++k) {
+        const double xv = static_cast<double>(bf16_bits_to_float(x[m * d_in + k]));
+        base += xv * static_cast<double>(bf16_bits_to_float(w_base[n * d_in + k]));
+        signs += packed_bit(packed, d_in, n, k) ? xv : -xv;
+      }
+      y[m * d_out + n] = base + a * signs;
+    }
+  }
+}
+
 // The same linear, one output element at a time: y_out[i] = y[m_idx[i]][n_idx[i]].
 void orc_linear_at(const uint16_t* x, int64_t M, const uint16_t* w_base, const uint8_t* packed,
                    const float* alpha, int per_row, int64_t d_out, int64_t d_in,

@@ -274,6 +274,62 @@ def test_linear_matches_numpy_on_reconstructed():
                                    rtol=1e-12, atol=1e-12)
 
 
+def test_golden_linear_split_per_row(tiny):
+    """The split form on the hand-derived fixture: with per-row α every
+    W_base ± α there is exact in bf16 (or α = 0), so the unrounded effective
+    weight equals the rounded one and y is the hand-derived y."""
+    packed = np.array(tiny["packed"], np.uint8)
+    alpha = np.array(tiny["alpha_per_row"], np.float32)
+    y = oracle.linear_split(tiny["xb"], tiny["wb"], packed, alpha, per_row=True)
+    assert y.tolist() == tiny["y_per_row"]
+
+
+def test_linear_split_closed_form_popcount():
+    """W_base = 0, x = 1: y_n = α_n · (2·popcount(row n) − d_in), exact, for
+    any α (nothing is rounded in the split form)."""
+    d_out, d_in = 16, 64
+    g = np.random.default_rng(13)
+    packed = g.integers(0, 256, size=(d_out, d_in // 8), dtype=np.uint8)
+    alpha = g.uniform(1e-4, 3e-2, size=d_out).astype(np.float32)
+    wb = np.zeros((d_out, d_in), np.uint16)
+    x = synth.bf16_bits(np.ones((3, d_in), np.float32))
+    y = oracle.linear_split(x, wb, packed, alpha, per_row=True)
+    pop = np.array([sum(bin(int(b)).count("1") for b in row) for row in packed])
+    ref = alpha.astype(np.float64) * (2 * pop - d_in)
+    for m in range(3):
+        assert np.array_equal(y[m], ref)
+    y1 = oracle.linear_split(x, wb, packed, alpha[:1], per_row=False)
+    assert np.array_equal(y1[0], float(alpha[0]) * (2 * pop - d_in))
+
+
+def test_linear_split_alpha_zero_is_plain_gemm():
+    wb, wf = synth.layer(12, 40, 128)
+    x = synth.activations(12, 6, 128)
+    packed, _, _ = oracle.compress(wb, wf, True)
+    y = oracle.linear_split(x, wb, packed, np.zeros(40, np.float32), per_row=True)
+    ref = synth.bf16_to_f32(x).astype(np.float64) @ synth.bf16_to_f32(wb).astype(np.float64).T
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_split_differs_from_rounded_by_the_weight_rounding():
+    """The two forms differ only by the bf16 rounding of W_eff: per output,
+    |split − rounded| <= Σ_k |x_k| · 2^-8 · |W_eff,k| · (1 + 2^-7) (RNE to 8
+    significant bits moves a value by at most 2^-8 of itself), and with
+    deltas as large as the weights they do differ."""
+    wb = synth.base_weight(14, 32, 256)
+    wf = synth.finetuned_weight(14, wb, b=0.02, stream=3)
+    x = synth.activations(14, 5, 256)
+    for per_row in (True, False):
+        packed, a32, _ = oracle.compress(wb, wf, per_row)
+        split = oracle.linear_split(x, wb, packed, a32, per_row)
+        rounded = oracle.linear(x, wb, packed, a32, per_row)
+        weff = synth.bf16_to_f32(oracle.reconstruct(wb, packed, a32, per_row)).astype(np.float64)
+        xa = np.abs(synth.bf16_to_f32(x).astype(np.float64))
+        bound = 2.0 ** -8 * (1 + 2.0 ** -7) * (xa @ np.abs(weff).T)
+        assert (np.abs(split - rounded) <= bound).all()
+        assert np.abs(split - rounded).max() > 0
+
+
 def test_linear_at_matches_full():
     wb, wf = synth.layer(6, 33, 64)
     x = synth.activations(6, 9, 64)
