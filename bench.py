@@ -45,11 +45,10 @@ import torch  # noqa: E402
 
 METRIC = "bitdelta_linear TFLOP/s (prefill) & GB/s (decode) as % of GB300 roofline"
 # DRAM bytes (read + write) of one decode launch (4096 x 4096, M = 8) from an ncu
-# capture of `python bench.py --profile decode`, summarised in the file named by
-# DECODE_PROFILE.  Valid for the kernel build that capture was taken on; reset
-# to None whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 35_761_152
-DECODE_PROFILE = "profiles/gemv_single_async_decode_4096x4096_M8.md"
+# capture of `python bench.py --profile decode` (dram__bytes_read.sum +
+# dram__bytes_write.sum of gemv_single_async_kernel).  Valid for the kernel
+# build that capture was taken on; None whenever that kernel has changed since.
+DECODE_TRAFFIC_BYTES = None
 
 # --------------------------------------------------------------------------- peaks
 
@@ -426,32 +425,29 @@ class Slice40:
     name = "slice40_llama70b_prefill512_decode8x2variants_compress3rd"
     L = 40
     shapes = Prefill.shapes
-    prefill_M = 512
-    decode_M = 8
+    prefill_M = 512   # synth.device.SLICE_PREFILL_TOKENS
+    decode_M = 8      # synth.device.SLICE_DECODE_ROWS
 
     def __init__(self, bd, seed: int = 5):
-        import synth
         import synth.device as sd
         self.bd = bd
         self.layers = []
-        scales = synth.variant_scales(seed, 3)
         for l in range(self.L):
             mats = {}
             for i, (nm, d_out, d_in) in enumerate(self.shapes):
-                wb = sd.normal_bf16((d_out, d_in), seed, 10000 + 10 * l + i, 0.02)
+                wb = sd.slice_base(l, i, seed)
                 var = []
-                for v in range(2):
-                    wf = sd.finetuned_bf16(wb, seed, 20000 + 100 * l + 10 * i + v, float(scales[v]))
+                for v in (1, 2):
+                    wf = sd.slice_finetuned(wb, l, i, v, seed)
                     var.append(bd.bitdelta_compress(wb, wf, per_row=True))
                     del wf
                 pt, at = bd.variant_tables([var[0][0], var[1][0]], [var[0][1], var[1][1]], "cuda")
                 mats[nm] = (wb, var, pt, at)
             self.layers.append(mats)
-        self.b3 = float(scales[2])
         self.seed = seed
         widths = sorted({d_in for _, _, d_in in self.shapes})
-        self.xp = {d: sd.normal_bf16((self.prefill_M, d), seed, 30000 + d) for d in widths}
-        self.xd = {d: sd.normal_bf16((self.decode_M, d), seed, 40000 + d) for d in widths}
+        self.xp = {d: sd.slice_inputs(d, self.prefill_M, False, seed) for d in widths}
+        self.xd = {d: sd.slice_inputs(d, self.decode_M, True, seed) for d in widths}
         self.yp = {nm: torch.empty((self.prefill_M, d_out), dtype=torch.bfloat16, device="cuda")
                    for nm, d_out, _ in self.shapes}
         self.yd = {nm: torch.empty((self.decode_M, d_out), dtype=torch.bfloat16, device="cuda")
@@ -514,12 +510,7 @@ class Slice40:
         total = 0.0
         for l, mats in enumerate(self.layers):
             for i, (nm, d_out, d_in) in enumerate(self.shapes):
-                wb = mats[nm][0]
-                rc = sd._load().synth_finetuned_bf16(
-                    ctypes.c_void_p(self.wf3[nm].data_ptr()), ctypes.c_void_p(wb.data_ptr()),
-                    wb.numel(), self.seed, 50000 + 10 * l + i, self.b3, sd._stream())
-                if rc != 0:
-                    raise RuntimeError(f"synth_finetuned_bf16 failed: cuda error {rc}")
+                sd.slice_finetuned(mats[nm][0], l, i, 3, self.seed, out=self.wf3[nm])
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
             for nm, d_out, d_in in self.shapes:
@@ -1164,8 +1155,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": DECODE_TRAFFIC_BYTES,
-                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, "
-                                           f"one M=8 launch ({DECODE_PROFILE})",
+                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of "
+                                           "one gemv_single_async_kernel launch, 4096x4096, M=8",
                          "kernel": "bitdelta_linear decode: gemv_single_async_kernel (M=1..8), "
                                    "gemv_single_kernel (M=16)",
                          "peak_source": peaks["source"]},

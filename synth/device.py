@@ -58,8 +58,9 @@ def normal_bf16(shape, seed: int, stream: int, sigma: float = 1.0, device="cuda"
     return out
 
 
-def finetuned_bf16(base: torch.Tensor, seed: int, stream: int, b: float = LAPLACE_B):
-    out = torch.empty_like(base)
+def finetuned_bf16(base: torch.Tensor, seed: int, stream: int, b: float = LAPLACE_B,
+                   out: torch.Tensor = None):
+    out = torch.empty_like(base) if out is None else out
     rc = _load().synth_finetuned_bf16(ctypes.c_void_p(out.data_ptr()),
                                       ctypes.c_void_p(base.data_ptr()), base.numel(), seed,
                                       stream, b, _stream())
@@ -73,3 +74,46 @@ def layer(seed: int, d_out: int, d_in: int, sigma: float = SIGMA_BASE, b: float 
     """(W_base, W_ft) bf16 CUDA tensors [d_out, d_in]."""
     wb = normal_bf16((d_out, d_in), seed, 2 * stream + 1, sigma)
     return wb, finetuned_bf16(wb, seed, 2 * stream + 2, b)
+
+
+# --------------------------------------------------------------------------- 40-layer slice
+
+# Projections of one Llama-70B-shaped decoder layer (name, d_out, d_in): QKV
+# 8192 -> 10240 (64 query and 8 key/value heads of 128), O 8192 -> 8192,
+# gate+up 8192 -> 2 x 28672, down 28672 -> 8192.
+SLICE_SHAPES = (("qkv", 10240, 8192), ("o", 8192, 8192), ("gate_up", 57344, 8192),
+                ("down", 8192, 28672))
+SLICE_SEED = 5
+SLICE_PREFILL_TOKENS = 512
+SLICE_DECODE_ROWS = 8
+
+
+def slice_variant_scales(seed: int = SLICE_SEED):
+    """Laplace scales of the slice's three fine-tuned variants (two resident,
+    the third compressed layer by layer)."""
+    from . import variant_scales
+    return variant_scales(seed, 3)
+
+
+def slice_base(layer: int, proj: int, seed: int = SLICE_SEED):
+    """W_base of projection `proj` (index into SLICE_SHAPES) of layer `layer`."""
+    _, d_out, d_in = SLICE_SHAPES[proj]
+    return normal_bf16((d_out, d_in), seed, 10000 + 10 * layer + proj, SIGMA_BASE)
+
+
+def slice_finetuned(wb: torch.Tensor, layer: int, proj: int, variant: int,
+                    seed: int = SLICE_SEED, out: torch.Tensor = None):
+    """W_ft of resident variant 1 or 2, or of variant 3 (the one compressed
+    layer by layer), for one projection of the slice."""
+    b = float(slice_variant_scales(seed)[variant - 1])
+    if variant == 3:
+        stream = 50000 + 10 * layer + proj
+    else:
+        stream = 20000 + 100 * layer + 10 * proj + (variant - 1)
+    return finetuned_bf16(wb, seed, stream, b, out)
+
+
+def slice_inputs(d_in: int, rows: int, decode: bool, seed: int = SLICE_SEED):
+    """x of one projection's width: the 512-token prefill input or the 8-row
+    decode batch (fresh N(0, 1) per width; projections are not chained)."""
+    return normal_bf16((rows, d_in), seed, (40000 if decode else 30000) + d_in)
