@@ -41,6 +41,10 @@ CACHE_EXPORTED = (
     "bd_cache_create", "bd_cache_destroy", "bd_cache_register", "bd_cache_acquire",
     "bd_cache_release", "bd_cache_get_stats", "bd_cache_slot_of",
 )
+KMERGE_EXPORTED = (
+    "bd_kmerge_create", "bd_kmerge_destroy", "bd_kmerge_request", "bd_kmerge_commit",
+    "bd_kmerge_entry_of", "bd_kmerge_entry_info", "bd_kmerge_get_stats",
+)
 
 
 class BitDeltaError(RuntimeError):
@@ -110,6 +114,17 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bd_cache_get_stats.argtypes = [p, ctypes.POINTER(_CacheStats)]
     lib.bd_cache_slot_of.argtypes = [p, i32, ctypes.POINTER(i32)]
     for name in CACHE_EXPORTED:
+        getattr(lib, name).restype = st
+    u64 = ctypes.c_uint64
+    lib.bd_kmerge_create.argtypes = [u64, ctypes.POINTER(p)]
+    lib.bd_kmerge_destroy.argtypes = [p]
+    lib.bd_kmerge_request.argtypes = [p, i32, u64, p, i32, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(i32)]
+    lib.bd_kmerge_commit.argtypes = [p, i32, i32, i32, u64]
+    lib.bd_kmerge_entry_of.argtypes = [p, i32, ctypes.POINTER(i32)]
+    lib.bd_kmerge_entry_info.argtypes = [p, i32, ctypes.POINTER(u64), ctypes.POINTER(i32)]
+    lib.bd_kmerge_get_stats.argtypes = [p, ctypes.POINTER(_KMergeStats)]
+    for name in KMERGE_EXPORTED:
         getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -425,6 +440,95 @@ class DeltaCache:
     def close(self) -> None:
         if self.handle is not None:
             _check("bd_cache_destroy", load().bd_cache_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# --------------------------------------------------------------------------- K-Merge pool
+
+
+class _KMergeStats(ctypes.Structure):
+    _fields_ = [("entries", ctypes.c_int32), ("adapters", ctypes.c_int32)] + [
+        (n, ctypes.c_uint64) for n in ("used_bytes", "budget_bytes", "stores", "merges_proposed",
+                                       "merges_accepted", "merges_rejected", "rejects", "hits")]
+
+
+class KMergePool:
+    """The K-Merge adapter pool of include/bitdelta_kmerge.h (host policy).
+
+    request(adapter, nbytes, cos=None) returns (action, entry), action one of
+    "hit", "store", "need_similarity", "merge", "reject"; after "merge" the
+    caller merges the adapter into the entry and reports the outcome with
+    commit().  Similarities come from bitdelta_sign_similarity against the
+    entries' stored deltas (see request_on_device)."""
+
+    ACTIONS = ("hit", "store", "need_similarity", "merge", "reject")
+
+    def __init__(self, budget_bytes: int):
+        handle = ctypes.c_void_p()
+        _check("bd_kmerge_create", load().bd_kmerge_create(budget_bytes, ctypes.byref(handle)))
+        self.handle = handle
+
+    def request(self, adapter: int, nbytes: int, cos=None):
+        action, entry = ctypes.c_int(), ctypes.c_int32()
+        if cos is None:
+            cptr, n = None, 0
+            keep = None
+        else:
+            keep = (ctypes.c_double * max(len(cos), 1))(*[float(c) for c in cos])
+            cptr, n = ctypes.cast(keep, ctypes.c_void_p), len(cos)
+        _check("bd_kmerge_request", load().bd_kmerge_request(
+            self.handle, adapter, nbytes, cptr, n, ctypes.byref(action), ctypes.byref(entry)))
+        return self.ACTIONS[action.value], entry.value
+
+    def request_on_device(self, adapter: int, nbytes: int, packed, alpha, entry_packed,
+                          entry_alpha, per_row: bool = True):
+        """request(); when the pool needs the similarities, computes them on
+        the GPU (bitdelta_sign_similarity of the adapter's packed/alpha with
+        every entry's, in entry order) and requests again.  Returns (action,
+        entry, cos) with cos a CPU float64 tensor or None."""
+        action, entry = self.request(adapter, nbytes)
+        if action != "need_similarity":
+            return action, entry, None
+        parts = []
+        for lo in range(0, len(entry_packed), 256):   # at most 256 members per call
+            ep, ea = list(entry_packed[lo:lo + 256]), list(entry_alpha[lo:lo + 256])
+            pt, at = variant_tables(ep, ea, packed.device)
+            cos, _ = bitdelta_sign_similarity(packed, alpha, pt, at, len(ep), per_row)
+            parts.append(cos.cpu())
+        cos_h = torch.cat(parts)
+        action, entry = self.request(adapter, nbytes, cos_h.tolist())
+        return action, entry, cos_h
+
+    def commit(self, adapter: int, entry: int, accepted: bool, merged_bytes: int) -> None:
+        _check("bd_kmerge_commit", load().bd_kmerge_commit(self.handle, adapter, entry,
+                                                           1 if accepted else 0, merged_bytes))
+
+    def entry_of(self, adapter: int) -> int:
+        e = ctypes.c_int32()
+        _check("bd_kmerge_entry_of", load().bd_kmerge_entry_of(self.handle, adapter,
+                                                               ctypes.byref(e)))
+        return e.value
+
+    def entry_info(self, entry: int):
+        b, n = ctypes.c_uint64(), ctypes.c_int32()
+        _check("bd_kmerge_entry_info", load().bd_kmerge_entry_info(
+            self.handle, entry, ctypes.byref(b), ctypes.byref(n)))
+        return int(b.value), int(n.value)
+
+    def stats(self) -> dict:
+        st = _KMergeStats()
+        _check("bd_kmerge_get_stats", load().bd_kmerge_get_stats(self.handle, ctypes.byref(st)))
+        return {n: int(getattr(st, n)) for n, _ in _KMergeStats._fields_}
+
+    def close(self) -> None:
+        if self.handle is not None:
+            _check("bd_kmerge_destroy", load().bd_kmerge_destroy(self.handle))
             self.handle = None
 
     def __del__(self):

@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "bitdelta")
 LIB_PATH = os.path.join(HERE, "libbitdelta.so")
 
-SOURCES = ["abi.cu", "compress.cu", "reconstruct.cu", "gemv.cu", "gemm_tc.cu", "gemm_pair.cu",
-           "cache.cu", "similarity.cu", "monosoup.cu"]
+SOURCES = ["abi.cu", "compress.cu", "reconstruct.cu", "gemv.cu", "gemm_pair.cu", "cache.cu",
+           "kmerge.cu", "similarity.cu", "monosoup.cu"]
 HEADERS = ["common.cuh", "kernels.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -35,6 +35,7 @@ def _inputs_mtime() -> float:
     paths = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     paths.append(os.path.join(INCLUDE, "bitdelta.h"))
     paths.append(os.path.join(INCLUDE, "bitdelta_cache.h"))
+    paths.append(os.path.join(INCLUDE, "bitdelta_kmerge.h"))
     paths.append(os.path.abspath(__file__))
     return max(os.path.getmtime(p) for p in paths)
 

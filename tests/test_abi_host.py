@@ -56,6 +56,16 @@ def test_library_exports_the_delta_cache(lib):
     assert set(bd.CACHE_EXPORTED) == set(declared)
 
 
+def test_library_exports_the_kmerge_pool(lib):
+    text = open(os.path.join(os.path.dirname(HEADER), "bitdelta_kmerge.h")).read()
+    declared = sorted(set(re.findall(r"\b(bd_kmerge_\w+)\s*\(", text)))
+    out = subprocess.run(["nm", "-D", "--defined-only", bd.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert declared and set(declared) <= exported
+    assert set(bd.KMERGE_EXPORTED) == set(declared)
+
+
 def test_packed_bytes_and_workspace(lib):
     assert bd.bitdelta_packed_bytes(4096, 4096) == 4096 * 512   # "Infrastructure details"
     assert bd.bitdelta_packed_bytes(8, 16) == 16
