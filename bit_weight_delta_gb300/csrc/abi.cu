@@ -23,6 +23,10 @@ std::atomic<int> g_prefill_tile{BD_PREFILL_TILE_AUTO};
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDecodeMaxRows = 16;
+// Shared memory the decode kernel's grouped pass may give to its bucket
+// counts and short-row index list (the rest of the SM's shared memory is its
+// cp.async ring).
+constexpr size_t kGroupedListBytes = 200 * 1024;
 
 struct DeviceState {
   bool ready = false;
@@ -106,9 +110,6 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
   return d_in % 128 == 0 && d_in < INT32_MAX && d_out < INT32_MAX && rows_x < INT32_MAX;
 }
 
-#ifndef BD_GEMM_PAIR
-#define BD_GEMM_PAIR 1
-#endif
 // Cost of one 512-token pair tile in 256-token pair tiles, in quarters: the
 // steady state of the two kernels on 8192 x 57344 at M = 2048 measured 1454
 // and 1266 TFLOP/s, 2 x 1266 / 1454 = 1.74.
@@ -142,39 +143,27 @@ bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens) {
 // Launch the tensor-core kernel on g (x has rows_x rows, of which the
 // longest run of one tile schedule — M, or the longest segment — has
 // long_tokens; extra_tiles bounds the ragged token tiles beyond
-// ceil(rows_x / tile tokens), one per segment in grouped mode).  The pair
+// ceil(rows_x / tile tokens), one per segment in grouped mode): the pair
 // kernel (cta_group::2, 256 output rows by 256 or 512 tokens per tile,
-// use_wide_tiles) unless built with BD_GEMM_PAIR=0, or when the device cannot
-// place a cluster of two of its CTAs: then the one-CTA kernel.  Returns
-// false, launching nothing, when a tensor map cannot be encoded.
+// use_wide_tiles).  Returns false, launching nothing, when a tensor map
+// cannot be encoded or the device cannot place a cluster of two of its CTAs
+// (every GB300 can); the caller then runs the rows on the decode kernel.
 bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t rows_x,
-               int64_t long_tokens, int64_t extra_tiles, int num_sms, cudaStream_t s,
-               cudaError_t* err) {
+               int64_t long_tokens, int64_t extra_tiles, cudaStream_t s, cudaError_t* err) {
   CUtensorMap tw, tx;
-  if (BD_GEMM_PAIR) {
-    const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens);
-    const int bk = wide ? bd::gemm_pair_wide_block_k() : bd::gemm_pair_block_k();
-    const int64_t tok = bd::gemm_pair_tokens(wide);
-    if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
-        !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_pair_x_rows()))
-      return false;
-    const int64_t pair_tiles = ((g.d_out + 2 * bd::gemm_block_rows() - 1) /
-                                (2 * bd::gemm_block_rows())) *
-                               ((rows_x + tok - 1) / tok + extra_tiles);
-    *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, wide, s);
-    if (*err != cudaErrorInvalidConfiguration) return true;
-    (void)cudaGetLastError();  // no cluster fits: fall through to one CTA per tile
-  }
-  const int bk = bd::gemm_block_k();
+  const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens);
+  const int bk = wide ? bd::gemm_pair_wide_block_k() : bd::gemm_pair_block_k();
+  const int64_t tok = bd::gemm_pair_tokens(wide);
   if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
-      !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_block_tokens()))
+      !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_pair_x_rows()))
     return false;
-  const int64_t tok = bd::gemm_block_tokens();
-  const int64_t tiles = ((g.d_out + bd::gemm_block_rows() - 1) / bd::gemm_block_rows()) *
-                        ((rows_x + tok - 1) / tok + extra_tiles);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  *err = bd::launch_gemm(g, tw, tx, grid, s);
-  return true;
+  const int64_t pair_tiles =
+      ((g.d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows())) *
+      ((rows_x + tok - 1) / tok + extra_tiles);
+  *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, wide, s);
+  if (*err != cudaErrorInvalidConfiguration) return true;
+  (void)cudaGetLastError();  // no cluster of two fits: nothing was launched
+  return false;
 }
 
 }  // namespace
@@ -193,6 +182,11 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
   return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::mutex& host_cache_mutex() {
+  static std::mutex mu;
+  return mu;
 }
 
 // Error word, wait limit and SM count of the current device, for entry points
@@ -287,7 +281,7 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
     g.y = y;
     g.ctx = ctx;
     cudaError_t e = cudaSuccess;
-    if (launch_tc(g, w_base, x, M, M, 0, dev->num_sms, s, &e)) return from_cuda(e);
+    if (launch_tc(g, w_base, x, M, M, 0, s, &e)) return from_cuda(e);
   }
   bd::GemvArgs a{};
   a.x = x;
@@ -326,9 +320,19 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
   const bd::DevCtx ctx = make_ctx(dev);
 
   // Long segments on the tensor cores when the shape allows it; the decode
-  // kernel takes every segment the tensor-core kernel does not.
-  bool use_tc = max_seg_len > kDecodeMaxRows && tc_shape_ok(M_total, d_out, d_in) &&
-                n_seg <= bd::kGemmMaxSegs;
+  // kernel takes every segment the tensor-core kernel does not.  The pair
+  // kernel holds at most kGemmMaxSegs segments in shared memory, so a longer
+  // table is launched in consecutive slices of it (the offsets are absolute
+  // row indices, so a slice is a pointer offset into both tables).
+  bool use_tc = max_seg_len > kDecodeMaxRows && tc_shape_ok(M_total, d_out, d_in);
+  // Every check before the first launch: the short rows' index list must fit
+  // the decode kernel's shared memory whichever way the rows are split.
+  const int64_t short_rows_bound =
+      use_tc ? (M_total < int64_t{n_seg} * kDecodeMaxRows ? M_total
+                                                          : int64_t{n_seg} * kDecodeMaxRows)
+             : M_total;
+  if (bd::gemv_grouped_smem_bytes(n_var, short_rows_bound) > kGroupedListBytes)
+    return BD_ERR_UNSUPPORTED_SHAPE;
   if (use_tc) {
     bd::GemmArgs g{};
     g.M = M_total;
@@ -336,28 +340,31 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
     g.d_in = d_in;
     g.per_row = mode == BD_ALPHA_PER_ROW;
     g.y = y;
-    g.seg_off = seg_offsets;
-    g.seg_var = seg_variant;
-    g.n_seg = n_seg;
     g.n_var = n_var;
     g.max_short = static_cast<int32_t>(kDecodeMaxRows);
     g.packed_table = packed_table;
     g.alpha_table = alpha_table;
     g.ctx = ctx;
-    // token tiles over all segments <= total tiles of M_total + one ragged
-    // tile per segment
-    cudaError_t e = cudaSuccess;
-    use_tc = launch_tc(g, w_base, x, M_total, max_seg_len, n_seg, dev->num_sms, s, &e);
-    if (use_tc && (st = from_cuda(e)) != BD_OK) return st;
+    for (int32_t s0 = 0; s0 < n_seg; s0 += bd::kGemmMaxSegs) {
+      g.seg_off = seg_offsets + s0;
+      g.seg_var = seg_variant + s0;
+      g.n_seg = n_seg - s0 < bd::kGemmMaxSegs ? n_seg - s0 : bd::kGemmMaxSegs;
+      // token tiles over the slice's segments <= tiles of M_total + one
+      // ragged tile per segment
+      cudaError_t e = cudaSuccess;
+      const bool launched = launch_tc(g, w_base, x, M_total, max_seg_len, g.n_seg, s, &e);
+      if (launched && (st = from_cuda(e)) != BD_OK) return st;
+      if (!launched) {
+        if (s0 > 0) return BD_ERR_CUDA;  // the first slice launched: cannot happen
+        use_tc = false;                  // no CTA pair fits: every row on the decode kernel
+        break;
+      }
+    }
+    // nothing launched yet when the first slice fell back
+    if (!use_tc && bd::gemv_grouped_smem_bytes(n_var, M_total) > kGroupedListBytes)
+      return BD_ERR_UNSUPPORTED_SHAPE;
   }
   const int32_t short_limit = use_tc ? static_cast<int32_t>(kDecodeMaxRows) : INT32_MAX;
-
-  const int64_t short_rows_bound =
-      use_tc ? (M_total < int64_t{n_seg} * kDecodeMaxRows ? M_total
-                                                           : int64_t{n_seg} * kDecodeMaxRows)
-             : M_total;
-  if (bd::gemv_grouped_smem_bytes(n_var, short_rows_bound) > 200 * 1024)
-    return BD_ERR_UNSUPPORTED_SHAPE;
   bd::GemvArgs a{};
   a.x = x;
   a.M = M_total;
@@ -374,7 +381,7 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
   a.packed_table = packed_table;
   a.alpha_table = alpha_table;
   a.ctx = ctx;
-  return from_cuda(bd::launch_gemv_grouped(a, short_rows_bound, s));
+  return from_cuda(bd::launch_gemv_grouped(a, use_tc ? short_rows_bound : M_total, s));
 }
 
 bd_status bitdelta_check_error(bd_stream_t stream) {

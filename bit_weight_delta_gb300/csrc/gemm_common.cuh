@@ -1,7 +1,6 @@
-// gemm_common.cuh — pieces shared by the two prefill kernels (one CTA per
-// tile in gemm_tc.cu, CTA pairs in gemm_pair.cu): the tile schedule, the
-// W_eff transform arithmetic, tensor-memory stores, the A-from-TMEM MMA, and
-// the cluster primitives of the pair kernel.
+// gemm_common.cuh — pieces of the prefill kernel (CTA pairs, gemm_pair.cu):
+// the tile schedule, the W_eff transform arithmetic, tensor-memory stores and
+// loads, and the cluster forms of the tcgen05 and mbarrier primitives.
 #pragma once
 
 #include <cstdint>
@@ -222,18 +221,6 @@ __device__ __forceinline__ void store_acc_rows(uint32_t taddr, uint16_t* y, int6
     }
     yp += 32 * d_out;
   }
-}
-
-// D[tmem] (+)= A[tmem] · B[smem]ᵀ, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
-                                                 uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // ------------------------------------------------------------------ CTA pairs

@@ -503,6 +503,7 @@ cudaError_t pair_capacity(int* pairs) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(host_cache_mutex());
   if (!done[dev]) {
     e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel<kWide>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kWide>::kSmemBytes);
@@ -540,6 +541,7 @@ cudaError_t launch_pair_instance(const GemmArgs& p, const CUtensorMap& tmap_w,
 
 }  // namespace
 
+int gemm_block_rows() { return kBM; }
 int gemm_pair_x_rows() { return kXBox; }
 int gemm_pair_block_k() { return Cfg<false>::kBK; }
 int gemm_pair_wide_block_k() { return Cfg<true>::kBK; }
@@ -555,6 +557,26 @@ cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
                              cudaStream_t stream) {
   return wide ? launch_pair_instance<true>(p, tmap_w, tmap_x, pair_tiles_bound, stream)
               : launch_pair_instance<false>(p, tmap_w, tmap_x, pair_tiles_bound, stream);
+}
+
+// ------------------------------------------------------------------ test hook
+
+namespace {
+__global__ void wait_timeout_probe_kernel(DevCtx ctx) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    // Nothing ever arrives on `bar`: the bounded wait must give up.
+    mbar_wait(&bar, 0, ctx, nullptr);
+  }
+  __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout_probe(DevCtx ctx, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(ctx);
+  return cudaGetLastError();
 }
 
 }  // namespace bd

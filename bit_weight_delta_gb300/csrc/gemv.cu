@@ -26,8 +26,8 @@
 // shared memory (three super-chunks in flight per warp, no registers held) and
 // puts the W rows on the MMA's A side.  Per weight the kernels move
 // 2 + 1/8 bytes from HBM; x stays in L1/L2.  Launched with programmatic
-// dependent launch: the CTA prefetches its weight slice into L2 before it
-// waits for the previous kernel, so consecutive layers overlap.
+// dependent launch: the register kernel prefetches the head of its weight
+// slice into L2 before it waits for the previous kernel.
 #include <cstdint>
 
 #include "common.cuh"
@@ -730,22 +730,31 @@ __device__ __forceinline__ void gemv_group_mixed(const GemvArgs& p, const MixedG
 }
 
 // Single variant: blockIdx.y (strided) picks 16 consecutive x rows.
-// Before waiting on the previous kernel in the stream, pull this CTA's slice
-// of W_base (and its sign rows) towards L2: weights stream from HBM while the
-// previous kernel drains, and the main loop then reads them from L2.
+// Before waiting on the previous kernel in the stream, the register kernel
+// pulls the first kPrefetchCols columns of its W_base rows (and the first
+// line of each sign row) towards L2, so that its first loads, which it can
+// only keep two super-chunks deep, hit L2.  Only a bounded head of the slice:
+// prefetching whole slices (measured first) put the resident CTAs' slices
+// beyond L2 on large layers (8192 x 28672: 917 KB per CTA) and took both
+// decode kernels from 5.4-6.0 TB/s to 3.8-4.7 TB/s on 57344 x 8192 and
+// 8192 x 28672; with the head only, the register kernel at 16 rows runs
+// 4.9 TB/s there (3.9 without any prefetch), and the cp.async ring kernel
+// is fastest with none at all.  L2 is the point of coherence, so a
+// prefetch before griddep_wait cannot return stale data.
+constexpr int64_t kPrefetchCols = 1024;
 template <int NG>
 __device__ __forceinline__ void prefetch_weights(const GemvArgs& p) {
   const int64_t rows = 8 * NG;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * rows;
   const int64_t n_rows = p.d_out - n0 < rows ? p.d_out - n0 : rows;
-  const int64_t row_lines = (p.d_in * 2 + 127) / 128;
+  const int64_t cols = p.d_in < kPrefetchCols ? p.d_in : kPrefetchCols;
+  const int64_t row_lines = (cols * 2 + 127) / 128;
   for (int64_t i = threadIdx.x; i < n_rows * row_lines; i += blockDim.x) {
     const int64_t r = i / row_lines, l = i - r * row_lines;
     prefetch_l2(reinterpret_cast<const uint8_t*>(p.w + (n0 + r) * p.d_in) + 128 * l);
   }
-  const int64_t sign_bytes = n_rows * (p.d_in / 8);
-  const uint8_t* s0 = p.packed + n0 * (p.d_in / 8);
-  for (int64_t i = threadIdx.x * 128; i < sign_bytes; i += blockDim.x * 128) prefetch_l2(s0 + i);
+  for (int64_t r = threadIdx.x; r < n_rows; r += blockDim.x)
+    prefetch_l2(p.packed + (n0 + r) * (p.d_in / 8));
 }
 
 template <int NG, bool kM16, bool kSignVec>
@@ -768,13 +777,13 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
 }
 
 // Single variant through the deep cp.async queue (d_in % 128 == 0, aligned
-// sign rows); same grid, prefetch and dependent-launch protocol as above.
+// sign rows); same grid and dependent-launch protocol as above, no prefetch
+// (its ring keeps three super-chunks per warp in flight from the start).
 template <int NG, bool kM16>
 __global__ void __launch_bounds__(kKW * 32) gemv_single_async_kernel(GemvArgs p) {
   extern __shared__ __align__(16) uint8_t ring[];
   __shared__ float red[kKW * NG * 4 * 32];
   __shared__ RowGroup grp;
-  if (blockIdx.y == 0) prefetch_weights<NG>(p);
   griddep_launch_dependents();
   griddep_wait();
   const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
@@ -1117,6 +1126,7 @@ cudaError_t launch_single(const GemvArgs& p, bool sign_vec, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const size_t smem = m16 ? gemv_ring_bytes<2>() : gemv_ring_bytes<1>();
+    std::lock_guard<std::mutex> lock(host_cache_mutex());
     if (!attr_set[dev][m16 ? 1 : 0]) {
       e = cudaFuncSetAttribute(m16 ? gemv_single_async_kernel<NG, true>
                                    : gemv_single_async_kernel<NG, false>,
@@ -1157,11 +1167,15 @@ cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem > 48 * 1024 && smem > smem_set[dev]) {
-    e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    smem_set[dev] = smem;
+  {
+    std::lock_guard<std::mutex> lock(host_cache_mutex());
+    if (smem > 48 * 1024 && smem > smem_set[dev]) {
+      e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      smem_set[dev] = smem;
+    }
   }
   return launch_pdl(gemv_grouped_kernel<kNG, NT>, grid, dim3(kKW * 32), smem, stream, p,
                     ring_off);

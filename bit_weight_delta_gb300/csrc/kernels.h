@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -38,6 +39,10 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
 
 // Current device's error word, wait limit and SM count (a bd_status code).
 int current_device_context(DevCtx* ctx, int* num_sms);
+
+// Guards the per-device launch caches (kernel attributes raised once per
+// device, occupancy results): host threads may launch on one device at once.
+std::mutex& host_cache_mutex();
 
 cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out,
                             int64_t d_in, bool per_row, uint8_t* packed, float* alpha,
@@ -89,12 +94,7 @@ struct GemmArgs {
 };
 
 constexpr int kGemmMaxSegs = 1024;
-int gemm_block_rows();    // d_out rows per tile
-int gemm_block_tokens();  // x rows per tile
-int gemm_block_k();       // K per stage: 32 (64-byte swizzle) or 64 (128-byte swizzle)
-// grid: persistent CTAs (at most one per SM; each loops over tiles).
-cudaError_t launch_gemm(const GemmArgs& p, const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
-                        int grid, cudaStream_t stream);
+int gemm_block_rows();    // d_out rows per CTA of a pair tile (128)
 
 // Prefill-size linear on CTA pairs (tcgen05 cta_group::2): tiles of
 // 2 * gemm_block_rows() output rows x gemm_pair_tokens(wide) tokens (256, or

@@ -767,6 +767,7 @@ struct MsRunner {
     static int occ_dev[64] = {};  // per device: the attribute is per context
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    std::lock_guard<std::mutex> lock(host_cache_mutex());
     int& occ = occ_dev[dev];
     if (occ == 0) {
       const size_t smem = mul_smem_bytes<RP, kT>();
@@ -914,11 +915,14 @@ struct MsRunner {
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!merge_attr[dev]) {
-      if ((e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kMergeSmem))) != cudaSuccess)
-        return e;
-      merge_attr[dev] = true;
+    {
+      std::lock_guard<std::mutex> lock(host_cache_mutex());
+      if (!merge_attr[dev]) {
+        if ((e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kMergeSmem))) != cudaSuccess)
+          return e;
+        merge_attr[dev] = true;
+      }
     }
     const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
                     static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));

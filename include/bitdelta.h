@@ -37,6 +37,11 @@
  *   - Device-side faults that cannot be seen on the host (a wait that ran out
  *     of time, a variant id out of range in device memory) set a sticky error
  *     word that bitdelta_check_error() reports.
+ *   - The library caches, per device, the device addresses of its own
+ *     device arrays (the error word, the scratch array of
+ *     bitdelta_compress_noalloc) at the first call on that device.  Do not
+ *     use it across a device reset (cudaDeviceReset, or a teardown of the
+ *     primary context): those addresses would then be stale.
  */
 #ifndef BITDELTA_H_
 #define BITDELTA_H_
@@ -128,6 +133,13 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
  *                 segment longer than 16 rows takes the tensor-core kernel).
  * A malformed table found on the device sets BD_ERR_DEVICE_BOUNDS (see
  * bitdelta_check_error) and leaves the affected rows of y unspecified.
+ * Limits: the rows that run on the decode kernel (segments of at most 16 rows
+ * when max_seg_len > 16, else every row; the host bounds them by
+ * min(M_total, 16·n_seg)) are listed in its shared memory, 4 bytes each next
+ * to 8 bytes per variant slot, within 200 KB: a bound above
+ * 51200 − 2·(n_var + 2) rows returns BD_ERR_UNSUPPORTED_SHAPE before any
+ * launch.  A table of more than 1024 segments runs the tensor-core kernel
+ * once per slice of 1024 segments.
  */
 bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int32_t* seg_offsets,
                                   const int32_t* seg_variant, int32_t n_seg, int32_t max_seg_len,
@@ -151,7 +163,9 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
  *     BD_ALPHA_PER_MATRIX mode; larger d_out returns BD_ERR_WORKSPACE and
  *     launches nothing.  Per-row α needs no scratch and has no such limit.
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current and keeps it until the process exits; make that first
+ *     call before any stream capture, and do not call it across a device
+ *     reset (the kept address would be stale).
  *   - Every call on a device shares the one array and it keeps the last call's
  *     contents (the call clears its completion counter itself): calls that can
  *     overlap on the GPU (different streams without ordering) race and give

@@ -168,3 +168,50 @@ def test_grouped_unaligned_sign_rows_take_the_register_pass():
     assert bd.bitdelta_check_error() == 0
     ref = oracle.linear_grouped(x, off, var, wb, packs, alphas, True)
     assert_linear_close(bf16_values(y), ref)
+
+
+def test_grouped_more_segments_than_one_tensor_core_launch():
+    """1100 segments: the tensor-core kernel holds 1024 in shared memory, so
+    the long segments run in two launches (segments 0-1023, 1024-1099), with
+    long segments in both slices and short rows between them; every long
+    segment is checked at its first, middle and last row, every short row
+    whole."""
+    n_seg = 1100
+    rng = np.random.default_rng(61)
+    lengths = [1 + int(rng.integers(0, 3)) for _ in range(n_seg)]
+    for s in (5, 700, 1023, 1024, 1050, 1099):
+        lengths[s] = 40 + s % 7
+    wb, packs, alphas, off, var, x = _setup(61, 256, 256, 3, lengths)
+    y = _run(wb, packs, alphas, off, var, x, True)
+    rows = []
+    for s in range(n_seg):
+        a, b = int(off[s]), int(off[s + 1])
+        rows.extend([a, (a + b) // 2, b - 1] if b - a > 16 else range(a, b))
+    rows = np.array(sorted(set(rows)))
+    seg_of = np.searchsorted(off, rows, side="right") - 1
+    sub_off = np.arange(len(rows) + 1, dtype=np.int32)
+    ref = oracle.linear_grouped(x[rows], sub_off, var[seg_of].astype(np.int32), wb, packs,
+                                alphas, True)
+    for k, r in enumerate(rows):
+        assert_linear_close(y[r], ref[k], f"row {r} (segment {seg_of[k]})")
+
+
+def test_grouped_short_row_list_limit_refused_before_any_launch():
+    """More decode-kernel rows than its shared-memory row list holds: the call
+    returns BD_ERR_UNSUPPORTED_SHAPE before launching anything (y keeps its
+    contents, the error word stays clear)."""
+    n_seg, seg_len, d_out, d_in = 3300, 16, 8, 128
+    off = np.arange(n_seg + 1, dtype=np.int32) * seg_len
+    var = np.zeros(n_seg, np.int32)
+    M = int(off[-1])
+    x = torch.zeros((M, d_in), dtype=torch.bfloat16, device="cuda")
+    wb = torch.zeros((d_out, d_in), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((M, d_out), 7.0, dtype=torch.bfloat16, device="cuda")
+    pt, at = bd.variant_tables([], [], "cuda")
+    with pytest.raises(bd.BitDeltaError) as err:
+        bd.bitdelta_linear_grouped(x, to_dev(off), to_dev(var), wb, pt, at, n_var=0,
+                                   max_seg_len=seg_len, per_row=True, out=y)
+    assert err.value.code == 2   # BD_ERR_UNSUPPORTED_SHAPE
+    torch.cuda.synchronize()
+    assert bd.bitdelta_check_error() == 0
+    assert bool((y == 7.0).all())

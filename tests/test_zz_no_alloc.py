@@ -5,7 +5,9 @@ or a serving loop whose device memory is planned up front), through the C ABI.
 Its output must match bitdelta_compress, the entry point that takes a caller
 workspace: packed signs bit for bit, α within 1e-6 relative, on two calls in a
 row (the second call reuses the library's fixed scratch array, which must not
-carry the first call's state into the result).  This file is collected last.
+carry the first call's state into the result).  At the scratch array's row
+limit it is also checked against the oracle directly.  This file is
+collected last.
 """
 import ctypes
 
@@ -14,7 +16,9 @@ import pytest
 import torch
 
 import bit_weight_delta_gb300 as bd
+import oracle
 import synth.device as sd
+from gpu_util import from_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -59,3 +63,22 @@ def test_noalloc_rejects_rows_beyond_the_scratch():
     packed = torch.empty((65537, 1), dtype=torch.uint8, device="cuda")
     alpha = torch.empty((1,), dtype=torch.float32, device="cuda")
     assert _noalloc(lib, wb, wb, False, packed, alpha) == 4   # BD_ERR_WORKSPACE
+
+
+def test_noalloc_at_the_row_limit_matches_the_oracle():
+    """65536 rows, per-matrix α (the largest problem the scratch array takes),
+    two calls in a row on different inputs: signs bit for bit and α within
+    1e-6 of the oracle's fp64 mean |Δ| ("Mathematical foundation")."""
+    lib = bd.load()
+    torch.cuda.set_device(0)
+    d_out, d_in = 65536, 256
+    for call in range(2):
+        wb, wf = sd.layer(50 + call, d_out, d_in, stream=call)
+        packed = torch.full((d_out, d_in // 8), 0x5A, dtype=torch.uint8, device="cuda")
+        alpha = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+        assert _noalloc(lib, wb, wf, False, packed, alpha) == 0
+        assert bd.bitdelta_check_error() == 0
+        p_ref, _, a64 = oracle.compress(from_dev_bf16(wb), from_dev_bf16(wf), False)
+        assert np.array_equal(packed.cpu().numpy(), p_ref), f"call {call}: packed signs differ"
+        a = float(alpha.double().item())
+        assert abs(a - a64[0]) <= ALPHA_RTOL * abs(a64[0]), f"call {call}: alpha {a} vs {a64[0]}"
