@@ -63,10 +63,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// bf16x2 of ±1 for sign bits (2i, 2i+1) of `byte`: bit 1 -> +1.0 (0x3F80),
-// bit 0 -> −1.0 (0xBF80); column 2i in the low half.
+// bf16x2 of ±1 for sign bits (2i, 2i+1) of `byte` (< 256): bit 1 -> +1.0
+// (0x3F80), bit 0 -> −1.0 (0xBF80); column 2i in the low half.  One multiply
+// and one logic op: byte·(0x40008000 >> 2i) puts bit 2i at bit 15 and bit
+// 2i+1 at bit 31, and its two partial products (bits 9..22 and 24..37 at
+// most) never overlap, so no carry reaches either bit.
 __device__ __forceinline__ uint32_t pm_one_pair(uint32_t byte, int i) {
-  return (((byte >> (2 * i)) * 0x40008000u) & 0x80008000u) ^ 0xBF80BF80u;
+  return ((byte * (0x40008000u >> (2 * i))) & 0x80008000u) ^ 0xBF80BF80u;
 }
 
 // One 32-column chunk for NG groups of 8 W rows: base and sign products.
