@@ -187,6 +187,116 @@ def bf16_bits_host(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def graph_ms(fn, reps: int = 5) -> float:
+    """Median device time (ms) of one replay of `fn` captured as a CUDA graph."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    del g
+    return statistics.median(times)
+
+
+def eager_us(fn, reps: int = 200) -> float:
+    """Mean wall time of one eager call (launch latency included), in us."""
+    for _ in range(10):
+        fn()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) / reps * 1e6
+
+
+def hbm_roofline(gbs: float, peaks: dict, traffic=None) -> dict:
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peaks["source"]}
+
+
+def tensor_roofline(tflops: float, peaks: dict, key: str = "bf16_tflops") -> dict:
+    return {"bound": "tensor", "achieved": tflops, "peak": peaks[key], "unit": "TFLOP/s",
+            "frac": tflops / peaks[key], "traffic": None, "peak_source": peaks["source"]}
+
+
+def host_cores() -> int:
+    return os.cpu_count() or 1
+
+
+class Tiny:
+    """The tiny single layer (seed 0): W_base bf16 [256, 512] ~ N(0, 0.02),
+    Δ ~ Laplace(0, 1e-3), compress with α per matrix and per row, then the
+    fused linear on x [4, 512]; and the 8x16 case with |Δ| = 2^-10 whose
+    reconstruction is exact.  Launch-bound: reported as latency per call."""
+
+    name = "tiny_256x512_M4_alpha_per_matrix_and_per_row_plus_8x16_exact"
+
+    def __init__(self, bd):
+        import synth
+        self.bd = bd
+        self.wb_h, self.wf_h = synth.layer(0, 256, 512)
+        self.x_h = synth.activations(0, 4, 512)
+        self.cb_h, self.cf_h, _ = synth.constant_magnitude_case(0)
+        dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)
+        self.wb, self.wf, self.x = dev(self.wb_h), dev(self.wf_h), dev(self.x_h)
+        self.cb, self.cf = dev(self.cb_h), dev(self.cf_h)
+
+    def report(self):
+        bd = self.bd
+        out = {"workload": self.name}
+        for per_row in (False, True):
+            tag = "alpha_per_row" if per_row else "alpha_per_matrix"
+            packed, alpha = bd.bitdelta_compress(self.wb, self.wf, per_row=per_row)
+            ws = torch.empty(max(bd.bitdelta_compress_workspace_bytes(256, 512, per_row), 1),
+                             dtype=torch.uint8, device="cuda")
+            y = torch.empty((4, 256), dtype=torch.bfloat16, device="cuda")
+            out[f"compress_{tag}_us"] = eager_us(lambda: bd.bitdelta_compress(
+                self.wb, self.wf, per_row=per_row, packed_out=packed, alpha_out=alpha,
+                workspace=ws))
+            out[f"linear_{tag}_us"] = eager_us(lambda: bd.bitdelta_linear(
+                self.x, self.wb, packed, alpha, per_row=per_row, out=y))
+        cp, ca = bd.bitdelta_compress(self.cb, self.cf, per_row=True)
+        w8 = torch.empty_like(self.cb)
+        out["exact_8x16_compress_plus_reconstruct_us"] = eager_us(
+            lambda: (bd.bitdelta_compress(self.cb, self.cf, per_row=True, packed_out=cp,
+                                          alpha_out=ca),
+                     bd.bitdelta_reconstruct(self.cb, cp, ca, per_row=True, out=w8)))
+        out["note"] = ("eager calls from Python through the C ABI, launch latency included "
+                       "(wall time per call, synchronised once per 200 calls)")
+        return out
+
+    def oracle_sample(self):
+        import oracle
+        t = {}
+        for per_row in (False, True):
+            tag = "alpha_per_row" if per_row else "alpha_per_matrix"
+            t0 = time.perf_counter()
+            for _ in range(20):
+                p_, a_, _ = oracle.compress(self.wb_h, self.wf_h, per_row)
+            t[f"compress_{tag}_us"] = (time.perf_counter() - t0) / 20 * 1e6
+            t0 = time.perf_counter()
+            for _ in range(20):
+                oracle.linear(self.x_h, self.wb_h, p_, a_, per_row)
+            t[f"linear_{tag}_us"] = (time.perf_counter() - t0) / 20 * 1e6
+        return {"value": t["linear_alpha_per_row_us"], "unit": "us per linear call",
+                "cores": 1, "kind": "oracle", "per_call_us": t,
+                "sample": "the whole tiny workload, 20 calls of each, 1 host core of "
+                          f"{host_cores()}"}
+
+
 class DecodeStack:
     """Decode sweep on 4096x4096 layers (alpha per row), 32 distinct layers."""
 
@@ -239,6 +349,23 @@ class DecodeStack:
 
     def dominant(self):
         return [p for p in self.phases if p.startswith("linear")]
+
+    def unfused_timing(self):
+        """The unfused reference on the same 32-layer stack: bitdelta_reconstruct
+        of W_eff to memory, then cuBLAS bf16 x·W_effᵀ, per layer and M.  Rates
+        are the fused op's algorithmic bytes over the unfused time."""
+        bd = self.bd
+        out = {}
+        for M in self.Ms:
+            def f():
+                for (wb, wf, packed, alpha) in self.layers:
+                    bd.bitdelta_reconstruct(wb, packed, alpha, per_row=True, out=self.w_eff)
+                    torch.matmul(self.x[:M], self.w_eff.T, out=self.y[M])
+            ms = graph_ms(f)
+            us = ms * 1e3 / self.L
+            out[f"M{M}"] = {"us_per_layer": us,
+                            "GB/s_of_fused_bytes": self.bytes[f"linear_M{M}"] / (us * 1e-6) / 1e9}
+        return out
 
     # ---------------------------------------------------------------- oracle
 
@@ -302,6 +429,28 @@ class Prefill:
         wb, packed, alpha = self.mats[phase]
         self.bd.bitdelta_linear(self.x[d_in], wb, packed, alpha, per_row=True,
                                 out=self.y[phase])
+
+    def oracle_sample(self):
+        """The oracle on 16 of the 2048 tokens through the O projection
+        (8192 -> 8192): compression untimed, the linear timed; the FLOP rate
+        extrapolates to the whole step (labelled so)."""
+        import oracle
+        import synth.device as sd
+        nm, d_out, d_in = self.shapes[1]
+        wb, wf = sd.layer(3, d_out, d_in, stream=1)
+        wb_h, wf_h = bf16_bits_host(wb), bf16_bits_host(wf)
+        del wb, wf
+        x_h = bf16_bits_host(self.x[d_in][:16])
+        packed, alpha, _ = oracle.compress(wb_h, wf_h, True)
+        t0 = time.perf_counter()
+        oracle.linear(x_h, wb_h, packed, alpha, True)
+        dt = time.perf_counter() - t0
+        tflops = 2.0 * 16 * d_out * d_in / dt / 1e12
+        return {"value": tflops, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "extrapolated_ms_per_step": self.flops_per_step() / (tflops * 1e12) * 1e3,
+                "sample": f"16 of {self.M} tokens through the O projection ({d_in}->{d_out}), "
+                          f"{dt:.1f} s on 1 host core of {host_cores()}; the step time is "
+                          "extrapolated from that FLOP rate"}
 
     def cublas_reference(self, reps=5):
         """cuBLAS bf16 GEMM x·W_baseᵀ, and reconstruct-to-HBM + cuBLAS (unfused)."""
@@ -400,6 +549,78 @@ class Grouped:
 
     def launches_per_step(self):
         return 2 * self.sets   # tensor-core kernel + decode kernel per call
+
+    def unfused_timing(self):
+        """The unfused reference for one call on copy 0: for each variant in
+        the batch, bitdelta_reconstruct of its W_eff to memory, then cuBLAS
+        bf16 products of that variant's rows (gathered, multiplied,
+        scattered); base rows multiply W_base directly."""
+        bd = self.bd
+        wb, packs, alphas, _, _ = self.copies[0]
+        off = self.off.cpu().numpy()
+        rows_of = {}
+        for s_, v in enumerate(self.var_host):
+            rows_of.setdefault(int(v), []).extend(range(int(off[s_]), int(off[s_ + 1])))
+        idx = {v: torch.tensor(r, dtype=torch.int64, device="cuda") for v, r in rows_of.items()}
+        w_eff = torch.empty_like(wb)
+        y = torch.empty_like(self.y)
+
+        def f():
+            for v, ix in idx.items():
+                w = wb
+                if v > 0:
+                    bd.bitdelta_reconstruct(wb, packs[v - 1], alphas[v - 1], per_row=True,
+                                            out=w_eff)
+                    w = w_eff
+                y.index_copy_(0, ix, torch.matmul(self.x.index_select(0, ix), w.T))
+        ms = graph_ms(f)
+        return {"ms_per_call": ms, "TFLOP/s": self.flops / (ms * 1e-3) / 1e12,
+                "variants_reconstructed": len([v for v in idx if v > 0])}
+
+    def oracle_sample(self):
+        """The oracle on 16 rows of one call (8 of the one-row decode segments
+        and 2 rows of each 512-row segment, each as a one-row segment of its
+        variant); compression of the variants involved untimed.  Rows/s
+        extrapolate to the whole call (labelled so)."""
+        import oracle
+        import synth
+        import synth.device as sd
+        wb = self.copies[0][0]
+        wb_h = bf16_bits_host(wb)
+        off = self.off.cpu().numpy()
+        rows, n_decode = [], 0
+        for s_ in range(len(self.var_host)):
+            a, b = int(off[s_]), int(off[s_ + 1])
+            if b - a == 1 and n_decode < 8:
+                rows.append(a)
+                n_decode += 1
+            elif b - a > 1:
+                rows.extend([a, b - 1])
+        rows = np.array(sorted(rows))
+        seg_of = np.searchsorted(off, rows, side="right") - 1
+        var = self.var_host[seg_of].astype(np.int32)
+        scales = synth.variant_scales(4, self.n_var)
+        packs, alphas = [], []
+        for v in range(1, self.n_var + 1):
+            if v in set(int(u) for u in var):
+                wf = sd.finetuned_bf16(wb, 4, 1000 + v - 1, float(scales[v - 1]))
+                p_, a_, _ = oracle.compress(wb_h, bf16_bits_host(wf), True)
+                del wf
+            else:   # not referenced by the sample: any table entry of the right shape
+                p_ = np.zeros((self.d_out, self.d_in // 8), np.uint8)
+                a_ = np.zeros(self.d_out, np.float32)
+            packs.append(p_)
+            alphas.append(a_)
+        x_h = bf16_bits_host(self.x[torch.from_numpy(rows).cuda()])
+        sub_off = np.arange(len(rows) + 1, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.linear_grouped(x_h, sub_off, var, wb_h, packs, alphas, True)
+        dt = time.perf_counter() - t0
+        rps = len(rows) / dt
+        return {"value": rps, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                "extrapolated_ms_per_call": self.M / rps * 1e3,
+                "sample": f"{len(rows)} of the call's {self.M} rows, {dt:.1f} s on 1 host core "
+                          f"of {host_cores()}; the call time is extrapolated from that row rate"}
 
     def run_phase(self, phase):
         c = int(phase[3:])
@@ -521,21 +742,86 @@ class Slice40:
             total += s.elapsed_time(e)
         return total
 
-    def report(self):
+    def run_decode_unfused(self, w_eff):
+        """The unfused reference of the decode step: per projection, each
+        variant's W_eff reconstructed to memory, then cuBLAS bf16 products of
+        that variant's rows."""
+        rows = {v: torch.tensor([r for r in range(self.decode_M) if 1 + r % 2 == v],
+                                dtype=torch.int64, device="cuda") for v in (1, 2)}
+        for mats in self.layers:
+            for nm, d_out, d_in in self.shapes:
+                wb, var, _, _ = mats[nm]
+                w = w_eff[:d_out * d_in].view(d_out, d_in)
+                for v in (1, 2):
+                    self.bd.bitdelta_reconstruct(wb, var[v - 1][0], var[v - 1][1], per_row=True,
+                                                 out=w)
+                    self.yd[nm].index_copy_(0, rows[v], torch.matmul(
+                        self.xd[d_in].index_select(0, rows[v]), w.T))
+
+    def oracle_sample(self):
+        """The oracle on the O projection (8192 -> 8192) of layer 0: the third
+        variant's compression, the decode batch (8 rows alternating variants
+        1 and 2, their compression untimed) and 4 of the 512 prefill tokens of
+        variant 1, each timed on 1 host core; per-leg rates over the same
+        algorithmic bytes or FLOPs as the GPU legs."""
+        import oracle
+        import synth.device as sd
+        proj = 1
+        nm, d_out, d_in = self.shapes[proj]
+        wb = self.layers[0][nm][0]
+        wb_h = bf16_bits_host(wb)
+        fts = {v: bf16_bits_host(sd.slice_finetuned(wb, 0, proj, v, self.seed)) for v in (1, 2, 3)}
+        n = d_out * d_in
+        t0 = time.perf_counter()
+        oracle.compress(wb_h, fts[3], True)
+        t_comp = time.perf_counter() - t0
+        comp = {v: oracle.compress(wb_h, fts[v], True) for v in (1, 2)}
+        xd = bf16_bits_host(self.xd[d_in])
+        off = np.arange(self.decode_M + 1, dtype=np.int32)
+        var = np.array([1 + r % 2 for r in range(self.decode_M)], np.int32)
+        t0 = time.perf_counter()
+        oracle.linear_grouped(xd, off, var, wb_h, [comp[1][0], comp[2][0]],
+                              [comp[1][1], comp[2][1]], True)
+        t_dec = time.perf_counter() - t0
+        xp = bf16_bits_host(self.xp[d_in][:4])
+        t0 = time.perf_counter()
+        oracle.linear(xp, wb_h, comp[1][0], comp[1][1], True)
+        t_pre = time.perf_counter() - t0
+        dec_bytes = 2 * n + 2 * (n / 8 + 4 * d_out) + 2 * self.decode_M * (d_in + d_out)
+        return {"value": dec_bytes / t_dec / 1e9, "unit": "GB/s (decode leg)", "cores": 1,
+                "kind": "oracle",
+                "compress_GB/s": (4 * n + n / 8 + 4 * d_out) / t_comp / 1e9,
+                "prefill_TFLOP/s": 2.0 * 4 * n / t_pre / 1e12,
+                "sample": f"the O projection ({d_in}->{d_out}) of layer 0: compression of the "
+                          f"third variant ({t_comp:.1f} s), the 8-row decode batch "
+                          f"({t_dec:.1f} s), 4 of 512 prefill tokens ({t_pre:.1f} s), on 1 "
+                          f"host core of {host_cores()}"}
+
+    def report(self, peaks, cpu: bool = True):
         pre = self.timed(self.run_prefill)
         dec = self.timed(self.run_decode)
         comp = self.compress_ms()
+        pre_tf = self.prefill_flops / (pre * 1e-3) / 1e12
+        dec_gbs = self.decode_bytes / (dec * 1e-3) / 1e9
+        comp_gbs = self.compress_bytes / (comp * 1e-3) / 1e9
+        w_eff = torch.empty(max(d_out * d_in for _, d_out, d_in in self.shapes),
+                            dtype=torch.bfloat16, device="cuda")
+        dec_unfused = self.timed(lambda: self.run_decode_unfused(w_eff), reps=2)
+        del w_eff
         return {
             "workload": self.name,
-            "prefill": {"ms": pre, "TFLOP/s": self.prefill_flops / (pre * 1e-3) / 1e12,
-                        "tokens": self.prefill_M, "launches": 4 * self.L},
-            "decode": {"ms_per_step": dec, "GB/s": self.decode_bytes / (dec * 1e-3) / 1e9,
+            "prefill": {"ms": pre, "TFLOP/s": pre_tf, "tokens": self.prefill_M,
+                        "launches": 4 * self.L,
+                        "roofline": tensor_roofline(pre_tf, peaks, "bf16_tflops_sustained")},
+            "decode": {"ms_per_step": dec, "GB/s": dec_gbs,
                        "batch": self.decode_M, "variants": "rows alternate 1,2,1,2,...",
-                       "launches": 4 * self.L},
-            "compress": {"ms": comp, "GB/s": self.compress_bytes / (comp * 1e-3) / 1e9,
-                         "ms_per_layer": comp / self.L},
+                       "launches": 4 * self.L, "roofline": hbm_roofline(dec_gbs, peaks),
+                       "unfused_reconstruct_plus_cublas_ms_per_step": dec_unfused},
+            "compress": {"ms": comp, "GB/s": comp_gbs, "ms_per_layer": comp / self.L,
+                         "roofline": hbm_roofline(comp_gbs, peaks)},
             "resident_weights_gb": (2 * self.weights_per_layer * self.L
                                     + 2 * self.L * (self.weights_per_layer / 8)) / 1e9,
+            "cpu_baseline": self.oracle_sample() if cpu else None,
         }
 
 
@@ -1032,6 +1318,8 @@ def main():
     ap.add_argument("--workloads", default="all", help="comma list: prefill,grouped or all|none")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true",
+                    help="skip the per-workload oracle samples (cpu_baseline of each workload)")
     ap.add_argument("--profile", default=None,
                     help="decode|compress|reconstruct|prefill|grouped|kmerge|monosoup: "
                          "a few eager launches for ncu")
@@ -1073,11 +1361,20 @@ def main():
                       / peaks["hbm_gbs"]}
                   for p in dec.phases}
 
+    decode_unfused = dec.unfused_timing()
+
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"prefill", "grouped", "slice40", "cache", "kmerge", "monosoup"}
+        {"tiny", "prefill", "grouped", "slice40", "cache", "kmerge", "monosoup"}
         if args.workloads == "all"
         else set())
+    cpu_on = rank == 0 and not args.no_cpu
+    if "tiny" in wanted:
+        tw = Tiny(bd)
+        workloads["tiny"] = tw.report()
+        if cpu_on:
+            workloads["tiny"]["cpu_baseline"] = tw.oracle_sample()
+        del tw
     if "prefill" in wanted:
         pre = Prefill(bd)
         pms, pph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
@@ -1095,6 +1392,8 @@ def main():
             "fused_vs_unfused_by_tokens": ref["fused_vs_unfused_by_tokens"],
             "frac_of_cublas": ref["cublas_plain"]["ms_per_step"] / pms,
         }
+        if cpu_on:
+            workloads["prefill"]["cpu_baseline"] = pre.oracle_sample()
         del pre
         torch.cuda.empty_cache()
     if "grouped" in wanted:
@@ -1110,12 +1409,15 @@ def main():
                          "unit": "TFLOP/s", "frac": tfl / peaks["bf16_tflops"],
                          "roofline_time_ms": t_roof * 1e3,
                          "frac_of_roofline_time": t_roof * 1e3 / per_call, "traffic": None},
+            "unfused_reconstruct_plus_cublas": grp.unfused_timing(),
         }
+        if cpu_on:
+            workloads["grouped"]["cpu_baseline"] = grp.oracle_sample()
         del grp
         torch.cuda.empty_cache()
     if "slice40" in wanted:
         sl = Slice40(bd)
-        workloads["slice40"] = sl.report()
+        workloads["slice40"] = sl.report(peaks, cpu=cpu_on)
         del sl
         torch.cuda.empty_cache()
     if "kmerge" in wanted:
@@ -1161,6 +1463,7 @@ def main():
                                    "gemv_single_kernel (M=16)",
                          "peak_source": peaks["source"]},
             "per_kernel": per_kernel,
+            "decode_unfused_reconstruct_plus_cublas": decode_unfused,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": dec.launches_per_step() * args.steps,
