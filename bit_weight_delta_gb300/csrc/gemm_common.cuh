@@ -239,9 +239,19 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem_addr, uint32
 // Arrive on an mbarrier given by cluster address (possibly the other CTA's),
 // with the instruction's default ordering.  A release at cluster scope here
 // put a full memory barrier on every transform stage (ncu: 22% of the pair
-// kernel's warp samples stalled on it); what the consumer needs from these
-// arrivals is ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync
-// (tensor memory) and by the arriving thread's own acquire of the TMA barrier.
+// kernel's warp samples stalled on it on 256-token tiles; on the 512-token
+// tiles' rank-1 arrivals alone it cost 45% of their throughput).  What the
+// MMA needs from these arrivals stays on the arriving CTA's own SM: in a
+// cta_group::2 MMA each CTA's tensor core reads that CTA's A rows (its W_eff),
+// so rank 1's transform output is read by rank 1's tensor core.  On the
+// 256-token tile that output is in rank 1's tensor memory, ordered before the
+// arrival by tcgen05.wait::st and tcgen05.fence::before_thread_sync; on the
+// 512-token tile it is in rank 1's shared memory, ordered by each writing
+// thread's fence.proxy.async.shared::cta and the warp barrier before lane 0
+// arrives.  The MMA that reads it is issued only after rank 0 has observed
+// the arrival, so no read can start before those fences.  The bit-for-bit
+// equality of the two tile widths on the same problem (a GPU test) is the
+// measured side of that argument.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
