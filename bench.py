@@ -48,7 +48,7 @@ METRIC = "bitdelta_linear TFLOP/s (prefill) & GB/s (decode) as % of GB300 roofli
 # capture of `python bench.py --profile decode` (dram__bytes_read.sum +
 # dram__bytes_write.sum of gemv_single_async_kernel).  Valid for the kernel
 # build that capture was taken on; None whenever that kernel has changed since.
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 35_750_912
 
 # --------------------------------------------------------------------------- peaks
 
@@ -1288,6 +1288,25 @@ def run_profile(kind: str, prefill_tile: str = "auto"):
         grp = Grouped(bd)
         for i in range(4):
             grp.run_phase(f"set{i % grp.sets}")
+    elif kind == "slice_decode":
+        # the 40-layer slice's decode instance on its largest projection
+        # (gate+up, 8192 -> 57344): 8 rows alternating two variants through
+        # the grouped linear, and the single-variant decode of the same rows
+        wb = sd.slice_base(0, 2)
+        var = []
+        for v in (1, 2):
+            wf = sd.slice_finetuned(wb, 0, 2, v)
+            var.append(bd.bitdelta_compress(wb, wf, per_row=True))
+            del wf
+        pt, at = bd.variant_tables([var[0][0], var[1][0]], [var[0][1], var[1][1]], "cuda")
+        x = sd.slice_inputs(wb.shape[1], 8, True)
+        off = torch.arange(9, dtype=torch.int32, device="cuda")
+        seg_var = torch.tensor([1 + r % 2 for r in range(8)], dtype=torch.int32, device="cuda")
+        y = torch.empty((8, wb.shape[0]), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            bd.bitdelta_linear_grouped(x, off, seg_var, wb, pt, at, n_var=2, max_seg_len=1,
+                                       per_row=True, out=y)
+            bd.bitdelta_linear(x, wb, var[0][0], var[0][1], per_row=True, out=y)
     elif kind == "kmerge":
         km = KMergeSimilarity(bd)
         n_b = km.n_var - 1
@@ -1321,8 +1340,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the per-workload oracle samples (cpu_baseline of each workload)")
     ap.add_argument("--profile", default=None,
-                    help="decode|compress|reconstruct|prefill|grouped|kmerge|monosoup: "
-                         "a few eager launches for ncu")
+                    help="decode|compress|reconstruct|prefill|grouped|slice_decode|kmerge|"
+                         "monosoup: a few eager launches for ncu")
     ap.add_argument("--prefill-tile", default="auto", choices=["auto", "256", "512"],
                     help="token width of the tensor-core kernel's pair tiles (profile runs)")
     args = ap.parse_args()
