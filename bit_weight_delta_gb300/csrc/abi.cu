@@ -381,7 +381,7 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
   a.packed_table = packed_table;
   a.alpha_table = alpha_table;
   a.ctx = ctx;
-  return from_cuda(bd::launch_gemv_grouped(a, use_tc ? short_rows_bound : M_total, s));
+  return from_cuda(bd::launch_gemv_grouped(a, use_tc ? short_rows_bound : M_total, dev->num_sms, s));
 }
 
 bd_status bitdelta_check_error(bd_stream_t stream) {

@@ -806,28 +806,31 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_async_kernel(GemvArgs p)
 // gemv_group_async), the W rows are the MMA's A operand and NT tiles of 8
 // tokens its B operand.  Each variant's sign product runs over all the
 // group's tokens; a token reads only its own variant's accumulator, so no
-// masking is needed.  Requires d_in % 128 == 0 and 16-byte aligned sign rows
-// for every variant of the group.
-template <int NT>
+// masking is needed.  Groups hold at most V delta variants (2 when the call
+// has no more, else 4).  Requires d_in % 128 == 0; a variant table entry off
+// a 16-byte boundary has its sign words fetched with plain loads.
+template <int NT, int V>
 __host__ __device__ constexpr int mixed_stage_bytes() {
-  return kStageRows * 256 + kMaxGroupVars * kStageRows * 16 + NT * 8 * 256;
+  return kStageRows * 256 + V * kStageRows * 16 + NT * 8 * 256;
 }
-template <int NT>
-__host__ __device__ constexpr int mixed_ring_stages() { return NT == 1 ? 3 : 2; }
-template <int NT>
+// Ring depth D (stages per warp): 3 while the grid's 16-row blocks fit one
+// wave at two CTAs per SM (each warp then needs two stages in flight), 2 on
+// larger grids, whose CTAs then fit four per SM: on the slice's projections
+// (8192-57344 rows, two variants) 2 stages took 4.1 -> 5.3 TB/s on 57344 x
+// 8192 and 3.0 -> 4.0 on 10240 x 8192, and 15.0 -> 16.5 µs on a 4096-row
+// layer (one wave) against 3 stages.
+template <int NT, int V, int D>
 constexpr size_t mixed_ring_bytes() {
-  return static_cast<size_t>(mixed_ring_stages<NT>()) * kKW * mixed_stage_bytes<NT>();
+  return static_cast<size_t>(D) * kKW * mixed_stage_bytes<NT, V>();
 }
 
-template <int NT>
+template <int NT, int V, int D>
 __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const MixedGroup& grp,
                                                        float* red, uint8_t* ring) {
   constexpr int CPS = kCPS;
-  constexpr int V = kMaxGroupVars;
   constexpr int R = kStageRows;  // 16 W rows
   static_assert(R == 16 && V % 2 == 0, "two 8-row halves; variants copied in pairs");
-  constexpr int D = mixed_ring_stages<NT>();
-  constexpr int kSB = mixed_stage_bytes<NT>();
+  constexpr int kSB = mixed_stage_bytes<NT, V>();
   constexpr int kSOff = R * 256;              // sign words: [variant][row] × 16 bytes
   constexpr int kXOff = R * 256 + V * R * 16; // x segments of NT·8 token rows
   const int lane = threadIdx.x & 31;
@@ -864,12 +867,14 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
   const int cr = lane >> 4, cw = lane & 15;
   const uint16_t* const wsrc0 = p.w + (n0 + cr) * d_in + 8 * cw;
   const uint8_t* ssrc[V / 2];
+  bool s_al[V / 2];  // 16-byte aligned sign row: cp.async; else plain loads
 #pragma unroll
   for (int k = 0; k < V / 2; ++k) {
     const int v = 2 * k + cr;
     ssrc[k] = (v < nv && cw < rows_here)
                   ? p.packed_table[grp.vars[v] - 1] + (n0 + cw) * row_bytes
                   : nullptr;
+    s_al[k] = (reinterpret_cast<uintptr_t>(ssrc[k]) & 15u) == 0;
   }
   const uint16_t* xsrc[4 * NT];
 #pragma unroll
@@ -889,9 +894,26 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
           cp_async_16_cg(st + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), wsrc0 + 2 * k * d_in + kc0);
       }
 #pragma unroll
-      for (int k = 0; k < V / 2; ++k)
-        if (ssrc[k] != nullptr)
-          cp_async_16_cg(st + kSOff + 16u * ((2 * k + cr) * R + cw), ssrc[k] + kc0 / 8);
+      for (int k = 0; k < V / 2; ++k) {
+        if (ssrc[k] == nullptr) continue;
+        const uint32_t dst = st + kSOff + 16u * ((2 * k + cr) * R + cw);
+        if (s_al[k]) {
+          cp_async_16_cg(dst, ssrc[k] + kc0 / 8);
+        } else {
+          // read by the other lanes after the stage's __syncwarp, like the copies
+          const uint8_t* src = ssrc[k] + kc0 / 8;
+          uint32_t wv[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            wv[b] = static_cast<uint32_t>(__ldg(src + 4 * b)) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 1)) << 8) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 2)) << 16) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 3)) << 24);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(wv[0]),
+                       "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                       : "memory");
+        }
+      }
 #pragma unroll
       for (int k = 0; k < 4 * NT; ++k) {
         const int r = 2 * k + cr;
@@ -1001,8 +1023,11 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
 // groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
 // builds the same grouping in shared memory, then covers its 8·NG output
 // columns for every group.
-template <int NG, int kAsyncNT>
-__global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p, int ring_off) {
+// One token tile with a two-stage ring: four CTAs per SM, so at most 128
+// registers per thread.
+template <int NG, int kAsyncNT, int V, int D>
+__global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
+    gemv_grouped_kernel(GemvArgs p, int ring_off) {
   __shared__ float red[kKW * NG * 4 * 32];
   extern __shared__ __align__(16) int32_t dyn[];
   griddep_launch_dependents();
@@ -1076,7 +1101,7 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p, int 
         int slot = -1;
         if (bk > 0) {
           if (nvars == 0 || mg.vars[nvars - 1] != bk) {
-            if (nvars == kMaxGroupVars) break;
+            if (nvars == V) break;
             mg.vars[nvars++] = bk;
             vec = vec && (reinterpret_cast<uintptr_t>(p.packed_table[bk - 1]) & 15u) == 0;
           }
@@ -1098,16 +1123,15 @@ __global__ void __launch_bounds__(kKW * 32) gemv_grouped_kernel(GemvArgs p, int 
     }
     __syncthreads();
     if constexpr (kAsyncNT > 0) {
-      if (mg_vec) {
-        gemv_group_mixed_async<kAsyncNT>(p, mg, red,
-                                         reinterpret_cast<uint8_t*>(dyn) + ring_off);
-        continue;
-      }
+      // the ring (d_in % 128 == 0): unaligned variant tables included
+      gemv_group_mixed_async<kAsyncNT, V, D>(p, mg, red,
+                                             reinterpret_cast<uint8_t*>(dyn) + ring_off);
+    } else {
+      if (mg_vec)
+        gemv_group_mixed<NG, true>(p, mg, red);
+      else
+        gemv_group_mixed<NG, false>(p, mg, red);
     }
-    if (mg_vec)
-      gemv_group_mixed<NG, true>(p, mg, red);
-    else
-      gemv_group_mixed<NG, false>(p, mg, red);
   }
 }
 
@@ -1160,7 +1184,7 @@ cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream) {
   return launch_single<kNG>(p, sign_vec, stream);
 }
 
-template <int NT>
+template <int NT, int V, int D>
 cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off, dim3 grid,
                                     cudaStream_t stream) {
   // Raise the dynamic shared-memory limit only when a call needs more than
@@ -1173,34 +1197,55 @@ cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off
   {
     std::lock_guard<std::mutex> lock(host_cache_mutex());
     if (smem > 48 * 1024 && smem > smem_set[dev]) {
-      e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT>,
+      e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT, V, D>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       smem_set[dev] = smem;
     }
   }
-  return launch_pdl(gemv_grouped_kernel<kNG, NT>, grid, dim3(kKW * 32), smem, stream, p,
+  return launch_pdl(gemv_grouped_kernel<kNG, NT, V, D>, grid, dim3(kKW * 32), smem, stream, p,
                     ring_off);
 }
 
-cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, cudaStream_t stream) {
+cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, int num_sms,
+                                cudaStream_t stream) {
   const size_t group_smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
   const int64_t n_blocks = (p.d_out + 8 * kNG - 1) / (8 * kNG);
   const dim3 grid(static_cast<unsigned>(n_blocks));
   // The deep-queue pass (d_in % 128 == 0) with one token tile when no group
-  // can hold more than 8 rows, else two; its ring follows the grouping lists.
+  // can hold more than 8 rows, else two; groups of at most two delta
+  // variants when the call has no more (half the ring's sign slots, fewer
+  // registers); a two-stage ring on grids of more than one wave at two CTAs
+  // per SM (see mixed_ring_bytes).  The ring follows the grouping lists.
   const size_t ring_off = (group_smem + 15) / 16 * 16;
   const size_t kMaxDyn = 200 * 1024;
+  const int ro = static_cast<int>(ring_off);
   if (p.d_in % 128 == 0) {
-    if (max_rows <= 8 && ring_off + mixed_ring_bytes<1>() <= kMaxDyn)
-      return launch_grouped_instance<1>(p, ring_off + mixed_ring_bytes<1>(),
-                                        static_cast<int>(ring_off), grid, stream);
-    if (ring_off + mixed_ring_bytes<2>() <= kMaxDyn)
-      return launch_grouped_instance<2>(p, ring_off + mixed_ring_bytes<2>(),
-                                        static_cast<int>(ring_off), grid, stream);
+    const bool two = p.n_var <= 2;
+    const bool shallow = n_blocks > 2 * static_cast<int64_t>(num_sms);
+    if (max_rows <= 8) {
+      if (two && shallow && ring_off + mixed_ring_bytes<1, 2, 2>() <= kMaxDyn)
+        return launch_grouped_instance<1, 2, 2>(p, ring_off + mixed_ring_bytes<1, 2, 2>(), ro,
+                                                grid, stream);
+      if (two && ring_off + mixed_ring_bytes<1, 2, 3>() <= kMaxDyn)
+        return launch_grouped_instance<1, 2, 3>(p, ring_off + mixed_ring_bytes<1, 2, 3>(), ro,
+                                                grid, stream);
+      if (shallow && ring_off + mixed_ring_bytes<1, 4, 2>() <= kMaxDyn)
+        return launch_grouped_instance<1, 4, 2>(p, ring_off + mixed_ring_bytes<1, 4, 2>(), ro,
+                                                grid, stream);
+      if (ring_off + mixed_ring_bytes<1, 4, 3>() <= kMaxDyn)
+        return launch_grouped_instance<1, 4, 3>(p, ring_off + mixed_ring_bytes<1, 4, 3>(), ro,
+                                                grid, stream);
+    }
+    if (two && ring_off + mixed_ring_bytes<2, 2, 2>() <= kMaxDyn)
+      return launch_grouped_instance<2, 2, 2>(p, ring_off + mixed_ring_bytes<2, 2, 2>(), ro, grid,
+                                              stream);
+    if (ring_off + mixed_ring_bytes<2, 4, 2>() <= kMaxDyn)
+      return launch_grouped_instance<2, 4, 2>(p, ring_off + mixed_ring_bytes<2, 4, 2>(), ro, grid,
+                                              stream);
   }
-  return launch_grouped_instance<0>(p, group_smem, 0, grid, stream);
+  return launch_grouped_instance<0, kMaxGroupVars, 2>(p, group_smem, 0, grid, stream);
 }
 
 }  // namespace bd
