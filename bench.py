@@ -1259,19 +1259,21 @@ def run_profile(kind: str, prefill_tile: str = "auto"):
     bd.load()
     torch.cuda.set_device(0)
     bd.bitdelta_set_prefill_tile(prefill_tile if prefill_tile == "auto" else int(prefill_tile))
-    if kind in ("decode", "compress", "reconstruct"):
+    if kind in ("decode", "decode16", "compress", "reconstruct"):
         layers = []
         for l in range(4):
             wb, wf = sd.layer(1, 4096, 4096, stream=l)
             p, a = bd.bitdelta_compress(wb, wf, per_row=True)
             layers.append((wb, wf, p, a))
         x = sd.normal_bf16((16, 4096), 1, 9999)
-        y = torch.empty((8, 4096), dtype=torch.bfloat16, device="cuda")
+        y = torch.empty((16, 4096), dtype=torch.bfloat16, device="cuda")
         w = torch.empty((4096, 4096), dtype=torch.bfloat16, device="cuda")
         for i in range(6):
             wb, wf, p, a = layers[i % 4]
             if kind == "decode":
-                bd.bitdelta_linear(x[:8], wb, p, a, per_row=True, out=y)
+                bd.bitdelta_linear(x[:8], wb, p, a, per_row=True, out=y[:8])
+            elif kind == "decode16":
+                bd.bitdelta_linear(x, wb, p, a, per_row=True, out=y)
             elif kind == "compress":
                 bd.bitdelta_compress(wb, wf, per_row=True, packed_out=p, alpha_out=a)
             else:
@@ -1340,8 +1342,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the per-workload oracle samples (cpu_baseline of each workload)")
     ap.add_argument("--profile", default=None,
-                    help="decode|compress|reconstruct|prefill|grouped|slice_decode|kmerge|"
-                         "monosoup: a few eager launches for ncu")
+                    help="decode|decode16|compress|reconstruct|prefill|grouped|slice_decode|"
+                         "kmerge|monosoup: a few eager launches for ncu")
     ap.add_argument("--prefill-tile", default="auto", choices=["auto", "256", "512"],
                     help="token width of the tensor-core kernel's pair tiles (profile runs)")
     args = ap.parse_args()
