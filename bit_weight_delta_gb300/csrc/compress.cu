@@ -81,7 +81,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                     float* __restrict__ alpha, double* __restrict__ row_sums,
                     unsigned int* __restrict__ done_counter, DevCtx ctx) {
   (void)ctx;
-  griddep_launch_dependents();
+  // No early signal to dependents: what this kernel writes can be a weight
+  // operand of the next call, and bitdelta_linear reads weights before it
+  // waits for the previous kernel, so a dependent starts only once this
+  // grid has finished.  The wait covers inputs an earlier kernel writes.
   griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;

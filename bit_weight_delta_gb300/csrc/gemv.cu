@@ -425,7 +425,8 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
     xsrc[k] = row >= 0 ? p.x + static_cast<int64_t>(row) * d_in + 8 * cw : nullptr;
   }
   const int64_t n_sc = d_in / (32 * CPS);
-  auto issue = [&](int s, int64_t sc) {
+  // the weight operands of a stage: W_base row segments and sign words
+  auto issue_w = [&](int s, int64_t sc) {
     if (sc < n_sc) {
       const int64_t kc0 = sc * 32 * CPS;
       const uint32_t st = wring_sa + s * kSB;
@@ -437,6 +438,13 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
       }
       if (has_delta && lane < rows_here && lane < R)
         cp_async_16_cg(st + R * 256 + 16u * lane, ssrc0 + kc0 / 8);
+    }
+  };
+  // the activations of a stage: x row segments
+  auto issue_x = [&](int s, int64_t sc) {
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * 32 * CPS;
+      const uint32_t st = wring_sa + s * kSB;
 #pragma unroll
       for (int k = 0; k < 4 * NT; ++k) {
         const int r = 2 * k + cr;
@@ -444,19 +452,34 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
           cp_async_16_x(st + kXOff + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), xsrc[k] + kc0);
       }
     }
-    cp_async_commit();  // one group per stage, empty past the end
   };
 
+  // Prologue: the weight halves of the first D-1 stages are issued before
+  // waiting for the previous kernel in the stream (weights are never its
+  // output), the x halves after it.  That makes 2(D-1) commit groups
+  // W_0..W_{D-2}, X_0..X_{D-2}; in iteration i the loop below commits one
+  // more group (both halves of stage i+D-1) and waits until at most D-1
+  // groups are pending, which leaves only groups newer than X_i (i < D-1) or
+  // than stage i: stage i is complete in either case.
   int64_t next = warp;
 #pragma unroll
   for (int s = 0; s < D - 1; ++s) {
-    issue(s, next);
-    next += kKW;
+    issue_w(s, next + s * kKW);
+    cp_async_commit();
   }
+  griddep_wait();
+#pragma unroll
+  for (int s = 0; s < D - 1; ++s) {
+    issue_x(s, next + s * kKW);
+    cp_async_commit();
+  }
+  next += (D - 1) * kKW;
   int s_rd = 0;
   for (int64_t sc = warp; sc < n_sc; sc += kKW) {
     __syncwarp();  // every lane is done reading the slot refilled next
-    issue(s_rd == 0 ? D - 1 : s_rd - 1, next);
+    issue_w(s_rd == 0 ? D - 1 : s_rd - 1, next);
+    issue_x(s_rd == 0 ? D - 1 : s_rd - 1, next);
+    cp_async_commit();  // one group per stage, empty past the end
     next += kKW;
     cp_async_wait<D - 1>();  // this lane's copies of the stage have landed
     __syncwarp();            // ... and every other lane's
@@ -780,15 +803,17 @@ __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
 }
 
 // Single variant through the deep cp.async queue (d_in % 128 == 0, aligned
-// sign rows); same grid and dependent-launch protocol as above, no prefetch
-// (its ring keeps three super-chunks per warp in flight from the start).
+// sign rows); same grid as above.  It waits for the previous kernel in the
+// stream only after it has issued the weight loads of its first ring stages
+// (inside gemv_group_async): W_base, the signs and α are inputs that no
+// kernel still in flight writes, so a CTA that starts while the previous
+// launch drains fills most of its ring before x is ready.
 template <int NG, bool kM16>
 __global__ void __launch_bounds__(kKW * 32) gemv_single_async_kernel(GemvArgs p) {
   extern __shared__ __align__(16) uint8_t ring[];
   __shared__ float red[kKW * NG * 4 * 32];
   __shared__ RowGroup grp;
   griddep_launch_dependents();
-  griddep_wait();
   const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
   for (int64_t c = blockIdx.y; c < n_chunks; c += gridDim.y) {
     if (threadIdx.x < kMaxGroupRows) {

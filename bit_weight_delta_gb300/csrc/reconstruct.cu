@@ -46,7 +46,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     reconstruct_kernel(const uint16_t* __restrict__ w_base, const uint8_t* __restrict__ packed,
                        const float* __restrict__ alpha, int per_row, int64_t d_out,
                        int64_t d_in, uint16_t* __restrict__ w_out) {
-  griddep_launch_dependents();
+  // No early signal to dependents: what this kernel writes can be a weight
+  // operand of the next call, and bitdelta_linear reads weights before it
+  // waits for the previous kernel, so a dependent starts only once this
+  // grid has finished.  The wait covers inputs an earlier kernel writes.
   griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;

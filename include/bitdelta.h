@@ -113,6 +113,16 @@ bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, co
  * runs on CTA pairs with tiles of 256 output rows by 256 or 512 tokens
  * (bitdelta_set_prefill_tile).
  * y must not overlap the inputs.
+ * Stream order: the decode kernel is launched with programmatic dependent
+ * launch and issues its first loads of w_base and packed before it waits for
+ * the kernels ahead of it on the stream (x and alpha are read after the
+ * wait, y written after it).  So w_base and packed must not be written by a
+ * kernel that may still be running when this call's kernel starts, that is
+ * by one that signals its dependents early (griddepcontrol.launch_dependents
+ * or cudaTriggerProgrammaticLaunchCompletion).  This library's calls that
+ * write such tensors (bitdelta_compress, bitdelta_compress_noalloc,
+ * bitdelta_reconstruct) do not signal early; kernels that do not use
+ * programmatic dependent launch never do.
  */
 bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
                           const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
