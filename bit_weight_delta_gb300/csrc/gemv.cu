@@ -26,8 +26,9 @@
 // shared memory (three super-chunks in flight per warp, no registers held) and
 // puts the W rows on the MMA's A side.  Per weight the kernels move
 // 2 + 1/8 bytes from HBM; x stays in L1/L2.  Launched with programmatic
-// dependent launch: the register kernel prefetches the head of its weight
-// slice into L2 before it waits for the previous kernel.
+// dependent launch: both kernels issue their first weight loads (and the
+// register kernel an L2 prefetch of the head of its weight slice) before
+// they wait for the previous kernel in the stream; x is read after the wait.
 #include <cstdint>
 
 #include "common.cuh"
@@ -172,7 +173,8 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
   using F = Frag<NG, CPS, kM16>;
 
-  auto load = [&](F& f, int64_t kc0) {
+  // the weight operands of a super-chunk (W_base words, sign words) ...
+  auto load_w = [&](F& f, int64_t kc0) {
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
       if (wrow[ng] != nullptr) {
@@ -198,11 +200,18 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
         }
       }
     }
+  };
+  // ... and its activations
+  auto load_x = [&](F& f, int64_t kc0) {
 #pragma unroll
     for (int j = 0; j < CPS; ++j) {
       f.xa[j] = xra != nullptr ? ldg_v4(xra + kc0 + 32 * j + 8 * t) : zero4;
       if (kM16) f.xb[j] = xrb != nullptr ? ldg_v4(xrb + kc0 + 32 * j + 8 * t) : zero4;
     }
+  };
+  auto load = [&](F& f, int64_t kc0) {
+    load_w(f, kc0);
+    load_x(f, kc0);
   };
   auto compute = [&](const F& f) {
 #pragma unroll
@@ -220,9 +229,14 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
   if constexpr (kSignVec) {
     // Two super-chunks in flight per warp: the loads of the next one are
     // issued before the products of the current one.
+    // The first super-chunk's weight loads go out before the wait for the
+    // previous kernel in the stream (weights are never its output), its x
+    // loads after it.
     F f0, f1;
     int64_t sc = warp;
-    if (sc < n_sc) load(f0, sc * 32 * CPS);
+    if (sc < n_sc) load_w(f0, sc * 32 * CPS);
+    griddep_wait();
+    if (sc < n_sc) load_x(f0, sc * 32 * CPS);
     while (sc < n_sc) {
       const int64_t sc1 = sc + kKW;
       if (sc1 < n_sc) load(f1, sc1 * 32 * CPS);
@@ -236,6 +250,7 @@ __device__ __forceinline__ void gemv_group(const GemvArgs& p, const RowGroup& gr
   } else {
     // Sign rows not 16-byte aligned: byte-wise sign loads, one super-chunk
     // at a time.
+    griddep_wait();
     for (int64_t sc = warp; sc < n_sc; sc += kKW) {
       F f;
       load(f, sc * 32 * CPS);
@@ -783,13 +798,14 @@ __device__ __forceinline__ void prefetch_weights(const GemvArgs& p) {
     prefetch_l2(p.packed + (n0 + r) * (p.d_in / 8));
 }
 
+// gemv_group waits for the previous kernel itself, after its first weight
+// loads.
 template <int NG, bool kM16, bool kSignVec>
 __global__ void __launch_bounds__(kKW * 32) gemv_single_kernel(GemvArgs p) {
   __shared__ float red[kKW * NG * 4 * 32];
   __shared__ RowGroup grp;
   if (blockIdx.y == 0) prefetch_weights<NG>(p);
   griddep_launch_dependents();
-  griddep_wait();
   const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
   for (int64_t c = blockIdx.y; c < n_chunks; c += gridDim.y) {
     if (threadIdx.x < kMaxGroupRows) {
