@@ -1060,30 +1060,21 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
   __syncthreads();
 }
 
-// Multi-tenant: rows of short segments, bucketed by variant, then taken in
-// groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
-// builds the same grouping in shared memory, then covers its 8·NG output
-// columns for every group.
-// One token tile with a two-stage ring: four CTAs per SM, so at most 128
-// registers per thread.
-template <int NG, int kAsyncNT, int V, int D>
-__global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
-    gemv_grouped_kernel(GemvArgs p, int ring_off) {
-  __shared__ float red[kKW * NG * 4 * 32];
-  extern __shared__ __align__(16) int32_t dyn[];
-  griddep_launch_dependents();
-  griddep_wait();
-  // dyn: [n_var+2] bucket counts | [n_var+2] bucket starts | [max_rows] rows
+// The short rows of a grouped call (segments of at most max_short rows),
+// bucketed by variant in this CTA's shared memory: dyn holds [n_var+2] bucket
+// counts, [n_var+2] bucket starts and the row list; rows
+// [start[v], start[v+1]) of the list belong to variant v (0 = base).  The
+// whole table is validated first: offsets non-decreasing inside [0, M], ids
+// inside [0, n_var].  One bad entry rejects the table (the error word records
+// it, no row is computed and false is returned to every thread), so segments
+// never overlap and the list never exceeds its bound.  Called by all threads.
+__device__ bool bucket_short_rows(const GemvArgs& p, int32_t* dyn) {
   const int nb = p.n_var + 1;
   int32_t* cnt = dyn;
   int32_t* start = dyn + (nb + 1);
   int32_t* rows = dyn + 2 * (nb + 1);
   for (int i = threadIdx.x; i < nb + 1; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
-  // Validate the whole table first: offsets must be non-decreasing inside
-  // [0, M] and ids inside [0, n_var].  One bad entry rejects the table (the
-  // error word records it and no row is computed), so segments can never
-  // overlap and the row list below never exceeds its bound.
   int bad_local = 0;
   for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
     const int32_t a = __ldg(p.seg_off + s), b = __ldg(p.seg_off + s + 1);
@@ -1092,7 +1083,7 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
   }
   if (__syncthreads_or(bad_local)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
-    return;
+    return false;
   }
   // pass 1: count short-segment rows per variant
   for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
@@ -1120,6 +1111,26 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     for (int32_t r = a; r < b; ++r) rows[pos + (r - a)] = r;
   }
   __syncthreads();
+  return true;
+}
+
+// Multi-tenant: rows of short segments, bucketed by variant, then taken in
+// groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
+// builds the same grouping in shared memory, then covers its 8·NG output
+// columns for every group.
+// One token tile with a two-stage ring: four CTAs per SM, so at most 128
+// registers per thread.
+template <int NG, int kAsyncNT, int V, int D>
+__global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
+    gemv_grouped_kernel(GemvArgs p, int ring_off) {
+  __shared__ float red[kKW * NG * 4 * 32];
+  extern __shared__ __align__(16) int32_t dyn[];
+  griddep_launch_dependents();
+  griddep_wait();
+  if (!bucket_short_rows(p, dyn)) return;
+  const int nb = p.n_var + 1;
+  const int32_t* start = dyn + (nb + 1);
+  const int32_t* rows = dyn + 2 * (nb + 1);
   // Groups of up to 16 rows taken in bucket (variant) order, closed early
   // when a fifth delta variant would join: each group is one pass over this
   // CTA's W_base rows.  Thread 0 forms the next group in shared memory.
@@ -1173,6 +1184,331 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
       else
         gemv_group_mixed<NG, false>(p, mg, red);
     }
+  }
+}
+
+// ------------------------------------------------------------------ wide passes
+
+// The short rows of a grouped call when there can be more of them than one
+// group holds: up to kWideTok rows of up to kWideVars delta variants (and any
+// number of base rows) in ONE pass over the CTA's 16 W_base rows, instead of
+// one pass per group of 16 rows and 4 variants.  The rows, in bucket
+// (variant) order, are cut into tiles of at most 8 rows of ONE variant, so a
+// tile needs one sign product and no masking: y = x·W_baseᵀ + α_v ⊙ (x·S_vᵀ)
+// with the two products in separate accumulators over all of d_in and α
+// applied once at the end, as in the other decode kernels.  The CTA shares
+// one cp.async ring of 128-column stages, each holding the W_base row
+// segments, the sign words of every variant of the pass and the x segments of
+// every row; warp w owns tiles w, w + W, ... (W warps) over all columns (no
+// cross-warp sum) and reads each W_base fragment once for its tiles.  The
+// inner loop has no data-dependent branch: a base tile takes the sign
+// product of the pass's first variant slot (±1 values, so finite) and
+// scales it by α = 0, and lanes past a tile's rows compute on its first row.
+// Measured on 14336 x 4096 with 14 variants: a pass over 64 rows in 173 µs
+// against 274 µs for the groups of 16 rows and 4 variants; tracking the
+// variant of the previous tile to skip a conversion, and predicated zero
+// operands, each cost more issue slots than they saved (208 µs).
+constexpr int kWideTok = 64;    // rows of x per pass (the ring's x segments)
+constexpr int kWideTiles = 16;  // tiles of at most 8 rows of one variant per pass
+#ifndef BD_WIDE_WARPS
+#define BD_WIDE_WARPS 4
+#endif
+constexpr int kWideWarps = BD_WIDE_WARPS;  // warps of a CTA
+constexpr int kWideThreads = 32 * kWideWarps;
+constexpr int kWideTilesPerWarp = kWideTiles / kWideWarps;
+constexpr int kWideVars = 16;   // delta variants per pass
+#ifndef BD_WIDE_COLS
+#define BD_WIDE_COLS 128
+#endif
+struct WidePass {
+  int32_t rows[kWideTok];         // x/y row of the pass's row slot i, −1 = empty
+  int32_t vars[kWideVars];        // the pass's delta variant ids (>= 1)
+  int32_t tile_r0[kWideTiles];    // first row slot of the tile
+  int32_t tile_n[kWideTiles];     // row slots of the tile (1..8; 0 = no tile)
+  int32_t tile_var[kWideTiles];   // index into vars[] of the tile's variant, −1 = base
+  int32_t n_tok, n_vars, n_tiles;
+  uint32_t unaligned;  // bit v: variant v's sign table is off the copy size (C/8 bytes)
+};
+// A ring stage of C columns (64 or 128): W_base row segments (16 × 2C
+// bytes, swizzled), the sign segments of every variant ([variant][row] ×
+// C/8 bytes), then the x segments of every row slot (64 × 2C bytes, swizzled).
+template <int C>
+__host__ __device__ constexpr int wide_s_off() { return 16 * 2 * C; }
+template <int C>
+__host__ __device__ constexpr int wide_x_off() { return wide_s_off<C>() + kWideVars * 16 * (C / 8); }
+template <int C>
+__host__ __device__ constexpr int wide_stage_bytes() { return wide_x_off<C>() + kWideTok * 2 * C; }
+template <int C, int D>
+constexpr size_t wide_ring_bytes() {
+  return static_cast<size_t>(D) * wide_stage_bytes<C>();
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* a) {
+  return *reinterpret_cast<const uint4*>(a);
+}
+
+template <int C, int D>
+__device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass& wp,
+                                               const float2 (&al_s)[kWideVars][8],
+                                               uint8_t* ring, int64_t n0) {
+  constexpr int R = 16;
+  constexpr int TW = kWideTilesPerWarp;
+  static_assert(C == 64 || C == 128, "stages of 64 or 128 columns");
+  constexpr int WPR = C / 8;                 // 16-byte words per row segment
+  constexpr int RPR = kWideThreads / WPR;    // row segments one round of the CTA's threads copies
+  constexpr int SPR = kWideThreads;          // (variant, row) sign segments per round
+  constexpr int SB = C / 8;             // sign bytes per row segment
+  constexpr int kSOff = wide_s_off<C>(), kXOff = wide_x_off<C>(), kSB = wide_stage_bytes<C>();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t d_in = p.d_in, d_out = p.d_out;
+  const int64_t row_bytes = d_in / 8;
+  const int64_t rows_here = d_out - n0 < R ? d_out - n0 : R;
+  const int n_tok = wp.n_tok, nv = wp.n_vars;
+  const uint32_t ring_sa = smem_addr(ring);
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+
+  // copy side: thread T moves word T % WPR of W rows T / WPR + RPR·k, the
+  // sign segment of (variant, row) pairs T + SPR·k, and word T % WPR of row
+  // slots T / WPR + RPR·k
+  constexpr int kSK = kWideVars * 16 / SPR;
+  const int cw = tid % WPR, cr = tid / WPR;
+  const uint8_t* ssrc[kSK];
+  bool s_al[kSK];
+#pragma unroll
+  for (int k = 0; k < kSK; ++k) {
+    const int i = tid + SPR * k, v = i >> 4, r = i & 15;
+    ssrc[k] = (v < nv && r < rows_here) ? p.packed_table[wp.vars[v] - 1] + (n0 + r) * row_bytes
+                                        : nullptr;
+    s_al[k] = v < nv && ((wp.unaligned >> v) & 1u) == 0;
+  }
+  int32_t xrow[kWideTok / RPR];
+#pragma unroll
+  for (int k = 0; k < kWideTok / RPR; ++k) {
+    const int slot = cr + RPR * k;
+    xrow[k] = slot < n_tok ? wp.rows[slot] : -1;
+  }
+  const int64_t n_sc = d_in / C;
+  auto issue = [&](int s, int64_t sc) {
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * C;
+      const uint32_t st = ring_sa + s * kSB;
+#pragma unroll
+      for (int k = 0; k < R / RPR; ++k) {
+        const int r = cr + RPR * k;
+        if (r < rows_here)
+          cp_async_16_cg(st + 16u * (r * WPR + (cw ^ ((r & 1) << 2))),
+                         p.w + (n0 + r) * d_in + kc0 + 8 * cw);
+      }
+#pragma unroll
+      for (int k = 0; k < kSK; ++k) {
+        if (ssrc[k] == nullptr) continue;
+        const uint32_t dst = st + kSOff + SB * (tid + SPR * k);
+        const uint8_t* src = ssrc[k] + kc0 / 8;
+        if (s_al[k]) {
+          if constexpr (SB == 16)
+            cp_async_16_cg(dst, src);
+          else
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src)
+                         : "memory");
+        } else {
+          // read by the other warps after the stage's barrier, like the copies
+          uint32_t w4[4];
+#pragma unroll
+          for (int b = 0; b < SB / 4; ++b)
+            w4[b] = static_cast<uint32_t>(__ldg(src + 4 * b)) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 1)) << 8) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 2)) << 16) |
+                    (static_cast<uint32_t>(__ldg(src + 4 * b + 3)) << 24);
+          if constexpr (SB == 16)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w4[0]),
+                         "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                         : "memory");
+          else
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(w4[0]), "r"(w4[1])
+                         : "memory");
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kWideTok / RPR; ++k) {
+        const int slot = cr + RPR * k;
+        if (xrow[k] >= 0)
+          cp_async_16_x(st + kXOff + 16u * (slot * WPR + (cw ^ ((slot & 1) << 2))),
+                        p.x + static_cast<int64_t>(xrow[k]) * d_in + kc0 + 8 * cw);
+      }
+    }
+    cp_async_commit();  // one group per stage, empty past the end
+  };
+
+  // compute side: this warp's tiles warp + kWideWarps·k.  The lane's B
+  // column is row slot r0 + g of the tile; lanes past the tile's rows read
+  // its first row instead (their columns of the products are never stored),
+  // and W rows past d_out hold whatever the ring held (their rows of the
+  // products are never stored either), so no fragment read needs a select.
+  // Per tile: byte offsets within a stage of the lane's x row and of its
+  // sign bytes (rows g, g + 8), and the x row's swizzle (64 bytes on odd
+  // rows: the word index XOR 4).
+  int tvar[TW], xoff[TW], xpar[TW], soff[TW];
+  bool have[TW];
+#pragma unroll
+  for (int k = 0; k < TW; ++k) {
+    const int kt = warp + kWideWarps * k;
+    const int n = wp.tile_n[kt];
+    have[k] = n > 0;
+    tvar[k] = wp.tile_var[kt];
+    const int xs = wp.tile_r0[kt] + (g < n ? g : 0);
+    xoff[k] = kXOff + 16 * (xs * WPR + t);
+    xpar[k] = (xs & 1) << 6;
+    const int vs = tvar[k] > 0 ? tvar[k] : 0;
+    soff[k] = kSOff + SB * (vs * 16 + g) + t;
+  }
+  int my_tiles = 0;  // tiles are numbered densely, so this warp's are k < my_tiles
+#pragma unroll
+  for (int k = 0; k < TW; ++k) my_tiles += have[k] ? 1 : 0;
+  const int w_off0 = 16 * (g * WPR + t), w_off1 = 16 * ((g + 8) * WPR + t);
+  const int wpar = (g & 1) << 6;
+  float acc_b[TW][4], acc_s[TW][4];
+#pragma unroll
+  for (int k = 0; k < TW; ++k)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc_b[k][e] = acc_s[k][e] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < D - 1; ++s) issue(s, s);
+  int slot = 0;
+  for (int64_t sc = 0; sc < n_sc; ++sc) {
+    cp_async_wait<D - 2>();  // this thread's copies of stage sc have landed
+    __syncthreads();         // ... everyone's; and the slot refilled next is free
+    issue(slot == 0 ? D - 1 : slot - 1, sc + D - 1);
+    const uint8_t* st = ring + slot * kSB;
+#pragma unroll
+    for (int j = 0; j < C / 32; ++j) {  // 32-column chunks: word 4j + t of a row
+      const uint4 wv0 = lds128(st + w_off0 + ((64 * j) ^ wpar));
+      const uint4 wv1 = lds128(st + w_off1 + ((64 * j) ^ wpar));
+#pragma unroll
+      for (int k = 0; k < TW; ++k) {
+        if (k >= my_tiles) break;
+        const uint4 xv = lds128(st + xoff[k] + ((64 * j) ^ xpar[k]));
+        const uint32_t b0 = st[soff[k] + 4 * j];
+        const uint32_t b1 = st[soff[k] + 8 * SB + 4 * j];
+        uint32_t s0[4], s1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s0[i] = pm_one_pair(b0, i);
+          s1[i] = pm_one_pair(b1, i);
+        }
+        mma_16816(acc_b[k], wv0.x, wv1.x, wv0.y, wv1.y, xv.x, xv.y);
+        mma_16816(acc_b[k], wv0.z, wv1.z, wv0.w, wv1.w, xv.z, xv.w);
+        mma_16816(acc_s[k], s0[0], s1[0], s0[1], s1[1], xv.x, xv.y);
+        mma_16816(acc_s[k], s0[2], s1[2], s0[3], s1[3], xv.z, xv.w);
+      }
+    }
+    slot = slot == D - 1 ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+
+  // y = acc_b + α_v[n]·acc_s; C columns 2t, 2t+1 are the tile's rows
+#pragma unroll
+  for (int k = 0; k < TW; ++k) {
+    if (!have[k]) continue;
+    const int kt = warp + kWideWarps * k;
+    const int n_rows = wp.tile_n[kt], r0 = wp.tile_r0[kt];
+    const float2 al = tvar[k] >= 0 ? al_s[tvar[k]][g] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 2 * t + (e & 1);
+      const int64_t n = n0 + g + 8 * (e >> 1);
+      if (c >= n_rows || n >= d_out) continue;
+      const float v = fmaf((e >> 1) ? al.y : al.x, acc_s[k][e], acc_b[k][e]);
+      p.y[static_cast<int64_t>(wp.rows[r0 + c]) * d_out + n] =
+          static_cast<uint16_t>(pack_bf16x2_rn(v, 0.f) & 0xFFFFu);
+    }
+  }
+  __syncthreads();  // the ring and the pass tables are reused by the next pass
+}
+
+// Requires d_in % 128 == 0.  One CTA per 16 W_base rows; every CTA buckets
+// the short rows (as the grouped kernel does), then runs the passes: thread 0
+// cuts the rows, in bucket order, into tiles of at most 8 rows of one
+// variant, closing the pass when it holds kWideTok rows or kWideTiles tiles,
+// or when a (kWideVars+1)-th delta variant would join.
+template <int C, int D>
+__global__ void __launch_bounds__(kWideThreads,
+                                  (wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3) * 128 /
+                                      kWideThreads)
+    gemv_wide_kernel(GemvArgs p, int ring_off) {
+  extern __shared__ __align__(16) int32_t dyn[];
+  __shared__ WidePass wp;
+  __shared__ float2 al_s[kWideVars][8];  // α of the pass's variants: rows n0+g, n0+8+g
+  __shared__ int32_t cursor, bucket;
+  griddep_launch_dependents();
+  griddep_wait();
+  if (!bucket_short_rows(p, dyn)) return;
+  const int nb = p.n_var + 1;
+  const int32_t* start = dyn + (nb + 1);
+  const int32_t* rows = dyn + 2 * (nb + 1);
+  const int32_t total = start[nb];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(dyn) + ring_off;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16;
+  if (threadIdx.x == 0) {
+    cursor = 0;
+    bucket = 0;
+  }
+  __syncthreads();
+  while (cursor < total) {
+    if (threadIdx.x == 0) {
+      int n = 0, nvars = 0, ntl = 0;
+      uint32_t unal = 0;
+      int32_t c = cursor, bk = bucket;
+      while (c < total && n < kWideTok && ntl < kWideTiles) {
+        while (c >= start[bk + 1]) ++bk;  // the bucket (variant) of sorted row c
+        int vslot = -1;
+        if (bk > 0) {
+          if (nvars == kWideVars) break;
+          vslot = nvars;
+          wp.vars[nvars] = bk;
+          if ((reinterpret_cast<uintptr_t>(p.packed_table[bk - 1]) & (C / 8 - 1)) != 0)
+            unal |= 1u << nvars;
+          ++nvars;
+        }
+        const int32_t end = start[bk + 1];
+        while (c < end && n < kWideTok && ntl < kWideTiles) {
+          int32_t cnt = end - c;
+          cnt = cnt < 8 ? cnt : 8;
+          cnt = cnt < kWideTok - n ? cnt : kWideTok - n;
+          wp.tile_r0[ntl] = n;
+          wp.tile_n[ntl] = cnt;
+          wp.tile_var[ntl] = vslot;
+          ++ntl;
+          for (int32_t i = 0; i < cnt; ++i) wp.rows[n++] = rows[c++];
+        }
+      }
+      for (int i = n; i < kWideTok; ++i) wp.rows[i] = -1;
+      for (int k = ntl; k < kWideTiles; ++k) {
+        wp.tile_r0[k] = 0;
+        wp.tile_n[k] = 0;
+        wp.tile_var[k] = -1;
+      }
+      wp.n_tok = n;
+      wp.n_vars = nvars;
+      wp.n_tiles = ntl;
+      wp.unaligned = unal;
+      cursor = c;
+      bucket = bk;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < wp.n_vars * 16; i += blockDim.x) {
+      const int v = i >> 4, r = i & 15;
+      const int64_t n = n0 + r;
+      const float* a = p.alpha_table[wp.vars[v] - 1];
+      const float val = n < p.d_out ? (p.per_row ? __ldg(a + n) : __ldg(a)) : 0.f;
+      if (r < 8)
+        al_s[v][r].x = val;
+      else
+        al_s[v][r - 8].y = val;
+    }
+    __syncthreads();
+    gemv_wide_pass<C, D>(p, wp, al_s, ring, n0);
   }
 }
 
@@ -1249,6 +1585,28 @@ cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off
                     ring_off);
 }
 
+template <int C, int D>
+cudaError_t launch_wide_instance(const GemvArgs& p, size_t smem, int ring_off, dim3 grid,
+                                 cudaStream_t stream) {
+  static size_t smem_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(host_cache_mutex());
+    if (smem > 48 * 1024 && smem > smem_set[dev]) {
+      e = cudaFuncSetAttribute(gemv_wide_kernel<C, D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      smem_set[dev] = smem;
+    }
+  }
+  return launch_pdl(gemv_wide_kernel<C, D>, grid, dim3(kWideThreads), smem, stream, p,
+                    ring_off);
+}
+
 cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, int num_sms,
                                 cudaStream_t stream) {
   const size_t group_smem = gemv_grouped_smem_bytes(p.n_var, max_rows);
@@ -1262,6 +1620,15 @@ cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, int num_sms
   const size_t ring_off = (group_smem + 15) / 16 * 16;
   const size_t kMaxDyn = 200 * 1024;
   const int ro = static_cast<int>(ring_off);
+#ifndef BD_WIDE_STAGES
+#define BD_WIDE_STAGES 3
+#endif
+  // More short rows than one group holds: the wide pass (all of them, up to
+  // 64 rows and 16 variants per pass, in one pass over W_base).
+  constexpr size_t kWideRing = wide_ring_bytes<BD_WIDE_COLS, BD_WIDE_STAGES>();
+  if (p.d_in % 128 == 0 && max_rows > kMaxGroupRows && ring_off + kWideRing <= kMaxDyn)
+    return launch_wide_instance<BD_WIDE_COLS, BD_WIDE_STAGES>(p, ring_off + kWideRing, ro, grid,
+                                                               stream);
   if (p.d_in % 128 == 0) {
     const bool two = p.n_var <= 2;
     const bool shallow = n_blocks > 2 * static_cast<int64_t>(num_sms);

@@ -22,7 +22,8 @@ import torch
 import bit_weight_delta_gb300 as bd
 import oracle
 import synth
-from gpu_util import bf16_values, from_dev_bf16, to_dev, to_dev_bf16
+from gpu_util import (assert_split_elementwise, bf16_values, from_dev_bf16, to_dev,
+                      to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,19 +31,7 @@ BIG_B = 0.02
 
 
 def _assert_split_close(y, x, wb, packed, alpha, per_row, what):
-    """|y − y_split| within bf16 output rounding plus fp32 accumulation (the
-    bound of the element-wise decode tests)."""
-    d_out, d_in = wb.shape
-    ref = oracle.linear_split(x, wb, packed, alpha, per_row)
-    xa = np.abs(synth.bf16_to_f32(x).astype(np.float64))
-    a_rows = alpha.astype(np.float64) if per_row else np.full(d_out, float(alpha[0]))
-    acc = (d_in / 16 + 8) * 2.0 ** -21 * (
-        xa @ np.abs(synth.bf16_to_f32(wb).astype(np.float64)).T
-        + xa.sum(axis=1, keepdims=True) * a_rows[None, :])
-    err = np.abs(y - ref)
-    bound = 2.0 ** -8 * np.abs(ref) + acc
-    assert not (err > bound).any(), (f"{what}: {int((err > bound).sum())} outputs off, worst "
-                                     f"{float((err - bound).max()):.3e} over the bound")
+    assert_split_elementwise(y, x, wb, packed, alpha, per_row, what)
 
 
 @pytest.mark.parametrize("M", [4, 12])
