@@ -30,6 +30,7 @@
 // register kernel an L2 prefetch of the head of its weight slice) before
 // they wait for the previous kernel in the stream; x is read after the wait.
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -1204,10 +1205,12 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
 // inner loop has no data-dependent branch: a base tile takes the sign
 // product of the pass's first variant slot (±1 values, so finite) and
 // scales it by α = 0, and lanes past a tile's rows compute on its first row.
-// Measured on 14336 x 4096 with 14 variants: a pass over 64 rows in 173 µs
+// Measured on 14336 x 4096 with 14 variants: a pass over 64 rows in 158 µs
 // against 274 µs for the groups of 16 rows and 4 variants; tracking the
 // variant of the previous tile to skip a conversion, and predicated zero
-// operands, each cost more issue slots than they saved (208 µs).
+// operands, each cost more issue slots than they saved (208 µs), and so did
+// a tile loop with an exit on the warp's tile count (173 µs: the compiler
+// cannot interleave tiles across the exits), hence one body per count.
 constexpr int kWideTok = 64;    // rows of x per pass (the ring's x segments)
 constexpr int kWideTiles = 16;  // tiles of at most 8 rows of one variant per pass
 #ifndef BD_WIDE_WARPS
@@ -1381,28 +1384,42 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
     __syncthreads();         // ... everyone's; and the slot refilled next is free
     issue(slot == 0 ? D - 1 : slot - 1, sc + D - 1);
     const uint8_t* st = ring + slot * kSB;
+    // The stage's products for this warp's first NTK tiles, with NTK known
+    // at compile time: one straight-line block the compiler can interleave
+    // across tiles (a loop with an exit on the tile count cannot be).
+    auto stage = [&](auto ntk) {
+      constexpr int NTK = decltype(ntk)::value;
 #pragma unroll
-    for (int j = 0; j < C / 32; ++j) {  // 32-column chunks: word 4j + t of a row
-      const uint4 wv0 = lds128(st + w_off0 + ((64 * j) ^ wpar));
-      const uint4 wv1 = lds128(st + w_off1 + ((64 * j) ^ wpar));
+      for (int j = 0; j < C / 32; ++j) {  // 32-column chunks: word 4j + t of a row
+        const uint4 wv0 = lds128(st + w_off0 + ((64 * j) ^ wpar));
+        const uint4 wv1 = lds128(st + w_off1 + ((64 * j) ^ wpar));
 #pragma unroll
-      for (int k = 0; k < TW; ++k) {
-        if (k >= my_tiles) break;
-        const uint4 xv = lds128(st + xoff[k] + ((64 * j) ^ xpar[k]));
-        const uint32_t b0 = st[soff[k] + 4 * j];
-        const uint32_t b1 = st[soff[k] + 8 * SB + 4 * j];
-        uint32_t s0[4], s1[4];
+        for (int k = 0; k < NTK; ++k) {
+          const uint4 xv = lds128(st + xoff[k] + ((64 * j) ^ xpar[k]));
+          const uint32_t b0 = st[soff[k] + 4 * j];
+          const uint32_t b1 = st[soff[k] + 8 * SB + 4 * j];
+          uint32_t s0[4], s1[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s0[i] = pm_one_pair(b0, i);
-          s1[i] = pm_one_pair(b1, i);
+          for (int i = 0; i < 4; ++i) {
+            s0[i] = pm_one_pair(b0, i);
+            s1[i] = pm_one_pair(b1, i);
+          }
+          mma_16816(acc_b[k], wv0.x, wv1.x, wv0.y, wv1.y, xv.x, xv.y);
+          mma_16816(acc_b[k], wv0.z, wv1.z, wv0.w, wv1.w, xv.z, xv.w);
+          mma_16816(acc_s[k], s0[0], s1[0], s0[1], s1[1], xv.x, xv.y);
+          mma_16816(acc_s[k], s0[2], s1[2], s0[3], s1[3], xv.z, xv.w);
         }
-        mma_16816(acc_b[k], wv0.x, wv1.x, wv0.y, wv1.y, xv.x, xv.y);
-        mma_16816(acc_b[k], wv0.z, wv1.z, wv0.w, wv1.w, xv.z, xv.w);
-        mma_16816(acc_s[k], s0[0], s1[0], s0[1], s1[1], xv.x, xv.y);
-        mma_16816(acc_s[k], s0[2], s1[2], s0[3], s1[3], xv.z, xv.w);
       }
-    }
+    };
+    static_assert(TW <= 4, "stage bodies for 1..4 tiles per warp");
+    if (my_tiles >= TW)
+      stage(std::integral_constant<int, TW>{});
+    else if (TW > 3 && my_tiles == 3)
+      stage(std::integral_constant<int, (TW > 3 ? 3 : 1)>{});
+    else if (TW > 2 && my_tiles == 2)
+      stage(std::integral_constant<int, (TW > 2 ? 2 : 1)>{});
+    else if (my_tiles == 1)
+      stage(std::integral_constant<int, 1>{});
     slot = slot == D - 1 ? 0 : slot + 1;
   }
   cp_async_wait<0>();
