@@ -868,7 +868,7 @@ constexpr size_t mixed_ring_bytes() {
 
 template <int NT, int V, int D>
 __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const MixedGroup& grp,
-                                                       float* red, uint8_t* ring) {
+                                                       float* red, uint8_t* ring, bool w_ahead) {
   constexpr int CPS = kCPS;
   constexpr int R = kStageRows;  // 16 W rows
   static_assert(R == 16 && V % 2 == 0, "two 8-row halves; variants copied in pairs");
@@ -925,7 +925,7 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
     xsrc[k] = row >= 0 ? p.x + static_cast<int64_t>(row) * d_in + 8 * cw : nullptr;
   }
   const int64_t n_sc = d_in / (32 * CPS);
-  auto issue = [&](int s, int64_t sc) {
+  auto issue_w = [&](int s, int64_t sc) {
     if (sc < n_sc) {
       const int64_t kc0 = sc * 32 * CPS;
       const uint32_t st = wring_sa + s * kSB;
@@ -935,6 +935,12 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
         if (r < rows_here)
           cp_async_16_cg(st + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), wsrc0 + 2 * k * d_in + kc0);
       }
+    }
+  };
+  auto issue_sx = [&](int s, int64_t sc) {
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * 32 * CPS;
+      const uint32_t st = wring_sa + s * kSB;
 #pragma unroll
       for (int k = 0; k < V / 2; ++k) {
         if (ssrc[k] == nullptr) continue;
@@ -963,13 +969,29 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
           cp_async_16_x(st + kXOff + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), xsrc[k] + kc0);
       }
     }
+  };
+  auto issue = [&](int s, int64_t sc) {
+    issue_w(s, sc);
+    issue_sx(s, sc);
     cp_async_commit();  // one group per stage, empty past the end
   };
 
+  // Prologue.  With w_ahead the W rows of stages 0..D-2 are already in
+  // flight as D-1 commit groups of their own (issued by mixed_issue_w before
+  // the kernel waited for the previous one); their sign words and x follow
+  // as D-1 more groups.  Iteration i of the loop below commits one group and
+  // then waits until at most D-1 are pending: for i < D-1 that leaves only
+  // groups newer than stage i's signs and x, later only groups newer than
+  // stage i, so stage i has landed either way.
   int64_t next = warp;
 #pragma unroll
   for (int s = 0; s < D - 1; ++s) {
-    issue(s, next);
+    if (w_ahead) {
+      issue_sx(s, next);
+      cp_async_commit();
+    } else {
+      issue(s, next);
+    }
     next += kKW;
   }
   int s_rd = 0;
@@ -1115,6 +1137,39 @@ __device__ bool bucket_short_rows(const GemvArgs& p, int32_t* dyn) {
   return true;
 }
 
+// The W_base rows of this warp's first D-1 ring stages for the first group
+// of gemv_group_mixed_async (same slots and copy mapping), one commit group
+// per stage.  W_base is never the output of a kernel still in flight, so
+// this runs before the grouped kernel waits for the previous kernel.
+template <int NT, int V, int D>
+__device__ __forceinline__ void mixed_issue_w(const GemvArgs& p, uint8_t* ring) {
+  constexpr int R = kStageRows;
+  constexpr int kSB = mixed_stage_bytes<NT, V>();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cr = lane >> 4, cw = lane & 15;
+  const int64_t d_in = p.d_in;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int64_t rows_here = p.d_out - n0 < R ? p.d_out - n0 : R;
+  const int64_t n_sc = d_in / (32 * kCPS);
+  const uint32_t wring_sa = smem_addr(ring + static_cast<size_t>(warp) * D * kSB);
+  const uint16_t* const wsrc0 = p.w + (n0 + cr) * d_in + 8 * cw;
+#pragma unroll
+  for (int s = 0; s < D - 1; ++s) {
+    const int64_t sc = warp + static_cast<int64_t>(s) * kKW;
+    if (sc < n_sc) {
+      const int64_t kc0 = sc * 32 * kCPS;
+      const uint32_t st = wring_sa + s * kSB;
+#pragma unroll
+      for (int k = 0; k < R / 2; ++k) {
+        const int r = 2 * k + cr;
+        if (r < rows_here)
+          cp_async_16_cg(st + 16u * (r * 16 + (cw ^ ((r & 1) << 2))), wsrc0 + 2 * k * d_in + kc0);
+      }
+    }
+    cp_async_commit();
+  }
+}
+
 // Multi-tenant: rows of short segments, bucketed by variant, then taken in
 // groups of up to 16 rows of up to kMaxGroupVars delta variants.  Every CTA
 // builds the same grouping in shared memory, then covers its 8·NG output
@@ -1127,8 +1182,13 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
   __shared__ float red[kKW * NG * 4 * 32];
   extern __shared__ __align__(16) int32_t dyn[];
   griddep_launch_dependents();
+  if constexpr (kAsyncNT > 0)
+    mixed_issue_w<kAsyncNT, V, D>(p, reinterpret_cast<uint8_t*>(dyn) + ring_off);
   griddep_wait();
-  if (!bucket_short_rows(p, dyn)) return;
+  if (!bucket_short_rows(p, dyn)) {
+    cp_async_wait<0>();  // no copy may land after the CTA has left
+    return;
+  }
   const int nb = p.n_var + 1;
   const int32_t* start = dyn + (nb + 1);
   const int32_t* rows = dyn + 2 * (nb + 1);
@@ -1144,6 +1204,7 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     bucket = 0;
   }
   __syncthreads();
+  bool first = true;  // the first group (its W rows are in flight already)
   while (cursor < total) {
     if (threadIdx.x == 0) {
       int i = 0, nvars = 0;
@@ -1176,9 +1237,11 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     }
     __syncthreads();
     if constexpr (kAsyncNT > 0) {
-      // the ring (d_in % 128 == 0): unaligned variant tables included
+      // the ring (d_in % 128 == 0): unaligned variant tables included; the
+      // first group's W rows were issued before the dependency wait
       gemv_group_mixed_async<kAsyncNT, V, D>(p, mg, red,
-                                             reinterpret_cast<uint8_t*>(dyn) + ring_off);
+                                             reinterpret_cast<uint8_t*>(dyn) + ring_off, first);
+      first = false;
     } else {
       if (mg_vec)
         gemv_group_mixed<NG, true>(p, mg, red);
@@ -1186,6 +1249,7 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
         gemv_group_mixed<NG, false>(p, mg, red);
     }
   }
+  cp_async_wait<0>();  // no short rows: the early W copies still land before exit
 }
 
 // ------------------------------------------------------------------ wide passes
