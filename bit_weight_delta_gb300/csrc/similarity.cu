@@ -14,7 +14,8 @@
 // HBM-bound: the candidate's signs are read once, each member's once
 // ((1 + n_b)/16 bytes per weight).  A warp takes one row of the candidate at
 // a time into registers (16 bytes per lane per 4096 columns) and streams the
-// pool members' same row, sixteen members per round of loads.  The lanes'
+// pool members' same row, sixteen members per round of loads, and starts an
+// L2 prefetch of the next row it will take.  The lanes'
 // disagreement counts are summed by a transposing butterfly that leaves
 // member j's row total in lanes 2j and 2j+1 (16 shuffles for 16 members),
 // and the even lanes do the fp64 α arithmetic side by side.  Per-CTA partial
@@ -101,9 +102,21 @@ __global__ void __launch_bounds__(kThreads) sign_similarity_kernel(SimArgs p) {
 
   const int64_t row_bytes = p.d_in / 8;
   const double d_in = static_cast<double>(p.d_in);
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + warp; r < p.d_out;
-       r += static_cast<int64_t>(gridDim.x) * kWarps) {
+  const int64_t r_step = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + warp; r < p.d_out; r += r_step) {
     const uint8_t* ra = p.pa + r * row_bytes;
+    // The next row this warp takes, of the candidate and every member,
+    // towards L2 while this row's loads and sums run (lane L takes every
+    // 32nd 128-byte line of the (1 + n_b) row segments).
+    if (r + r_step < p.d_out) {
+      const int64_t rn = r + r_step;
+      const int64_t lines = (row_bytes + 127) / 128;
+      for (int64_t i = lane; i < (1 + n_b) * lines; i += 32) {
+        const int64_t m = i / lines, l = i - m * lines;
+        const uint8_t* base = m == 0 ? p.pa : s_pb[m - 1];
+        prefetch_l2(base + rn * row_bytes + 128 * l);
+      }
+    }
     const double alpha_a = static_cast<double>(p.per_row ? __ldg(p.aa + r) : __ldg(p.aa));
     for (int b0 = 0; b0 < n_b; b0 += kRound) {
       int cnt[kRound];
