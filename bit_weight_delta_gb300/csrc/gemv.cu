@@ -500,12 +500,13 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
     cp_async_wait<D - 1>();  // this lane's copies of the stage have landed
     __syncwarp();            // ... and every other lane's
     const uint8_t* st = wring + s_rd * kSB;
+    // No selects on the fragment reads: a W row past d_out or an empty token
+    // slot holds whatever the ring held and feeds only products of that row
+    // or token, which are never stored (nor are sign words without a delta).
     uint4 sw[NG];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng)
-      sw[ng] = (row_ok[ng] && has_delta)
-                   ? *reinterpret_cast<const uint4*>(st + R * 256 + 16 * (8 * ng + g))
-                   : zero4;
+      sw[ng] = *reinterpret_cast<const uint4*>(st + R * 256 + 16 * (8 * ng + g));
 #pragma unroll
     for (int j = 0; j < CPS; ++j) {
       uint4 wv[NG];
@@ -513,9 +514,7 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
         const int r = 8 * ng + g;
-        wv[ng] = row_ok[ng] ? *reinterpret_cast<const uint4*>(
-                                  st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
-                            : zero4;
+        wv[ng] = *reinterpret_cast<const uint4*>(st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))));
         const uint32_t word = j == 0 ? sw[ng].x : j == 1 ? sw[ng].y : j == 2 ? sw[ng].z : sw[ng].w;
         sb[ng] = (word >> (8 * t)) & 0xFFu;
       }
@@ -523,9 +522,8 @@ __device__ __forceinline__ void gemv_group_async(const GemvArgs& p, const RowGro
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int r = 8 * nt + g;
-        xv[nt] = x_ok[nt] ? *reinterpret_cast<const uint4*>(
-                                st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
-                          : zero4;
+        xv[nt] = *reinterpret_cast<const uint4*>(
+            st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))));
       }
       chunk_mma_t<NT>(acc_b, acc_s, wv, sb, xv, has_delta);
     }
@@ -1002,31 +1000,29 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
     cp_async_wait<D - 1>();
     __syncwarp();
     const uint8_t* st = wring + s_rd * kSB;
+    // No selects on the fragment reads: a W row past d_out, an empty token
+    // slot or a variant slot past nv holds whatever the ring held, and feeds
+    // only products of that row, token or slot, which are never stored.
     uint4 sw[V][2];
 #pragma unroll
     for (int v = 0; v < V; ++v)
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        sw[v][h] = (v < nv && row_ok[h])
-                       ? *reinterpret_cast<const uint4*>(st + kSOff + 16 * (v * R + 8 * h + g))
-                       : zero4;
+        sw[v][h] = *reinterpret_cast<const uint4*>(st + kSOff + 16 * (v * R + 8 * h + g));
 #pragma unroll
     for (int j = 0; j < CPS; ++j) {
       uint4 wv[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r = 8 * h + g;
-        wv[h] = row_ok[h] ? *reinterpret_cast<const uint4*>(
-                                st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
-                          : zero4;
+        wv[h] = *reinterpret_cast<const uint4*>(st + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))));
       }
       uint4 xv[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int r = 8 * nt + g;
-        xv[nt] = x_ok[nt] ? *reinterpret_cast<const uint4*>(
-                                st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))))
-                          : zero4;
+        xv[nt] = *reinterpret_cast<const uint4*>(
+            st + kXOff + 16 * (r * 16 + ((4 * j + t) ^ ((r & 1) << 2))));
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
