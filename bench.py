@@ -1480,8 +1480,8 @@ def main():
                          "traffic": DECODE_TRAFFIC_BYTES,
                          "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of "
                                            "one gemv_single_async_kernel launch, 4096x4096, M=8",
-                         "kernel": "bitdelta_linear decode: gemv_single_async_kernel (M=1..8), "
-                                   "gemv_single_kernel (M=16)",
+                         "kernel": "bitdelta_linear decode: gemv_single_async_kernel (M=1..16; "
+                                   "the 4096x4096 grid is one wave at two CTAs per SM)",
                          "peak_source": peaks["source"]},
             "per_kernel": per_kernel,
             "decode_unfused_reconstruct_plus_cublas": decode_unfused,

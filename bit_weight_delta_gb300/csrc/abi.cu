@@ -294,7 +294,7 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
   a.per_row = mode == BD_ALPHA_PER_ROW;
   a.y = y;
   a.ctx = ctx;
-  return from_cuda(bd::launch_gemv(a, s));
+  return from_cuda(bd::launch_gemv(a, dev->num_sms, s));
 }
 
 bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int32_t* seg_offsets,

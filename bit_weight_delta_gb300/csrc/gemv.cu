@@ -1589,15 +1589,22 @@ __global__ void __launch_bounds__(kWideThreads,
   }
 }
 
+// The ring kernel takes M <= 8, and M = 9..16 (two token tiles) when the
+// grid is one wave at two CTAs per SM: there it beats the register kernel
+// (4096 x 4096: 9.3 / 10.0 µs against 10.1 / 10.2 at M = 12 / 16), while on
+// multi-wave grids the two tiles' x copies cost it more than it gains
+// (57344 x 8192 at M = 16: 218 against 204 µs).
 template <int NG>
-cudaError_t launch_single(const GemvArgs& p, bool sign_vec, cudaStream_t stream) {
+cudaError_t launch_single(const GemvArgs& p, bool sign_vec, int num_sms, cudaStream_t stream) {
   const int64_t n_blocks = (p.d_out + 8 * NG - 1) / (8 * NG);
   const int64_t n_chunks = (p.M + kMaxGroupRows - 1) / kMaxGroupRows;
   dim3 grid(static_cast<unsigned>(n_blocks),
             static_cast<unsigned>(n_chunks < 65535 ? n_chunks : 65535));
   const bool m16 = p.M > 8;
   const dim3 block(kKW * 32);
-  if (sign_vec && p.M <= BD_GEMV_ASYNC_MAX_M) {
+  const bool one_wave = n_blocks <= 2 * static_cast<int64_t>(num_sms);
+  const int64_t ring_max_m = one_wave ? kMaxGroupRows : BD_GEMV_ASYNC_MAX_M;
+  if (sign_vec && p.M <= ring_max_m) {
     // The ring needs more than the default 48 KB of dynamic shared memory:
     // raise the limit once per device (outside any capture in practice: the
     // first call on a device).
@@ -1632,10 +1639,10 @@ size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows) {
   return sizeof(int32_t) * (2 * (static_cast<size_t>(n_var) + 2) + static_cast<size_t>(max_rows));
 }
 
-cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream) {
+cudaError_t launch_gemv(const GemvArgs& p, int num_sms, cudaStream_t stream) {
   const bool sign_vec = (p.d_in % 128 == 0) &&
                         (reinterpret_cast<uintptr_t>(p.packed) % 16 == 0);
-  return launch_single<kNG>(p, sign_vec, stream);
+  return launch_single<kNG>(p, sign_vec, num_sms, stream);
 }
 
 template <int NT, int V, int D>

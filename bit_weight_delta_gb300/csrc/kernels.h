@@ -72,7 +72,7 @@ struct GemvArgs {
   DevCtx ctx;
 };
 
-cudaError_t launch_gemv(const GemvArgs& p, cudaStream_t stream);
+cudaError_t launch_gemv(const GemvArgs& p, int num_sms, cudaStream_t stream);
 
 size_t gemv_grouped_smem_bytes(int32_t n_var, int64_t max_rows);
 cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, int num_sms,

@@ -163,11 +163,13 @@ def test_wait_timeout_is_reported():
                         oracle.linear(x, wb, packed, alpha, True))
 
 
-@pytest.mark.parametrize("shape", [(37, 256), (250, 1024), (1, 128), (17, 384)])
-@pytest.mark.parametrize("M", [1, 5, 8])
+@pytest.mark.parametrize("shape", [(37, 256), (250, 1024), (1, 128), (17, 384), (5003, 256)])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 12, 16])
 def test_decode_ring_ragged_d_out(shape, M):
-    """d_in a multiple of 128 (the cp.async ring for M <= 8) with a d_out that
-    leaves the last CTA a partial group of 16 rows, and empty token slots."""
+    """d_in a multiple of 128 (the cp.async ring for M <= 8, and for M = 9..16
+    on grids of one wave; 5003 rows make a grid of more than two CTAs per SM,
+    where M > 8 goes to the register kernel) with a d_out that leaves the last
+    CTA a partial group of 16 rows, and empty token slots."""
     d_out, d_in = shape
     wb, packed, alpha = _layer(3, d_out, d_in, True)
     x = synth.activations(3, M, d_in)
