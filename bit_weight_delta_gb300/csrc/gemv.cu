@@ -855,10 +855,13 @@ __host__ __device__ constexpr int mixed_stage_bytes() {
 }
 // Ring depth D (stages per warp): 3 while the grid's 16-row blocks fit one
 // wave at two CTAs per SM (each warp then needs two stages in flight), 2 on
-// larger grids, whose CTAs then fit four per SM: on the slice's projections
-// (8192-57344 rows, two variants) 2 stages took 4.1 -> 5.3 TB/s on 57344 x
-// 8192 and 3.0 -> 4.0 on 10240 x 8192, and 15.0 -> 16.5 µs on a 4096-row
-// layer (one wave) against 3 stages.
+// larger grids, whose CTAs then fit four per SM (52 KB of ring and no other
+// large buffer: the cross-warp sum goes through the ring): on the 40-layer
+// slice's projections (8192-57344 rows, two variants) 2 stages took 4.1 ->
+// 5.3 TB/s on 57344 x 8192 and 3.0 -> 4.0 on 10240 x 8192, and 15.0 -> 16.5
+// µs on a 4096-row layer (one wave) against 3 stages.  With a separate 4 KB
+// reduction buffer only three CTAs fitted per SM, and a grid of 512 blocks
+// (8192 x 28672, two variants) took 125 µs against 99 µs at four.
 template <int NT, int V, int D>
 constexpr size_t mixed_ring_bytes() {
   return static_cast<size_t>(D) * kKW * mixed_stage_bytes<NT, V>();
@@ -866,7 +869,7 @@ constexpr size_t mixed_ring_bytes() {
 
 template <int NT, int V, int D>
 __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const MixedGroup& grp,
-                                                       float* red, uint8_t* ring, bool w_ahead) {
+                                                       uint8_t* ring, bool w_ahead) {
   constexpr int CPS = kCPS;
   constexpr int R = kStageRows;  // 16 W rows
   static_assert(R == 16 && V % 2 == 0, "two 8-row halves; variants copied in pairs");
@@ -1054,7 +1057,12 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
   cp_async_wait<0>();
 
   // y_part = acc_b + α_v[n]·acc_s[v], v the token's own variant (fragment
-  // rows: W rows n0+g, n0+8+g; columns: tokens 8nt + 2t, 8nt + 2t + 1)
+  // rows: W rows n0+g, n0+8+g; columns: tokens 8nt + 2t, 8nt + 2t + 1).
+  // Each warp leaves its part at the head of its own ring, which it has
+  // finished reading and has no copy in flight to; no separate reduction
+  // buffer keeps the CTA small enough for four per SM with two stages.
+  __syncwarp();  // every lane has read its last stage and seen its copies land
+  float* red = reinterpret_cast<float*>(wring);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -1071,12 +1079,29 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
         const float* al = p.alpha_table[grp.vars[mv] - 1];
         val = fmaf(p.per_row ? __ldg(al + n) : __ldg(al), sv, val);
       }
-      red[(warp * NT * 4 + nt * 4 + e) * 32 + lane] = val;
+      red[(nt * 4 + e) * 32 + lane] = val;
     }
   }
   __syncthreads();
-  if (warp == 0) store_group_rows_t<NT>(p, grp, red, n0, lane);
-  __syncthreads();
+  if (warp == 0) {
+    // the kKW warps' parts summed in warp order, as store_group_rows_t does
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = 0.f;
+        for (int w = 0; w < kKW; ++w)
+          v += reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * D * kSB)
+              [(nt * 4 + e) * 32 + lane];
+        const int64_t n = n0 + g + 8 * (e >> 1);
+        const int row = grp.rows[8 * nt + 2 * t + (e & 1)];
+        if (row < 0 || n >= d_out) continue;
+        p.y[static_cast<int64_t>(row) * d_out + n] =
+            static_cast<uint16_t>(pack_bf16x2_rn(v, 0.f) & 0xFFFFu);
+      }
+    }
+  }
+  __syncthreads();  // the rings are refilled by the next group
 }
 
 // The short rows of a grouped call (segments of at most max_short rows),
@@ -1175,7 +1200,8 @@ __device__ __forceinline__ void mixed_issue_w(const GemvArgs& p, uint8_t* ring) 
 template <int NG, int kAsyncNT, int V, int D>
 __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     gemv_grouped_kernel(GemvArgs p, int ring_off) {
-  __shared__ float red[kKW * NG * 4 * 32];
+  // the ring pass reduces through its ring; only the register pass needs this
+  __shared__ float red[kAsyncNT > 0 ? 1 : kKW * NG * 4 * 32];
   extern __shared__ __align__(16) int32_t dyn[];
   griddep_launch_dependents();
   if constexpr (kAsyncNT > 0)
@@ -1235,7 +1261,7 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     if constexpr (kAsyncNT > 0) {
       // the ring (d_in % 128 == 0): unaligned variant tables included; the
       // first group's W rows were issued before the dependency wait
-      gemv_group_mixed_async<kAsyncNT, V, D>(p, mg, red,
+      gemv_group_mixed_async<kAsyncNT, V, D>(p, mg,
                                              reinterpret_cast<uint8_t*>(dyn) + ring_off, first);
       first = false;
     } else {
