@@ -1279,24 +1279,28 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
 // The short rows of a grouped call when there can be more of them than one
 // group holds: up to kWideTok rows of up to kWideVars delta variants (and any
 // number of base rows) in ONE pass over the CTA's 16 W_base rows, instead of
-// one pass per group of 16 rows and 4 variants.  The rows, in bucket
-// (variant) order, are cut into tiles of at most 8 rows of ONE variant, so a
-// tile needs one sign product and no masking: y = x·W_baseᵀ + α_v ⊙ (x·S_vᵀ)
-// with the two products in separate accumulators over all of d_in and α
-// applied once at the end, as in the other decode kernels.  The CTA shares
-// one cp.async ring of 128-column stages, each holding the W_base row
-// segments, the sign words of every variant of the pass and the x segments of
-// every row; warp w owns tiles w, w + W, ... (W warps) over all columns (no
-// cross-warp sum) and reads each W_base fragment once for its tiles.  The
-// inner loop has no data-dependent branch: a base tile takes the sign
-// product of the pass's first variant slot (±1 values, so finite) and
-// scales it by α = 0, and lanes past a tile's rows compute on its first row.
-// Measured on 14336 x 4096 with 14 variants: a pass over 64 rows in 158 µs
-// against 274 µs for the groups of 16 rows and 4 variants; tracking the
-// variant of the previous tile to skip a conversion, and predicated zero
-// operands, each cost more issue slots than they saved (208 µs), and so did
-// a tile loop with an exit on the warp's tile count (173 µs: the compiler
-// cannot interleave tiles across the exits), hence one body per count.
+// one pass per group of 16 rows and 4 variants.  y = x·W_baseᵀ + α_v ⊙
+// (x·S_vᵀ), the two products in separate accumulators over all of d_in and α
+// applied once at the end, as in the other decode kernels.  The base product
+// runs over the pass's rows in dense groups of 8; the sign product per tile
+// of at most 8 rows of ONE variant (the rows in bucket order; base rows have
+// no tile), so no masking is needed.  The CTA shares one cp.async ring of
+// 128-column stages, each holding the W_base row segments, the sign words of
+// every variant of the pass and the x segments of every row; warp w owns
+// groups and tiles w, w + W, ... (W warps) over all columns and reads each
+// W_base fragment once for them.  At the end the base sums meet the sign
+// products through shared memory.  The inner loop has no data-dependent
+// branch, and lanes past a tile's rows compute on its first row.
+// On 14336 x 4096 with 14 variants and 64 rows, where the legacy tensor path
+// (mma.sync m16n8k16, measured at most ~600 TFLOP/s on this part) bounds the
+// pass: 274 µs for groups of 16 rows and 4 variants; 158 µs for one pass with
+// a base product per tile (tiles of ~4 rows, so half of each n8 product
+// wasted, and a useless sign product on base tiles); 151 µs with the dense
+// base groups (27% fewer MMAs).  Tracking the variant of the previous tile
+// to skip a conversion, and predicated zero operands, each cost more issue
+// slots than they saved (208 µs), and so did a tile loop with an exit on the
+// warp's tile count (173 µs: the compiler cannot interleave tiles across the
+// exits), hence one body per count; eight warps per CTA took 161 µs.
 constexpr int kWideTok = 64;    // rows of x per pass (the ring's x segments)
 constexpr int kWideTiles = 16;  // tiles of at most 8 rows of one variant per pass
 #ifndef BD_WIDE_WARPS
@@ -1316,6 +1320,7 @@ struct WidePass {
   int32_t tile_n[kWideTiles];     // row slots of the tile (1..8; 0 = no tile)
   int32_t tile_var[kWideTiles];   // index into vars[] of the tile's variant, −1 = base
   int32_t n_tok, n_vars, n_tiles;
+  int32_t n_base;      // the first n_base row slots are base-model rows (no tile)
   uint32_t unaligned;  // bit v: variant v's sign table is off the copy size (C/8 bytes)
 };
 // A ring stage of C columns (64 or 128): W_base row segments (16 × 2C
@@ -1429,21 +1434,33 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
     cp_async_commit();  // one group per stage, empty past the end
   };
 
-  // compute side: this warp's tiles warp + kWideWarps·k.  The lane's B
-  // column is row slot r0 + g of the tile; lanes past the tile's rows read
-  // its first row instead (their columns of the products are never stored),
-  // and W rows past d_out hold whatever the ring held (their rows of the
-  // products are never stored either), so no fragment read needs a select.
-  // Per tile: byte offsets within a stage of the lane's x row and of its
-  // sign bytes (rows g, g + 8), and the x row's swizzle (64 bytes on odd
-  // rows: the word index XOR 4).
+  // compute side.  Base products over the pass's row slots in groups of 8
+  // (group q: slots 8q .. 8q+7), warp w owning groups w, w + W (W warps);
+  // sign products per tile of one delta variant (base rows have none), warp
+  // w owning tiles w, w + W, ....  Groups and tiles are numbered densely, so
+  // a warp's are a prefix of its list.  The lane's B column is slot 8q + g
+  // (group) or r0 + g (tile; lanes past a tile's rows read its first row,
+  // and their columns of the products are never stored); W rows past d_out
+  // and empty slots hold whatever the ring held, and feed only products
+  // that are never stored, so no fragment read needs a select.
+  constexpr int GW = kWideTok / 8 / kWideWarps;  // groups per warp
+  int goff[GW], gpar[GW];
+  int my_groups = 0;
+#pragma unroll
+  for (int q = 0; q < GW; ++q) {
+    const int grp = warp + kWideWarps * q;
+    const int xs = 8 * grp + g;
+    goff[q] = kXOff + 16 * (xs * WPR + t);
+    gpar[q] = (xs & 1) << 6;
+    my_groups += 8 * grp < n_tok ? 1 : 0;
+  }
   int tvar[TW], xoff[TW], xpar[TW], soff[TW];
-  bool have[TW];
+  int my_tiles = 0;
 #pragma unroll
   for (int k = 0; k < TW; ++k) {
     const int kt = warp + kWideWarps * k;
     const int n = wp.tile_n[kt];
-    have[k] = n > 0;
+    my_tiles += n > 0 ? 1 : 0;
     tvar[k] = wp.tile_var[kt];
     const int xs = wp.tile_r0[kt] + (g < n ? g : 0);
     xoff[k] = kXOff + 16 * (xs * WPR + t);
@@ -1451,16 +1468,17 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
     const int vs = tvar[k] > 0 ? tvar[k] : 0;
     soff[k] = kSOff + SB * (vs * 16 + g) + t;
   }
-  int my_tiles = 0;  // tiles are numbered densely, so this warp's are k < my_tiles
-#pragma unroll
-  for (int k = 0; k < TW; ++k) my_tiles += have[k] ? 1 : 0;
   const int w_off0 = 16 * (g * WPR + t), w_off1 = 16 * ((g + 8) * WPR + t);
   const int wpar = (g & 1) << 6;
-  float acc_b[TW][4], acc_s[TW][4];
+  float acc_b[GW][4], acc_s[TW][4];
+#pragma unroll
+  for (int q = 0; q < GW; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc_b[q][e] = 0.f;
 #pragma unroll
   for (int k = 0; k < TW; ++k)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc_b[k][e] = acc_s[k][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc_s[k][e] = 0.f;
 
 #pragma unroll
   for (int s = 0; s < D - 1; ++s) issue(s, s);
@@ -1470,15 +1488,21 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
     __syncthreads();         // ... everyone's; and the slot refilled next is free
     issue(slot == 0 ? D - 1 : slot - 1, sc + D - 1);
     const uint8_t* st = ring + slot * kSB;
-    // The stage's products for this warp's first NTK tiles, with NTK known
-    // at compile time: one straight-line block the compiler can interleave
-    // across tiles (a loop with an exit on the tile count cannot be).
-    auto stage = [&](auto ntk) {
-      constexpr int NTK = decltype(ntk)::value;
+    // The stage's products for this warp's first NGR groups and NTK tiles,
+    // both known at compile time: one straight-line block the compiler can
+    // interleave (a loop with an exit on a count cannot be).
+    auto stage = [&](auto ngr, auto ntk) {
+      constexpr int NGR = decltype(ngr)::value, NTK = decltype(ntk)::value;
 #pragma unroll
       for (int j = 0; j < C / 32; ++j) {  // 32-column chunks: word 4j + t of a row
         const uint4 wv0 = lds128(st + w_off0 + ((64 * j) ^ wpar));
         const uint4 wv1 = lds128(st + w_off1 + ((64 * j) ^ wpar));
+#pragma unroll
+        for (int q = 0; q < NGR; ++q) {
+          const uint4 xv = lds128(st + goff[q] + ((64 * j) ^ gpar[q]));
+          mma_16816(acc_b[q], wv0.x, wv1.x, wv0.y, wv1.y, xv.x, xv.y);
+          mma_16816(acc_b[q], wv0.z, wv1.z, wv0.w, wv1.w, xv.z, xv.w);
+        }
 #pragma unroll
         for (int k = 0; k < NTK; ++k) {
           const uint4 xv = lds128(st + xoff[k] + ((64 * j) ^ xpar[k]));
@@ -1490,44 +1514,129 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
             s0[i] = pm_one_pair(b0, i);
             s1[i] = pm_one_pair(b1, i);
           }
-          mma_16816(acc_b[k], wv0.x, wv1.x, wv0.y, wv1.y, xv.x, xv.y);
-          mma_16816(acc_b[k], wv0.z, wv1.z, wv0.w, wv1.w, xv.z, xv.w);
           mma_16816(acc_s[k], s0[0], s1[0], s0[1], s1[1], xv.x, xv.y);
           mma_16816(acc_s[k], s0[2], s1[2], s0[3], s1[3], xv.z, xv.w);
         }
       }
     };
-    static_assert(TW <= 4, "stage bodies for 1..4 tiles per warp");
-    if (my_tiles >= TW)
-      stage(std::integral_constant<int, TW>{});
-    else if (TW > 3 && my_tiles == 3)
-      stage(std::integral_constant<int, (TW > 3 ? 3 : 1)>{});
-    else if (TW > 2 && my_tiles == 2)
-      stage(std::integral_constant<int, (TW > 2 ? 2 : 1)>{});
-    else if (my_tiles == 1)
-      stage(std::integral_constant<int, 1>{});
+    static_assert(TW <= 4 && GW <= 2, "stage bodies for 0..4 tiles and 0..2 groups per warp");
+    auto tiles = [&](auto ngr) {
+      if (TW >= 4 && my_tiles >= 4)
+        stage(ngr, std::integral_constant<int, (TW >= 4 ? 4 : 0)>{});
+      else if (TW >= 3 && my_tiles == 3)
+        stage(ngr, std::integral_constant<int, (TW >= 3 ? 3 : 0)>{});
+      else if (TW >= 2 && my_tiles == 2)
+        stage(ngr, std::integral_constant<int, (TW >= 2 ? 2 : 0)>{});
+      else if (my_tiles == 1)
+        stage(ngr, std::integral_constant<int, 1>{});
+      else
+        stage(ngr, std::integral_constant<int, 0>{});
+    };
+    if (GW >= 2 && my_groups >= 2)
+      tiles(std::integral_constant<int, (GW >= 2 ? 2 : 0)>{});
+    else if (my_groups == 1)
+      tiles(std::integral_constant<int, 1>{});
+    else
+      tiles(std::integral_constant<int, 0>{});
     slot = slot == D - 1 ? 0 : slot + 1;
   }
   cp_async_wait<0>();
+  __syncthreads();  // every warp is done with the ring, which now takes the base sums
 
-  // y = acc_b + α_v[n]·acc_s; C columns 2t, 2t+1 are the tile's rows
+  // Base sums of every slot through shared memory: bsum[r][slot] for the
+  // CTA's W row r (fragment rows g, g + 8; columns 2t, 2t + 1 of a group).
+  constexpr int kBS = kWideTok + 1;  // row stride (floats)
+  float* bsum = reinterpret_cast<float*>(ring);
+#pragma unroll
+  for (int q = 0; q < GW; ++q) {
+    if (q >= my_groups) continue;
+    const int grp = warp + kWideWarps * q;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      bsum[(g + 8 * (e >> 1)) * kBS + 8 * grp + 2 * t + (e & 1)] = acc_b[q][e];
+  }
+  __syncthreads();
+  // delta rows: y = base + α_v[n]·(x·S_vᵀ); base rows (the pass's first
+  // n_base slots): y = base
 #pragma unroll
   for (int k = 0; k < TW; ++k) {
-    if (!have[k]) continue;
+    if (k >= my_tiles) continue;
     const int kt = warp + kWideWarps * k;
     const int n_rows = wp.tile_n[kt], r0 = wp.tile_r0[kt];
-    const float2 al = tvar[k] >= 0 ? al_s[tvar[k]][g] : make_float2(0.f, 0.f);
+    const float2 al = al_s[tvar[k]][g];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = 2 * t + (e & 1);
-      const int64_t n = n0 + g + 8 * (e >> 1);
+      const int r = g + 8 * (e >> 1);
+      const int64_t n = n0 + r;
       if (c >= n_rows || n >= d_out) continue;
-      const float v = fmaf((e >> 1) ? al.y : al.x, acc_s[k][e], acc_b[k][e]);
+      const float v = fmaf((e >> 1) ? al.y : al.x, acc_s[k][e], bsum[r * kBS + r0 + c]);
       p.y[static_cast<int64_t>(wp.rows[r0 + c]) * d_out + n] =
           static_cast<uint16_t>(pack_bf16x2_rn(v, 0.f) & 0xFFFFu);
     }
   }
+  for (int i = tid; i < wp.n_base * R; i += kWideThreads) {
+    const int s = i / R, r = i - s * R;
+    if (r >= rows_here) continue;
+    p.y[static_cast<int64_t>(wp.rows[s]) * d_out + n0 + r] =
+        static_cast<uint16_t>(pack_bf16x2_rn(bsum[r * kBS + s], 0.f) & 0xFFFFu);
+  }
   __syncthreads();  // the ring and the pass tables are reused by the next pass
+}
+
+// The next pass from the bucketed row list (run by one thread): rows in
+// bucket (variant) order take the pass's row slots; base rows (bucket 0)
+// first, without tiles, then each delta variant's rows cut into tiles of at
+// most 8 rows of that variant.  The pass closes when it holds kWideTok rows
+// or kWideTiles tiles, or when a (kWideVars+1)-th delta variant would join.
+// A variant whose sign table does not start on a `copy_bytes` boundary is
+// flagged in wp.unaligned (its signs are then fetched with plain loads).
+__device__ void form_wide_pass(const GemvArgs& p, const int32_t* start, const int32_t* rows,
+                               int32_t total, int copy_bytes, int32_t& cursor, int32_t& bucket,
+                               WidePass& wp) {
+  int n = 0, nvars = 0, ntl = 0, n_base = 0;
+  uint32_t unal = 0;
+  int32_t c = cursor, bk = bucket;
+  while (c < total && n < kWideTok && ntl < kWideTiles) {
+    while (c >= start[bk + 1]) ++bk;  // the bucket (variant) of sorted row c
+    const int32_t end = start[bk + 1];
+    if (bk == 0) {  // base rows (bucket 0, so a pass's first slots): no tile
+      while (c < end && n < kWideTok) {
+        wp.rows[n++] = rows[c++];
+        ++n_base;
+      }
+      continue;
+    }
+    if (nvars == kWideVars) break;
+    const int vslot = nvars;
+    wp.vars[nvars] = bk;
+    if ((reinterpret_cast<uintptr_t>(p.packed_table[bk - 1]) & (copy_bytes - 1)) != 0)
+      unal |= 1u << nvars;
+    ++nvars;
+    while (c < end && n < kWideTok && ntl < kWideTiles) {
+      int32_t cnt = end - c;
+      cnt = cnt < 8 ? cnt : 8;
+      cnt = cnt < kWideTok - n ? cnt : kWideTok - n;
+      wp.tile_r0[ntl] = n;
+      wp.tile_n[ntl] = cnt;
+      wp.tile_var[ntl] = vslot;
+      ++ntl;
+      for (int32_t i = 0; i < cnt; ++i) wp.rows[n++] = rows[c++];
+    }
+  }
+  for (int i = n; i < kWideTok; ++i) wp.rows[i] = -1;
+  for (int k = ntl; k < kWideTiles; ++k) {
+    wp.tile_r0[k] = 0;
+    wp.tile_n[k] = 0;
+    wp.tile_var[k] = -1;
+  }
+  wp.n_tok = n;
+  wp.n_vars = nvars;
+  wp.n_tiles = ntl;
+  wp.n_base = n_base;
+  wp.unaligned = unal;
+  cursor = c;
+  bucket = bk;
 }
 
 // Requires d_in % 128 == 0.  One CTA per 16 W_base rows; every CTA buckets
@@ -1538,7 +1647,10 @@ __device__ __forceinline__ void gemv_wide_pass(const GemvArgs& p, const WidePass
 template <int C, int D>
 __global__ void __launch_bounds__(kWideThreads,
                                   (wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3) * 128 /
-                                      kWideThreads)
+                                      kWideThreads > 0
+                                      ? (wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3) * 128 /
+                                            kWideThreads
+                                      : 2)
     gemv_wide_kernel(GemvArgs p, int ring_off) {
   extern __shared__ __align__(16) int32_t dyn[];
   __shared__ WidePass wp;
@@ -1559,46 +1671,7 @@ __global__ void __launch_bounds__(kWideThreads,
   }
   __syncthreads();
   while (cursor < total) {
-    if (threadIdx.x == 0) {
-      int n = 0, nvars = 0, ntl = 0;
-      uint32_t unal = 0;
-      int32_t c = cursor, bk = bucket;
-      while (c < total && n < kWideTok && ntl < kWideTiles) {
-        while (c >= start[bk + 1]) ++bk;  // the bucket (variant) of sorted row c
-        int vslot = -1;
-        if (bk > 0) {
-          if (nvars == kWideVars) break;
-          vslot = nvars;
-          wp.vars[nvars] = bk;
-          if ((reinterpret_cast<uintptr_t>(p.packed_table[bk - 1]) & (C / 8 - 1)) != 0)
-            unal |= 1u << nvars;
-          ++nvars;
-        }
-        const int32_t end = start[bk + 1];
-        while (c < end && n < kWideTok && ntl < kWideTiles) {
-          int32_t cnt = end - c;
-          cnt = cnt < 8 ? cnt : 8;
-          cnt = cnt < kWideTok - n ? cnt : kWideTok - n;
-          wp.tile_r0[ntl] = n;
-          wp.tile_n[ntl] = cnt;
-          wp.tile_var[ntl] = vslot;
-          ++ntl;
-          for (int32_t i = 0; i < cnt; ++i) wp.rows[n++] = rows[c++];
-        }
-      }
-      for (int i = n; i < kWideTok; ++i) wp.rows[i] = -1;
-      for (int k = ntl; k < kWideTiles; ++k) {
-        wp.tile_r0[k] = 0;
-        wp.tile_n[k] = 0;
-        wp.tile_var[k] = -1;
-      }
-      wp.n_tok = n;
-      wp.n_vars = nvars;
-      wp.n_tiles = ntl;
-      wp.unaligned = unal;
-      cursor = c;
-      bucket = bk;
-    }
+    if (threadIdx.x == 0) form_wide_pass(p, start, rows, total, C / 8, cursor, bucket, wp);
     __syncthreads();
     for (int i = threadIdx.x; i < wp.n_vars * 16; i += blockDim.x) {
       const int v = i >> 4, r = i & 15;

@@ -145,3 +145,43 @@ def test_wide_short_rows_beside_long_segments(n_short):
     dp, da = [to_dev(p) for p in packs], [to_dev(a) for a in alphas]
     y = _call(x, off, var, wb, dp, da, n_var, False)
     _check_segments(y, x, off, var, wb, packs, alphas, False)
+
+
+@pytest.mark.parametrize("shape,n_var,n_rows,per_row", [
+    ((12500, 256), 10, 150, True),   # 782 blocks of 16 rows, the last one of 4 rows
+    ((10000, 384), 20, 70, False),   # 625 blocks
+])
+def test_wide_pass_multi_wave_layers(shape, n_var, n_rows, per_row):
+    """Layers of several CTA waves (more than four 16-row blocks per SM):
+    a partial last block, several passes and the variant cap, element-wise."""
+    d_out, d_in = shape
+    wb = synth.base_weight(75, d_out, d_in)
+    packs, alphas = _variants(75, wb, n_var, per_row)
+    rng = np.random.default_rng(75 + d_out)
+    var = rng.integers(0, n_var + 1, size=n_rows).astype(np.int32)
+    off = _offsets([1] * n_rows)
+    x = synth.activations(75, int(off[-1]), d_in)
+    dp, da = [to_dev(p) for p in packs], [to_dev(a) for a in alphas]
+    y = _call(x, off, var, wb, dp, da, n_var, per_row)
+    _check_segments(y, x, off, var, wb, packs, alphas, per_row)
+
+
+def test_wide_pass_multi_wave_unaligned_signs_and_segments():
+    """A multi-wave layer with one variant's signs 8 bytes off a 16-byte boundary,
+    short segments of several rows (one variant over several tiles) and a
+    long segment on the tensor-core kernel."""
+    d_out, d_in, n_var = 12500, 256, 4
+    wb = synth.base_weight(76, d_out, d_in)
+    packs, alphas = _variants(76, wb, n_var, True)
+    dp = [to_dev(p) for p in packs]
+    raw = torch.empty(packs[2].size + 16, dtype=torch.uint8, device="cuda")
+    shifted = raw[8:8 + packs[2].size].view(packs[2].shape)
+    shifted.copy_(dp[2])
+    dp[2] = shifted
+    da = [to_dev(a) for a in alphas]
+    lengths = [16, 9, 1, 300, 12, 16, 3]
+    var = np.array([3, 3, 0, 1, 2, 4, 3], np.int32)
+    off = _offsets(lengths)
+    x = synth.activations(76, int(off[-1]), d_in)
+    y = _call(x, off, var, wb, dp, da, n_var, True)
+    _check_segments(y, x, off, var, wb, packs, alphas, True)
