@@ -891,6 +891,50 @@ class DeltaCacheLoads:
         self.cache.close()
 
 
+class DecodeLarge:
+    """bitdelta_linear decode on the 40-layer slice's largest projection
+    (gate+up, W_base 8192 -> 57344, 940 MB per layer), per-row α, at M = 1, 8
+    and 16, two distinct layers alternating (1.9 GB, far beyond L2): the
+    kernel's steady-state streaming rate, without the per-launch ramp that
+    bounds the 4096 x 4096 layers of the headline sweep."""
+
+    name = "decode_large_57344x8192_alpha_per_row_M1_8_16_2layers"
+    d_out, d_in, n_layers = 57344, 8192, 2
+
+    def __init__(self, bd, seed: int = 6):
+        import synth.device as sd
+        self.bd = bd
+        self.layers = []
+        for l in range(self.n_layers):
+            wb = sd.normal_bf16((self.d_out, self.d_in), seed, 2 * l + 1, 0.02)
+            wf = sd.finetuned_bf16(wb, seed, 2 * l + 2, 1e-3)
+            p, a = bd.bitdelta_compress(wb, wf, per_row=True)
+            del wf
+            self.layers.append((wb, p, a))
+        self.x = sd.normal_bf16((16, self.d_in), seed, 99)
+
+    def report(self, peaks, reps: int = 4):
+        out = {"workload": self.name}
+        for M in (1, 8, 16):
+            y = torch.empty((M, self.d_out), dtype=torch.bfloat16, device="cuda")
+            x = self.x[:M]
+
+            def f():
+                for _ in range(reps):
+                    for wb, p, a in self.layers:
+                        self.bd.bitdelta_linear(x, wb, p, a, per_row=True, out=y)
+
+            ms = graph_ms(f) / (reps * self.n_layers)
+            byts = (self.d_out * self.d_in * (2 + 1 / 8) + 4 * self.d_out
+                    + 2 * M * (self.d_in + self.d_out))
+            gbs = byts / (ms * 1e-3) / 1e9
+            out[f"M{M}"] = {"us_per_launch": ms * 1e3, "GB/s": gbs,
+                            "roofline": hbm_roofline(gbs, peaks),
+                            "kernel": "gemv_single_async_kernel" if M <= 8
+                            else "gemv_single_kernel (grid of 3584 CTAs: several waves)"}
+        return out
+
+
 class KMergeSimilarity:
     """K-Merge's first step on the grouped workload's layer (W_base
     4096->14336, 14 variants): the cosine similarity of variant 1's 1-bit task
@@ -1336,7 +1380,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workloads", default="all", help="comma list: prefill,grouped or all|none")
+    ap.add_argument("--workloads", default="all", help="comma list of tiny,prefill,grouped,slice40,decode_large,"
+                         "cache,kmerge,monosoup; or all|none")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true",
@@ -1386,7 +1431,7 @@ def main():
 
     workloads = {}
     wanted = set(args.workloads.split(",")) if args.workloads not in ("all", "none") else (
-        {"tiny", "prefill", "grouped", "slice40", "cache", "kmerge", "monosoup"}
+        {"tiny", "prefill", "grouped", "slice40", "decode_large", "cache", "kmerge", "monosoup"}
         if args.workloads == "all"
         else set())
     cpu_on = rank == 0 and not args.no_cpu
@@ -1440,6 +1485,11 @@ def main():
         sl = Slice40(bd)
         workloads["slice40"] = sl.report(peaks, cpu=cpu_on)
         del sl
+        torch.cuda.empty_cache()
+    if "decode_large" in wanted:
+        dl = DecodeLarge(bd)
+        workloads["decode_large"] = dl.report(peaks)
+        del dl
         torch.cuda.empty_cache()
     if "kmerge" in wanted:
         km = KMergeSimilarity(bd)
