@@ -317,9 +317,11 @@ constexpr int kStageRows = 8 * kNG;  // W rows of a CTA
 // and a load issued one iteration ahead would not hide that latency).
 template <int NT>
 __host__ __device__ constexpr int stage_bytes() { return kStageRows * 256 + kStageRows * 16 + NT * 8 * 256; }
-// Ring depth: two CTAs per SM (a ~100 KB ring each).
-// Ring depth of the M <= 8 kernel: 3 stages (77 KB per CTA) measured a few
-// percent faster than 4 on 4096 x 4096 layers, 2 far slower.
+// Ring depth: two CTAs per SM.  With one token tile (M <= 8) 3 stages (77 KB
+// per CTA) measured a few percent faster than 4 on 4096 x 4096 layers and 2
+// far slower there (12.1 against 7.4 µs at M = 1); 2 stages at four CTAs
+// per SM gained 2% on 57344 x 8192 and lost 7% on 8192 x 28672.  Two token
+// tiles (M = 9..16, one-wave grids only): 3 stages, 101 KB.
 #ifndef BD_GEMV_RING_STAGES
 #define BD_GEMV_RING_STAGES 3
 #endif
@@ -1337,6 +1339,16 @@ constexpr size_t wide_ring_bytes() {
   return static_cast<size_t>(D) * wide_stage_bytes<C>();
 }
 
+// CTAs per SM the wide kernel is compiled for (registers per thread capped
+// so that they fit): as many of four-warp CTAs as the ring leaves room for,
+// three with the 72 KB ring of three 128-column stages.
+template <int C, int D>
+constexpr int wide_min_blocks() {
+  const int by_smem = wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3;
+  const int b = by_smem * 128 / kWideThreads;
+  return b > 0 ? b : 1;
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t* a) {
   return *reinterpret_cast<const uint4*>(a);
 }
@@ -1645,12 +1657,7 @@ __device__ void form_wide_pass(const GemvArgs& p, const int32_t* start, const in
 // variant, closing the pass when it holds kWideTok rows or kWideTiles tiles,
 // or when a (kWideVars+1)-th delta variant would join.
 template <int C, int D>
-__global__ void __launch_bounds__(kWideThreads,
-                                  (wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3) * 128 /
-                                      kWideThreads > 0
-                                      ? (wide_ring_bytes<C, D>() <= 50 * 1024 ? 4 : 3) * 128 /
-                                            kWideThreads
-                                      : 2)
+__global__ void __launch_bounds__(kWideThreads, wide_min_blocks<C, D>())
     gemv_wide_kernel(GemvArgs p, int ring_off) {
   extern __shared__ __align__(16) int32_t dyn[];
   __shared__ WidePass wp;
