@@ -110,10 +110,13 @@ bool tc_shape_ok(int64_t rows_x, int64_t d_out, int64_t d_in) {
   return d_in % 128 == 0 && d_in < INT32_MAX && d_out < INT32_MAX && rows_x < INT32_MAX;
 }
 
-// Cost of one 512-token pair tile in 256-token pair tiles, in quarters: the
+// Cost of one 512-token pair tile in 256-token pair tiles, in eighths: the
 // steady state of the two kernels on 8192 x 57344 at M = 2048 measured 1454
-// and 1266 TFLOP/s, 2 x 1266 / 1454 = 1.74.
-constexpr int64_t kWideTileCost4 = 7;
+// and 1266 TFLOP/s (2 x 1266 / 1454 = 1.74); on 8192 x 10240 three rounds of
+// 512-token tiles took 300.6 µs against 308.0 for five rounds of 256-token
+// tiles (1.64).  13/8 picks the 512-token tile there and leaves every other
+// benchmark shape's choice as it was.
+constexpr int64_t kWideTileCost8 = 13;
 
 // 512-token pair tiles for this call?  Under BD_PREFILL_TILE_AUTO the width
 // whose rounds of tiles over the device's pairs cost less, ceil(tiles /
@@ -137,7 +140,7 @@ bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens) {
     const int64_t tiles = row_tiles * ((rows_x + tok - 1) / tok);
     return (tiles + pairs - 1) / pairs;
   };
-  return rounds(true) * kWideTileCost4 <= rounds(false) * 4;
+  return rounds(true) * kWideTileCost8 <= rounds(false) * 8;
 }
 
 // Launch the tensor-core kernel on g (x has rows_x rows, of which the
