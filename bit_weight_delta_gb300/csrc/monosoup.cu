@@ -788,8 +788,8 @@ struct MsRunner {
   // out_i = Δ_i·V_i (trans: Δ_iᵀ·V_i) for every checkpoint i; V_i at
   // v + i·v_stride (one V for all when v_stride is 0), out_i at
   // out + i·out_stride.  V is first split into three bf16 terms; the product
-  // is split over the contracted side so that the grid is about one even
-  // wave; *n_split = 0 when the outputs are complete, else the number of
+  // is split over the contracted side so that the grid is about two even
+  // waves; *n_split = 0 when the outputs are complete, else the number of
   // partials left in L.part.
   cudaError_t delta_mul(bool trans, const float* v, int64_t v_stride, float* out,
                         int64_t out_stride, int* n_split) const {
@@ -817,7 +817,11 @@ struct MsRunner {
     const int occ = resident_ctas<kT>();
     if (occ < 0) return cudaErrorInvalidConfiguration;
     const int64_t a_blocks = (A + kTileA - 1) / kTileA;
-    const int64_t want = static_cast<int64_t>(occ) * num_sms;
+    // two waves' worth of CTAs: the products are bound per SM (legacy tensor
+    // path and its operand traffic), and 1024 CTAs over 608 slots leave each
+    // SM within one CTA of the mean where one wave of 512 left 3 or 4 per SM
+    // (716 -> 675 µs per 4096 x 4096, k = 4, rank-32 merge; three waves 680)
+    const int64_t want = static_cast<int64_t>(occ) * num_sms * 2;
     int64_t split = want / (a_blocks * a.k);
     const int64_t split_max = kMaxSplit / a.k > 1 ? kMaxSplit / a.k : 1;
     if (split > split_max) split = split_max;
