@@ -338,6 +338,26 @@ __device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
 // x rows are read by every CTA at the same K position at about the same
 // time: keep them in L1 too (.ca), so the CTAs of an SM fetch each line from
 // L2 once instead of every warp queueing on the same few L2 lines.
+// CTA pairs (clusters of two) for the grouped pass split over d_in.
+__device__ __forceinline__ uint32_t pair_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void pair_store_f32(const float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+// Every thread of both CTAs: release of the CTA's shared-memory writes
+// (local and remote), acquire of the other's.
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 __device__ __forceinline__ void cp_async_16_x(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -869,9 +889,9 @@ constexpr size_t mixed_ring_bytes() {
   return static_cast<size_t>(D) * kKW * mixed_stage_bytes<NT, V>();
 }
 
-template <int NT, int V, int D>
+template <int NT, int V, int D, bool kSplit>
 __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const MixedGroup& grp,
-                                                       uint8_t* ring, bool w_ahead) {
+                                                       uint8_t* ring, bool w_ahead, float* xfer) {
   constexpr int CPS = kCPS;
   constexpr int R = kStageRows;  // 16 W rows
   static_assert(R == 16 && V % 2 == 0, "two 8-row halves; variants copied in pairs");
@@ -883,7 +903,11 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
   const int g = lane >> 2, t = lane & 3;
   const int64_t d_in = p.d_in, d_out = p.d_out;
   const int64_t row_bytes = d_in / 8;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+  // kSplit: CTAs 2b and 2b + 1 (one cluster) share row block b, CTA `half`
+  // taking the stages half·kKW + warp + 2·kKW·i
+  const int half = kSplit ? static_cast<int>(pair_rank()) : 0;
+  constexpr int kStep = kSplit ? 2 * kKW : kKW;
+  const int64_t n0 = static_cast<int64_t>(kSplit ? blockIdx.x >> 1 : blockIdx.x) * R;
   const int64_t rows_here = d_out - n0 < R ? d_out - n0 : R;
   const int nv = grp.n_vars;
 
@@ -986,7 +1010,7 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
   // then waits until at most D-1 are pending: for i < D-1 that leaves only
   // groups newer than stage i's signs and x, later only groups newer than
   // stage i, so stage i has landed either way.
-  int64_t next = warp;
+  int64_t next = half * kKW + warp;
 #pragma unroll
   for (int s = 0; s < D - 1; ++s) {
     if (w_ahead) {
@@ -995,13 +1019,13 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
     } else {
       issue(s, next);
     }
-    next += kKW;
+    next += kStep;
   }
   int s_rd = 0;
-  for (int64_t sc = warp; sc < n_sc; sc += kKW) {
+  for (int64_t sc = half * kKW + warp; sc < n_sc; sc += kStep) {
     __syncwarp();  // every lane is done reading the slot refilled next
     issue(s_rd == 0 ? D - 1 : s_rd - 1, next);
-    next += kKW;
+    next += kStep;
     cp_async_wait<D - 1>();
     __syncwarp();
     const uint8_t* st = wring + s_rd * kSB;
@@ -1085,25 +1109,44 @@ __device__ __forceinline__ void gemv_group_mixed_async(const GemvArgs& p, const 
     }
   }
   __syncthreads();
+  // the kKW warps' parts summed in warp order, as store_group_rows_t does;
+  // kSplit: CTA 1 hands its sums to CTA 0, which adds them after its own
+  float v[NT][4];
   if (warp == 0) {
-    // the kKW warps' parts summed in warp order, as store_group_rows_t does
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float v = 0.f;
+        float a = 0.f;
         for (int w = 0; w < kKW; ++w)
-          v += reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * D * kSB)
+          a += reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * D * kSB)
               [(nt * 4 + e) * 32 + lane];
+        v[nt][e] = a;
+        if (kSplit && half == 1) pair_store_f32(xfer + (nt * 4 + e) * 32 + lane, 0, a);
+      }
+    }
+  }
+  if constexpr (kSplit) pair_sync();  // CTA 1's sums are in CTA 0's xfer
+  if (warp == 0 && half == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = kSplit ? v[nt][e] + xfer[(nt * 4 + e) * 32 + lane] : v[nt][e];
         const int64_t n = n0 + g + 8 * (e >> 1);
         const int row = grp.rows[8 * nt + 2 * t + (e & 1)];
         if (row < 0 || n >= d_out) continue;
         p.y[static_cast<int64_t>(row) * d_out + n] =
-            static_cast<uint16_t>(pack_bf16x2_rn(v, 0.f) & 0xFFFFu);
+            static_cast<uint16_t>(pack_bf16x2_rn(a, 0.f) & 0xFFFFu);
       }
     }
   }
-  __syncthreads();  // the rings are refilled by the next group
+  // the rings are refilled by the next group (and, kSplit, CTA 0 is done
+  // with xfer before CTA 1 writes it again)
+  if constexpr (kSplit)
+    pair_sync();
+  else
+    __syncthreads();
 }
 
 // The short rows of a grouped call (segments of at most max_short rows),
@@ -1164,21 +1207,23 @@ __device__ bool bucket_short_rows(const GemvArgs& p, int32_t* dyn) {
 // of gemv_group_mixed_async (same slots and copy mapping), one commit group
 // per stage.  W_base is never the output of a kernel still in flight, so
 // this runs before the grouped kernel waits for the previous kernel.
-template <int NT, int V, int D>
+template <int NT, int V, int D, bool kSplit>
 __device__ __forceinline__ void mixed_issue_w(const GemvArgs& p, uint8_t* ring) {
   constexpr int R = kStageRows;
   constexpr int kSB = mixed_stage_bytes<NT, V>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cr = lane >> 4, cw = lane & 15;
   const int64_t d_in = p.d_in;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int half = kSplit ? static_cast<int>(pair_rank()) : 0;
+  constexpr int kStep = kSplit ? 2 * kKW : kKW;
+  const int64_t n0 = static_cast<int64_t>(kSplit ? blockIdx.x >> 1 : blockIdx.x) * R;
   const int64_t rows_here = p.d_out - n0 < R ? p.d_out - n0 : R;
   const int64_t n_sc = d_in / (32 * kCPS);
   const uint32_t wring_sa = smem_addr(ring + static_cast<size_t>(warp) * D * kSB);
   const uint16_t* const wsrc0 = p.w + (n0 + cr) * d_in + 8 * cw;
 #pragma unroll
   for (int s = 0; s < D - 1; ++s) {
-    const int64_t sc = warp + static_cast<int64_t>(s) * kKW;
+    const int64_t sc = half * kKW + warp + static_cast<int64_t>(s) * kStep;
     if (sc < n_sc) {
       const int64_t kc0 = sc * 32 * kCPS;
       const uint32_t st = wring_sa + s * kSB;
@@ -1199,15 +1244,19 @@ __device__ __forceinline__ void mixed_issue_w(const GemvArgs& p, uint8_t* ring) 
 // columns for every group.
 // One token tile with a two-stage ring: four CTAs per SM, so at most 128
 // registers per thread.
-template <int NG, int kAsyncNT, int V, int D>
+// kSplit (ring pass only): launched in clusters of two CTAs that share a row
+// block and split d_in (see gemv_group_mixed_async).
+template <int NG, int kAsyncNT, int V, int D, bool kSplit = false>
 __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     gemv_grouped_kernel(GemvArgs p, int ring_off) {
   // the ring pass reduces through its ring; only the register pass needs this
   __shared__ float red[kAsyncNT > 0 ? 1 : kKW * NG * 4 * 32];
+  // kSplit: CTA 1's sums, written into CTA 0's copy of this array
+  __shared__ float xfer[kSplit ? (kAsyncNT > 0 ? kAsyncNT : 1) * 4 * 32 : 1];
   extern __shared__ __align__(16) int32_t dyn[];
   griddep_launch_dependents();
   if constexpr (kAsyncNT > 0)
-    mixed_issue_w<kAsyncNT, V, D>(p, reinterpret_cast<uint8_t*>(dyn) + ring_off);
+    mixed_issue_w<kAsyncNT, V, D, kSplit>(p, reinterpret_cast<uint8_t*>(dyn) + ring_off);
   griddep_wait();
   if (!bucket_short_rows(p, dyn)) {
     cp_async_wait<0>();  // no copy may land after the CTA has left
@@ -1263,8 +1312,8 @@ __global__ void __launch_bounds__(kKW * 32, (kAsyncNT == 1 && D == 2) ? 4 : 1)
     if constexpr (kAsyncNT > 0) {
       // the ring (d_in % 128 == 0): unaligned variant tables included; the
       // first group's W rows were issued before the dependency wait
-      gemv_group_mixed_async<kAsyncNT, V, D>(p, mg,
-                                             reinterpret_cast<uint8_t*>(dyn) + ring_off, first);
+      gemv_group_mixed_async<kAsyncNT, V, D, kSplit>(
+          p, mg, reinterpret_cast<uint8_t*>(dyn) + ring_off, first, xfer);
       first = false;
     } else {
       if (mg_vec)
@@ -1751,7 +1800,7 @@ cudaError_t launch_gemv(const GemvArgs& p, int num_sms, cudaStream_t stream) {
   return launch_single<kNG>(p, sign_vec, num_sms, stream);
 }
 
-template <int NT, int V, int D>
+template <int NT, int V, int D, bool kSplit = false>
 cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off, dim3 grid,
                                     cudaStream_t stream) {
   // Raise the dynamic shared-memory limit only when a call needs more than
@@ -1764,15 +1813,35 @@ cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off
   {
     std::lock_guard<std::mutex> lock(host_cache_mutex());
     if (smem > 48 * 1024 && smem > smem_set[dev]) {
-      e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT, V, D>,
+      e = cudaFuncSetAttribute(gemv_grouped_kernel<kNG, NT, V, D, kSplit>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       smem_set[dev] = smem;
     }
   }
-  return launch_pdl(gemv_grouped_kernel<kNG, NT, V, D>, grid, dim3(kKW * 32), smem, stream, p,
-                    ring_off);
+  if constexpr (kSplit) {
+    // clusters of two CTAs (one row block each pair), with programmatic
+    // dependent launch as the others
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * grid.x);
+    cfg.blockDim = dim3(kKW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<kNG, NT, V, D, true>, p, ring_off);
+  } else {
+    return launch_pdl(gemv_grouped_kernel<kNG, NT, V, D>, grid, dim3(kKW * 32), smem, stream, p,
+                      ring_off);
+  }
 }
 
 template <int C, int D>
@@ -1822,7 +1891,20 @@ cudaError_t launch_gemv_grouped(const GemvArgs& p, int64_t max_rows, int num_sms
   if (p.d_in % 128 == 0) {
     const bool two = p.n_var <= 2;
     const bool shallow = n_blocks > 2 * static_cast<int64_t>(num_sms);
+    // Row blocks split over d_in between the two CTAs of a cluster when that
+    // evens out the per-SM load of a grid of a few waves, ceil(2b / SMs) / 2
+    // against ceil(b / SMs) row blocks on the busiest SM (b = 512 on 152
+    // SMs: 3.5 against 4), and each CTA keeps a long run of stages: on 8192
+    // x 28672 (two variants, 8 rows) 99.8 -> 94.4 µs, while on 8192 x 8192
+    // the half-length CTAs lost (32.7 -> 37.0 µs) and 10240 x 8192 gained
+    // nothing.
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    const int64_t per1 = (n_blocks + sms - 1) / sms, per2 = (2 * n_blocks + sms - 1) / sms;
+    const bool split = per2 < 2 * per1 && per1 <= 8 && p.d_in >= 16384;
     if (max_rows <= 8) {
+      if (two && shallow && split && ring_off + mixed_ring_bytes<1, 2, 2>() <= kMaxDyn)
+        return launch_grouped_instance<1, 2, 2, true>(p, ring_off + mixed_ring_bytes<1, 2, 2>(),
+                                                      ro, grid, stream);
       if (two && shallow && ring_off + mixed_ring_bytes<1, 2, 2>() <= kMaxDyn)
         return launch_grouped_instance<1, 2, 2>(p, ring_off + mixed_ring_bytes<1, 2, 2>(), ro,
                                                 grid, stream);

@@ -105,3 +105,39 @@ def test_grouped_short_rows_elementwise(d_in):
         _assert_elementwise(y[rows], ref, _bound(x[rows], wb, a.astype(np.float64), d_in),
                             f"segment {s} (variant {v})")
     assert_linear_close(y, oracle.linear_grouped(x, off, var, wb, packs, alphas, True))
+
+
+@pytest.mark.parametrize("d_out,d_in,per_row", [(5000, 16384, True), (8192, 16512, False),
+                                               (4864, 16384, True), (5000, 1024, True)])
+def test_grouped_two_variants_pair_split_elementwise(d_out, d_in, per_row):
+    """Eight one-row segments alternating two variants (the 40-layer slice's
+    decode batch) on layers of 313 and 512 row blocks with d_in >= 16384,
+    whose grids the host splits over d_in between the two CTAs of a cluster
+    (CTA 1's sums added to CTA 0's through distributed shared memory; 16512
+    leaves the two CTAs unequal runs of stages), and without the split (304
+    blocks; d_in = 1024): every output against the split form of its own
+    variant."""
+    n_var = 2
+    wb = synth.base_weight(42, d_out, d_in)
+    packs, alphas = [], []
+    for v in range(n_var):
+        wf = synth.finetuned_weight(42, wb, b=BIG_B * (0.6 + 0.4 * v), stream=300 + v)
+        p, a = oracle.compress(wb, wf, per_row)[:2]
+        packs.append(p)
+        alphas.append(a)
+    off = np.arange(9, dtype=np.int32)
+    var = np.array([1 + (r % 2) for r in range(8)], np.int32)
+    x = synth.activations(42, 8, d_in)
+    dp, da = [to_dev(p) for p in packs], [to_dev(a) for a in alphas]
+    pt, at = bd.variant_tables(dp, da, "cuda")
+    y = bf16_values(bd.bitdelta_linear_grouped(
+        to_dev_bf16(x), to_dev(off), to_dev(var), to_dev_bf16(wb), pt, at, n_var=n_var,
+        max_seg_len=1, per_row=per_row))
+    assert bd.bitdelta_check_error() == 0
+    for r in range(8):
+        v = int(var[r])
+        a = alphas[v - 1]
+        a_rows = (a if per_row else np.full(d_out, a[0], np.float32)).astype(np.float64)
+        ref = oracle.linear_split(x[r:r + 1], wb, packs[v - 1], a, per_row)
+        _assert_elementwise(y[r:r + 1], ref, _bound(x[r:r + 1], wb, a_rows, d_in),
+                            f"row {r} (variant {v})")
