@@ -1837,7 +1837,13 @@ cudaError_t launch_grouped_instance(const GemvArgs& p, size_t smem, int ring_off
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<kNG, NT, V, D, true>, p, ring_off);
+    const cudaError_t le =
+        cudaLaunchKernelEx(&cfg, gemv_grouped_kernel<kNG, NT, V, D, true>, p, ring_off);
+    if (le == cudaSuccess) return le;
+    // a device that cannot place the clusters: nothing was launched; the
+    // unsplit grid computes the same rows
+    (void)cudaGetLastError();
+    return launch_grouped_instance<NT, V, D, false>(p, smem, ring_off, grid, stream);
   } else {
     return launch_pdl(gemv_grouped_kernel<kNG, NT, V, D>, grid, dim3(kKW * 32), smem, stream, p,
                       ring_off);
