@@ -354,20 +354,23 @@ __global__ void __launch_bounds__(kRgThreads) reduce_gram_kernel(
 }
 
 // One CTA: G = Σ gpart (in order), G = L·Lᵀ over the leading r × r block,
-// T = L⁻ᵀ (RP × RP, zero outside r × r and in the columns of dropped pivots).
-// Every thread takes part in the partial sums; warp 0 alone then factorises
-// (lane L owns rows L and L + 32, warp barriers only) and inverts row by row
-// (lane L owns columns L and L + 32: row i of L⁻¹ needs only the lane's own
-// column of the rows above it, so that phase needs no barrier at all).
+// and F (RP × RP, row-major): L below the diagonal, 1 / L[i][i] on it, zero
+// outside r × r and for a dropped pivot (its row and column of L are zero
+// too).  apply_right_kernel then solves against it, so no inverse is formed
+// (the explicit triangular inverse here cost ~13 µs a launch: 672 against
+// 620 µs per 4096 x 4096, k = 4, rank-32 merge).  Every thread takes part in
+// the partial sums; warp 0 alone then factorises (rank <= 32: rows in the
+// lanes' registers, exchanged by shuffles; else lane L owns rows L and L +
+// 32 in shared memory, warp barriers only).
 template <int RP>
-__global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(
+__global__ void __launch_bounds__(kMsThreads) chol_factor_kernel(
     const float* __restrict__ gpart_all, int n_part, int r, float* __restrict__ t_all) {
   constexpr int OWN = RP > 32 ? 2 : 1;  // rows / columns per lane
   // one CTA per checkpoint
   const float* __restrict__ gpart = gpart_all + static_cast<int64_t>(blockIdx.x) * n_part * RP * RP;
   float* __restrict__ t_out = t_all + static_cast<int64_t>(blockIdx.x) * RP * RP;
   __shared__ float g[RP][RP + 1];       // G (lower part), factorised in place into L
-  __shared__ float x[RP][RP + 1];       // L⁻¹
+  __shared__ float x[RP][RP + 1];       // F, staged by the register form
   __shared__ float inv_d[RP];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -438,26 +441,12 @@ __global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(
           if (lane >= k) gr[k] = fmaf(-lij, lkj, gr[k]);
         }
       }
-      // X = L⁻¹, column `lane`: x[i] = (δ_i,lane − Σ_{m<i} L[i][m]·x[m]) · inv_d[i]
-      float xc[RP];
-#pragma unroll
-      for (int i = 0; i < RP; ++i) {
-        float s0 = lane == i ? 1.f : 0.f, s1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < i; ++m) {
-          const float lim = __shfl_sync(full, gr[m], i);  // L[i][m]
-          if (m & 1)
-            s1 = fmaf(-lim, xc[m], s1);
-          else
-            s0 = fmaf(-lim, xc[m], s0);
-        }
-        const float di = __shfl_sync(full, my_inv, i);
-        xc[i] = lane <= i ? (s0 + s1) * di : 0.f;
-      }
-      // T = Xᵀ: row `lane` of T is column `lane` of X
+      // row `lane` of F: L[lane][i] below the diagonal, 1 / L[lane][lane] on
+      // it (0 for a dropped pivot, and for rows and columns past r)
       if (lane < RP) {
 #pragma unroll
-        for (int i = 0; i < RP; ++i) x[lane][i] = (lane < r && i < r) ? xc[i] : 0.f;
+        for (int i = 0; i < RP; ++i)
+          x[lane][i] = (lane < r && i < r) ? (i < lane ? gr[i] : i == lane ? my_inv : 0.f) : 0.f;
       }
     }
     __syncthreads();
@@ -497,67 +486,54 @@ __global__ void __launch_bounds__(kMsThreads) chol_inverse_kernel(
       }
       __syncwarp();
     }
-    // X = L⁻¹: x[i][c] = (δ_ic − Σ_{c<=m<i} L[i][m]·x[m][c]) · inv_d[i]
-    for (int i = 0; i < r; ++i) {
-      const float di = inv_d[i];
-#pragma unroll
-      for (int o = 0; o < OWN; ++o) {
-        const int cc = lane + 32 * o;
-        if (cc > i) continue;
-        float s0 = cc == i ? 1.f : 0.f, s1 = 0.f;
-        int m = cc;
-        for (; m + 1 < i; m += 2) {
-          s0 = fmaf(-g[i][m], x[m][cc], s0);
-          s1 = fmaf(-g[i][m + 1], x[m + 1][cc], s1);
-        }
-        if (m < i) s0 = fmaf(-g[i][m], x[m][cc], s0);
-        x[i][cc] = (s0 + s1) * di;
-      }
-    }
   }
   __syncthreads();
   for (int q = tid; q < RP * RP; q += kMsThreads) {
     const int i = q / RP, j = q % RP;
-    t_out[q] = (i < r && j < r) ? x[j][i] : 0.f;  // T = Xᵀ
+    t_out[q] = (i < r && j < r) ? (j < i ? g[i][j] : j == i ? inv_d[i] : 0.f) : 0.f;
   }
 }
 
-// A[row] ← A[row]·T in place, one warp per row, for every checkpoint.
+// A[row] ← A[row]·L⁻ᵀ in place, one warp per row, for every checkpoint: the
+// row q with q·Lᵀ = a by forward substitution against F (see
+// chol_factor_kernel), q[c] = (a[c] − Σ_{m<c} L[c][m]·q[m]) / L[c][c]; lane
+// L owns columns L (and L + 32), each q[m] is broadcast as it is finished.
 template <int RP>
 __global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restrict__ a_all,
                                                                  int64_t a_stride, int64_t m,
-                                                                 const float* __restrict__ t_all) {
-  // checkpoint blockIdx.y: its rows and its T
+                                                                 const float* __restrict__ f_all) {
+  // checkpoint blockIdx.y: its rows and its F
   float* __restrict__ a = a_all + blockIdx.y * a_stride;
-  const float* __restrict__ t = t_all + static_cast<int64_t>(blockIdx.y) * RP * RP;
-  __shared__ float ts[RP][RP];
-  for (int q = threadIdx.x; q < RP * RP; q += kMsThreads) ts[q / RP][q % RP] = t[q];
+  const float* __restrict__ f = f_all + static_cast<int64_t>(blockIdx.y) * RP * RP;
+  __shared__ float fs[RP][RP + 1];  // padded: the lanes read a column
+  for (int q = threadIdx.x; q < RP * RP; q += kMsThreads) fs[q / RP][q % RP] = f[q];
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int PER = (RP + 31) / 32;
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMsThreads / 32) + warp; row < m;
        row += static_cast<int64_t>(gridDim.x) * (kMsThreads / 32)) {
     float* ar = a + row * RP;
-    float av[PER];
-#pragma unroll
-    for (int p = 0; p < PER; ++p) av[p] = 32 * p + lane < RP ? ar[32 * p + lane] : 0.f;
-    float out[PER];
-#pragma unroll
-    for (int p = 0; p < PER; ++p) out[p] = 0.f;
+    float sv[PER], qv[PER];
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
-      for (int src = 0; src < 32 && 32 * p + src < RP; ++src) {
-        const float ai = __shfl_sync(0xFFFFFFFFu, av[p], src);
-        const int i = 32 * p + src;
+      sv[p] = 32 * p + lane < RP ? ar[32 * p + lane] : 0.f;
+      qv[p] = 0.f;
+    }
 #pragma unroll
-        for (int o = 0; o < PER; ++o)
-          if (32 * o + lane < RP) out[o] = fmaf(ai, ts[i][32 * o + lane], out[o]);
+    for (int mm = 0; mm < RP; ++mm) {
+      const int pm = mm / 32, lm = mm % 32;
+      const float qm = __shfl_sync(0xFFFFFFFFu, sv[pm] * fs[mm][mm], lm);
+      if (lane == lm) qv[pm] = qm;
+#pragma unroll
+      for (int p = 0; p < PER; ++p) {
+        const int c = 32 * p + lane;
+        if (c > mm && c < RP) sv[p] = fmaf(-fs[c][mm], qm, sv[p]);
       }
     }
     __syncwarp();
 #pragma unroll
     for (int p = 0; p < PER; ++p)
-      if (32 * p + lane < RP) ar[32 * p + lane] = out[p];
+      if (32 * p + lane < RP) ar[32 * p + lane] = qv[p];
   }
 }
 
@@ -861,7 +837,7 @@ struct MsRunner {
   cudaError_t orth(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
     cudaError_t e = reduce_gram(m_ptr, stride, m, n_split);
     if (e != cudaSuccess) return e;
-    chol_inverse_kernel<RP><<<static_cast<unsigned>(a.k), kMsThreads, 0, s>>>(
+    chol_factor_kernel<RP><<<static_cast<unsigned>(a.k), kMsThreads, 0, s>>>(
         f(L.gpart), last_parts, a.rank, f(L.t));
     int64_t rows_blocks = (m + 7) / 8;
     if (rows_blocks > 1024) rows_blocks = 1024;
