@@ -56,6 +56,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 // Ω[c][j] = ±1 for j < r (a hash of (seed, c, j)), 0 for the padding columns.
 __global__ void sketch_fill_kernel(float* omega, int64_t d_in, int r, int rp, uint64_t seed) {
+  griddep_wait();
   const int64_t n = d_in * rp;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -66,6 +67,10 @@ __global__ void sketch_fill_kernel(float* omega, int64_t d_in, int r, int rp, ui
     z ^= z >> 31;
     omega[i] = j < r ? ((z & 1u) ? 1.f : -1.f) : 0.f;
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 // V split for the tensor-core Δ products: V (B × RP fp32, one per checkpoint
@@ -78,6 +83,7 @@ __global__ void sketch_fill_kernel(float* omega, int64_t d_in, int r, int rp, ui
 constexpr int kVTerms = 2;
 __global__ void vsplit_kernel(const float* __restrict__ v_all, int64_t v_stride, int64_t B,
                               int64_t bp, int rp, uint16_t* __restrict__ out) {
+  griddep_wait();
   const int64_t z = blockIdx.y;
   const float* __restrict__ v = v_all + z * v_stride;
   uint16_t* __restrict__ o = out + z * kVTerms * rp * bp;
@@ -104,6 +110,10 @@ __global__ void vsplit_kernel(const float* __restrict__ v_all, int64_t v_stride,
     *reinterpret_cast<uint4*>(o + static_cast<int64_t>(rp + j) * bp + b0) =
         make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -161,6 +171,7 @@ __global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
     CkptTable tab, const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
     const uint16_t* __restrict__ vs_all, int64_t vs_stride, int64_t bp,
     float* __restrict__ dst_all, int64_t dst_stride, int64_t b_chunk) {
+  griddep_wait();
   using G = MulStage<RP, kT>;
   constexpr int JT = RP / 8;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -294,6 +305,10 @@ __global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
       *reinterpret_cast<float2*>(dst + a * RP + 8 * jt + 2 * t) =
           make_float2(acc[jt][2 * h], acc[jt][2 * h + 1]);
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 // Checkpoint blockIdx.y, rows [r_lo, r_lo + kSlab) (1024 threads): A[row] = Σ_s part[s][row]
@@ -305,6 +320,7 @@ template <int RP>
 __global__ void __launch_bounds__(kRgThreads) reduce_gram_kernel(
     const float* __restrict__ part_all, int n_split, float* __restrict__ a_all,
     int64_t a_stride, int64_t m, float* __restrict__ gpart_all) {
+  griddep_wait();
   __shared__ __align__(16) float rows[kSlab][RP];
   const int tid = threadIdx.x;
   const int64_t z = blockIdx.y;  // checkpoint
@@ -351,6 +367,10 @@ __global__ void __launch_bounds__(kRgThreads) reduce_gram_kernel(
     }
     gp[q] = s0 + s1;
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 // One CTA: G = Σ gpart (in order), G = L·Lᵀ over the leading r × r block,
@@ -365,6 +385,10 @@ __global__ void __launch_bounds__(kRgThreads) reduce_gram_kernel(
 template <int RP>
 __global__ void __launch_bounds__(kMsThreads) chol_factor_kernel(
     const float* __restrict__ gpart_all, int n_part, int r, float* __restrict__ t_all) {
+  // one CTA per checkpoint, a single wave: the next launch may start at once
+  // and waits for this grid before it reads
+  griddep_launch_dependents();
+  griddep_wait();
   constexpr int OWN = RP > 32 ? 2 : 1;  // rows / columns per lane
   // one CTA per checkpoint
   const float* __restrict__ gpart = gpart_all + static_cast<int64_t>(blockIdx.x) * n_part * RP * RP;
@@ -502,6 +526,7 @@ template <int RP>
 __global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restrict__ a_all,
                                                                  int64_t a_stride, int64_t m,
                                                                  const float* __restrict__ f_all) {
+  griddep_wait();
   // checkpoint blockIdx.y: its rows and its F
   float* __restrict__ a = a_all + blockIdx.y * a_stride;
   const float* __restrict__ f = f_all + static_cast<int64_t>(blockIdx.y) * RP * RP;
@@ -535,6 +560,10 @@ __global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restri
     for (int p = 0; p < PER; ++p)
       if (32 * p + lane < RP) ar[32 * p + lane] = qv[p];
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 // Factor split for the tensor-core merge: the k checkpoints' factors
@@ -543,6 +572,7 @@ __global__ void __launch_bounds__(kMsThreads) apply_right_kernel(float* __restri
 // F_i[row][j]).  A thread converts 8 consecutive columns of one row.
 __global__ void fsplit_kernel(const float* __restrict__ f, int64_t rows, int rp, int k,
                               float scale, uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+  griddep_wait();
   const int64_t kp = static_cast<int64_t>(k) * rp;
   const int64_t n8 = rows * (kp / 8);
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n8;
@@ -564,6 +594,10 @@ __global__ void fsplit_kernel(const float* __restrict__ f, int64_t rows, int rp,
     *reinterpret_cast<uint4*>(hi + row * kp + col) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4*>(lo + row * kp + col) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
+  // the next launch may start as this grid's last CTAs finish (a trigger at
+  // the start let the next kernel's CTAs take the slots of this one's
+  // later waves)
+  griddep_launch_dependents();
 }
 
 constexpr int kMergeTile = 64;   // output rows and columns per CTA
@@ -582,6 +616,9 @@ __global__ void __launch_bounds__(kMulThreads) merge_kernel(
     const uint16_t* __restrict__ plo, const uint16_t* __restrict__ rhi,
     const uint16_t* __restrict__ rlo, int64_t kp, int64_t d_out, int64_t d_in,
     uint16_t* __restrict__ out, float* __restrict__ corr) {
+  // No early signal to dependents: this kernel writes the merged weights,
+  // which a following bitdelta_linear may read before it waits.
+  griddep_wait();
   constexpr int JT = kMergeTile / 8;
   extern __shared__ __align__(16) uint8_t sm[];
   const int tid = threadIdx.x;
@@ -785,8 +822,13 @@ struct MsRunner {
       const int64_t n = bp / 8 * RP;
       int64_t blocks = (n + 255) / 256;
       if (blocks > 2048) blocks = 2048;
-      vsplit_kernel<<<dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(nz)), 256, 0,
-                      s>>>(v, v_stride, B, bp, RP, vs);
+      {
+        const cudaError_t le =
+            launch_pdl(vsplit_kernel,
+                       dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(nz)),
+                       dim3(256), 0, s, v, v_stride, B, bp, RP, vs);
+        if (le != cudaSuccess) return le;
+      }
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -810,9 +852,13 @@ struct MsRunner {
     const int64_t dst_stride = split == 1 ? out_stride : split * A * RP;
     const dim3 grid(static_cast<unsigned>(a_blocks), static_cast<unsigned>(split),
                     static_cast<unsigned>(a.k));
-    delta_mul_kernel<RP, kT><<<grid, kMulThreads, mul_smem_bytes<RP, kT>(), s>>>(
-        tab, a.w_base, a.d_out, a.d_in, vs, v_stride == 0 ? 0 : kVTerms * RP * bp, bp, dst,
-        dst_stride, b_chunk);
+    {
+      const cudaError_t le =
+          launch_pdl(delta_mul_kernel<RP, kT>, dim3(grid), dim3(kMulThreads),
+                     mul_smem_bytes<RP, kT>(), s, tab, a.w_base, a.d_out, a.d_in, vs,
+                     v_stride == 0 ? 0 : kVTerms * RP * bp, bp, dst, dst_stride, b_chunk);
+      if (le != cudaSuccess) return le;
+    }
     *n_split = split == 1 ? 0 : static_cast<int>(split);
     return cudaGetLastError();
   }
@@ -820,9 +866,13 @@ struct MsRunner {
   // Σ of the split partials into the outputs (and their Gram partials)
   cudaError_t reduce_gram(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
     const int64_t parts = (m + kSlab - 1) / kSlab;
-    reduce_gram_kernel<RP><<<dim3(static_cast<unsigned>(parts), static_cast<unsigned>(a.k)),
-                             kRgThreads, 0, s>>>(f(L.part), n_split, m_ptr, stride, m,
-                                                 f(L.gpart));
+    {
+      const cudaError_t le =
+          launch_pdl(reduce_gram_kernel<RP>,
+                     dim3(static_cast<unsigned>(parts), static_cast<unsigned>(a.k)),
+                     dim3(kRgThreads), 0, s, f(L.part), n_split, m_ptr, stride, m, f(L.gpart));
+      if (le != cudaSuccess) return le;
+    }
     last_parts = static_cast<int>(parts);
     return cudaGetLastError();
   }
@@ -837,12 +887,21 @@ struct MsRunner {
   cudaError_t orth(float* m_ptr, int64_t stride, int64_t m, int n_split) const {
     cudaError_t e = reduce_gram(m_ptr, stride, m, n_split);
     if (e != cudaSuccess) return e;
-    chol_factor_kernel<RP><<<static_cast<unsigned>(a.k), kMsThreads, 0, s>>>(
-        f(L.gpart), last_parts, a.rank, f(L.t));
+    {
+      const cudaError_t le =
+          launch_pdl(chol_factor_kernel<RP>, dim3(static_cast<unsigned>(a.k)), dim3(kMsThreads),
+                     0, s, f(L.gpart), last_parts, a.rank, f(L.t));
+      if (le != cudaSuccess) return le;
+    }
     int64_t rows_blocks = (m + 7) / 8;
     if (rows_blocks > 1024) rows_blocks = 1024;
-    apply_right_kernel<RP><<<dim3(static_cast<unsigned>(rows_blocks), static_cast<unsigned>(a.k)),
-                             kMsThreads, 0, s>>>(m_ptr, stride, m, f(L.t));
+    {
+      const cudaError_t le =
+          launch_pdl(apply_right_kernel<RP>,
+                     dim3(static_cast<unsigned>(rows_blocks), static_cast<unsigned>(a.k)),
+                     dim3(kMsThreads), 0, s, m_ptr, stride, m, f(L.t));
+      if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
   }
 
@@ -850,9 +909,14 @@ struct MsRunner {
     cudaError_t e;
     if (a.rank > 0) {
       const int64_t n_om = a.d_in * RP;
-      sketch_fill_kernel<<<static_cast<unsigned>((n_om + 255) / 256 < 4096 ? (n_om + 255) / 256
-                                                                             : 4096),
-                           256, 0, s>>>(f(L.omega), a.d_in, a.rank, RP, a.seed);
+      {
+        const cudaError_t le =
+            launch_pdl(sketch_fill_kernel,
+                       dim3(static_cast<unsigned>((n_om + 255) / 256 < 4096 ? (n_om + 255) / 256
+                                                                               : 4096)),
+                       dim3(256), 0, s, f(L.omega), a.d_in, a.rank, RP, a.seed);
+        if (le != cudaSuccess) return le;
+      }
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       float* y = f(L.p);
       float* z = f(L.z);
@@ -884,11 +948,23 @@ struct MsRunner {
     uint16_t* rlo = rhi + a.d_in * kp;
     if (kp > 0) {
       const int64_t np = a.d_out * (kp / 8), nr = a.d_in * (kp / 8);
-      fsplit_kernel<<<static_cast<unsigned>((np + 255) / 256 < 4096 ? (np + 255) / 256 : 4096),
-                      256, 0, s>>>(f(L.p), a.d_out, RP, a.k, 1.0f / static_cast<float>(a.k),
-                                   phi, plo);
-      fsplit_kernel<<<static_cast<unsigned>((nr + 255) / 256 < 4096 ? (nr + 255) / 256 : 4096),
-                      256, 0, s>>>(f(L.r), a.d_in, RP, a.k, 1.0f, rhi, rlo);
+      {
+        const cudaError_t le =
+            launch_pdl(fsplit_kernel,
+                       dim3(static_cast<unsigned>((np + 255) / 256 < 4096 ? (np + 255) / 256
+                                                                             : 4096)),
+                       dim3(256), 0, s, f(L.p), a.d_out, RP, a.k, 1.0f / static_cast<float>(a.k),
+                       phi, plo);
+        if (le != cudaSuccess) return le;
+      }
+      {
+        const cudaError_t le =
+            launch_pdl(fsplit_kernel,
+                       dim3(static_cast<unsigned>((nr + 255) / 256 < 4096 ? (nr + 255) / 256
+                                                                             : 4096)),
+                       dim3(256), 0, s, f(L.r), a.d_in, RP, a.k, 1.0f, rhi, rlo);
+        if (le != cudaSuccess) return le;
+      }
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     static bool merge_attr[64] = {};  // per device
@@ -906,8 +982,12 @@ struct MsRunner {
     }
     const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
                     static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));
-    merge_kernel<<<grid, kMulThreads, kMergeSmem, s>>>(a.w_base, phi, plo, rhi, rlo, kp, a.d_out,
-                                                       a.d_in, a.w_merged, a.correction);
+    {
+      const cudaError_t le =
+          launch_pdl(merge_kernel, dim3(grid), dim3(kMulThreads), kMergeSmem, s, a.w_base, phi,
+                     plo, rhi, rlo, kp, a.d_out, a.d_in, a.w_merged, a.correction);
+      if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
   }
 };
