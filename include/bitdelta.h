@@ -121,7 +121,8 @@ bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, co
  * by one that signals its dependents early (griddepcontrol.launch_dependents
  * or cudaTriggerProgrammaticLaunchCompletion).  This library's calls that
  * write such tensors (bitdelta_compress, bitdelta_compress_noalloc,
- * bitdelta_reconstruct) do not signal early; kernels that do not use
+ * bitdelta_reconstruct, and the last kernel of bitdelta_monosoup, which
+ * writes the merged weights) do not signal early; kernels that do not use
  * programmatic dependent launch never do.
  */
 bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
