@@ -155,12 +155,15 @@ constexpr size_t mul_smem_bytes() {
 // cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 //   kT = false: a = row n of Δ, b = column c   (Y = Δ·V,  V: d_in × RP)
 //   kT = true:  a = column c,   b = row n      (Z = Δᵀ·V, V: d_out × RP)
-// Δ·V = W_i·V − W_base·V with both weights as exact bf16 operands and V as
-// the sum of two bf16 terms (vsplit_kernel): four products per tile, the
-// W_base ones with the V fragments' sign bits flipped, all into one fp32
+// Δ·V = W_i·Vhi − W_base·Vhi + Δ·Vlo with both weights as exact bf16
+// operands, V as the sum of two bf16 terms (vsplit_kernel) and Δ rounded to
+// bf16 for the low term only: three products per tile (four with W_i·Vlo −
+// W_base·Vlo took 629 against 601 µs per 4096 x 4096, k = 4, rank-32 merge),
+// the W_base one with the V fragments' sign bits flipped, all into one fp32
 // accumulator.  With V's columns orthonormal (as in the iteration), the
 // result stays within about 1e-6 of Δ·V relative to its largest entry
-// (fp64 emulation: 5e-7), despite the cancellation of the two products.  Grid
+// (fp64 emulation of the four-product form: 5e-7; Δ's rounding adds at most
+// 2^-17 of |Δ|·|V| per product), despite the cancellation.  Grid
 // (ceil(A / 64), S, k); split s covers b in [s·b_chunk, (s+1)·b_chunk) and
 // writes part[s][a][j] (or the output directly when S == 1); blockIdx.z picks
 // the checkpoint.  128 threads; warp w owns rows a0 + 16w .. +15 and all RP
@@ -268,6 +271,18 @@ __global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
           ldsm_x4_t(base + (k * G::kWRow + m) * 2, af[mtx][0], af[mtx][1], af[mtx][2], af[mtx][3]);
         }
       }
+      // Δ = W_i − W_base as one bf16 operand for V's low term: the difference
+      // of two bf16 values is exact in fp32, and rounding it to bf16 (2^-9 of
+      // Δ) multiplies a term 2^-8 of V, so three products per tile instead of
+      // four (W_i·Vhi − W_base·Vhi + Δ·Vlo)
+      uint32_t ad[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float dlo = __uint_as_float(af[0][r] << 16) - __uint_as_float(af[1][r] << 16);
+        const float dhi = __uint_as_float(af[0][r] & 0xFFFF0000u) -
+                          __uint_as_float(af[1][r] & 0xFFFF0000u);
+        ad[r] = pack_bf16x2_rn(dlo, dhi);
+      }
 #pragma unroll
       for (int jp = 0; jp < JT; jp += 2) {
         // B fragments of tiles jp, jp+1 for each V term: [term][b0 jp, b1 jp, b0 jp+1, b1 jp+1]
@@ -283,13 +298,12 @@ __global__ void __launch_bounds__(kMulThreads) delta_mul_kernel(
         for (int h = 0; h < 2; ++h) {
           if (jp + h >= JT) break;
           float (&c)[4] = acc[jp + h];
-#pragma unroll
-          for (int term = 0; term < kVTerms; ++term) {
-            const uint32_t b0 = bf[term][2 * h], b1 = bf[term][2 * h + 1];
-            mma_bf16_16816(c, af[0][0], af[0][1], af[0][2], af[0][3], b0, b1);
-            mma_bf16_16816(c, af[1][0], af[1][1], af[1][2], af[1][3], b0 ^ 0x80008000u,
-                           b1 ^ 0x80008000u);
-          }
+          static_assert(kVTerms == 2, "V as a high and a low bf16 term");
+          const uint32_t b0 = bf[0][2 * h], b1 = bf[0][2 * h + 1];
+          mma_bf16_16816(c, af[0][0], af[0][1], af[0][2], af[0][3], b0, b1);
+          mma_bf16_16816(c, af[1][0], af[1][1], af[1][2], af[1][3], b0 ^ 0x80008000u,
+                         b1 ^ 0x80008000u);
+          mma_bf16_16816(c, ad[0], ad[1], ad[2], ad[3], bf[1][2 * h], bf[1][2 * h + 1]);
         }
       }
     }
