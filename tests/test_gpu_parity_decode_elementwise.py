@@ -53,13 +53,13 @@ def _layer(seed, d_out, d_in, per_row):
 
 @pytest.mark.parametrize("per_row", [True, False])
 @pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
-@pytest.mark.parametrize("d_in", [1024, 1032])
-def test_decode_linear_elementwise(M, d_in, per_row):
-    """d_in = 1024: 16-byte sign rows (the cp.async ring for M <= 8, the
-    register pipeline for 9..16); d_in = 1032: sign rows not 16-byte aligned
-    (byte-wise sign loads, a 32-column tail).  d_out = 600: a partial last
-    group of 16 rows."""
-    d_out = 600
+@pytest.mark.parametrize("d_in,d_out", [(1024, 600), (1032, 600), (1024, 5000)])
+def test_decode_linear_elementwise(M, d_in, d_out, per_row):
+    """d_in = 1024: 16-byte sign rows (the cp.async ring for M <= 8, and for
+    9..16 on the one-wave grid of d_out = 600; d_out = 5000 is a grid of more
+    than two CTAs per SM, where 9..16 take the register pipeline); d_in =
+    1032: sign rows not 16-byte aligned (byte-wise sign loads, a 32-column
+    tail).  d_out = 600 and 5000: a partial last group of 16 rows."""
     wb, packed, alpha = _layer(31 + M, d_out, d_in, per_row)
     x = synth.activations(31 + M, M, d_in)
     y = bf16_values(bd.bitdelta_linear(to_dev_bf16(x), to_dev_bf16(wb), to_dev(packed),
