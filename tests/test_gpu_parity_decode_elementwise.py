@@ -107,16 +107,21 @@ def test_grouped_short_rows_elementwise(d_in):
     assert_linear_close(y, oracle.linear_grouped(x, off, var, wb, packs, alphas, True))
 
 
-@pytest.mark.parametrize("d_out,d_in,per_row", [(5000, 16384, True), (8192, 16512, False),
-                                               (4864, 16384, True), (5000, 1024, True)])
-def test_grouped_two_variants_pair_split_elementwise(d_out, d_in, per_row):
+@pytest.mark.parametrize("d_out,d_in,per_row,shift", [(5000, 16384, True, 0),
+                                                     (8192, 16512, False, 0),
+                                                     (5000, 16384, True, 8),
+                                                     (4864, 16384, True, 0),
+                                                     (5000, 1024, True, 0)])
+def test_grouped_two_variants_pair_split_elementwise(d_out, d_in, per_row, shift):
     """Eight one-row segments alternating two variants (the 40-layer slice's
     decode batch) on layers of 313 and 512 row blocks with d_in >= 16384,
     whose grids the host splits over d_in between the two CTAs of a cluster
     (CTA 1's sums added to CTA 0's through distributed shared memory; 16512
     leaves the two CTAs unequal runs of stages), and without the split (304
     blocks; d_in = 1024): every output against the split form of its own
-    variant."""
+    variant.  shift = 8: variant 2's sign table starts 8 bytes past a 16-byte
+    boundary (its words fetched with plain loads)."""
+    import torch
     n_var = 2
     wb = synth.base_weight(42, d_out, d_in)
     packs, alphas = [], []
@@ -129,6 +134,14 @@ def test_grouped_two_variants_pair_split_elementwise(d_out, d_in, per_row):
     var = np.array([1 + (r % 2) for r in range(8)], np.int32)
     x = synth.activations(42, 8, d_in)
     dp, da = [to_dev(p) for p in packs], [to_dev(a) for a in alphas]
+    keep = []
+    if shift:
+        raw = torch.empty(packs[1].size + 16, dtype=torch.uint8, device="cuda")
+        shifted = raw[shift:shift + packs[1].size].view(packs[1].shape)
+        shifted.copy_(dp[1])
+        assert shifted.data_ptr() % 16 == shift
+        keep.append(raw)
+        dp[1] = shifted
     pt, at = bd.variant_tables(dp, da, "cuda")
     y = bf16_values(bd.bitdelta_linear_grouped(
         to_dev_bf16(x), to_dev(off), to_dev(var), to_dev_bf16(wb), pt, at, n_var=n_var,
