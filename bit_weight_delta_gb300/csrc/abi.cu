@@ -160,9 +160,46 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
   if (!make_tmap_bf16(&tw, w_base, g.d_out, g.d_in, bk, bd::gemm_block_rows()) ||
       !make_tmap_bf16(&tx, x, rows_x, g.d_in, bk, bd::gemm_pair_x_rows()))
     return false;
-  const int64_t pair_tiles =
-      ((g.d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows())) *
-      ((rows_x + tok - 1) / tok + extra_tiles);
+  const int64_t row_tiles = (g.d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows());
+  const int64_t pair_tiles = row_tiles * ((rows_x + tok - 1) / tok + extra_tiles);
+  // One run of M rows on 512-token tiles (width chosen per shape) whose last
+  // round is small (at most half the pairs): that round's tiles (a suffix of
+  // the flat tile order) run instead as twice as many 256-token tiles in a
+  // second launch, all at once, for ~0.6 of a 512-token round.  8192 ->
+  // 10240 at M = 2048: 160 tiles over 76 pairs, the last 8 as 16; 300 -> 272
+  // µs.  The two widths give bit-identical outputs.
+  const bool auto_width = g_prefill_tile.load() == BD_PREFILL_TILE_AUTO;
+  const int pairs = wide && auto_width && g.seg_off == nullptr ? bd::gemm_pair_capacity(true) : 0;
+  const int64_t full = pairs > 0 ? pair_tiles / pairs : 0;
+  const int64_t rem = pairs > 0 ? pair_tiles - full * pairs : 0;
+  if (full >= 1 && rem > 0 && 2 * rem <= pairs) {
+    bd::GemmArgs head = g;
+    head.tile_lo = 0;
+    head.tile_hi = full * pairs;
+    *err = bd::launch_gemm_pair(head, tw, tx, full * pairs, true, s);
+    if (*err == cudaErrorInvalidConfiguration) {
+      (void)cudaGetLastError();  // no cluster of two fits: nothing was launched
+      return false;
+    }
+    if (*err != cudaSuccess) return true;
+    CUtensorMap tw_n, tx_n;
+    const int bk_n = bd::gemm_pair_block_k();
+    if (!make_tmap_bf16(&tw_n, w_base, g.d_out, g.d_in, bk_n, bd::gemm_block_rows()) ||
+        !make_tmap_bf16(&tx_n, x, rows_x, g.d_in, bk_n, bd::gemm_pair_x_rows())) {
+      *err = cudaErrorInvalidValue;  // the maps above were accepted: cannot happen
+      return true;
+    }
+    // wide tile (nt, j) is narrow tiles (nt, 2j) and (nt, 2j + 1)
+    const int64_t t_wide = (rows_x + tok - 1) / tok;
+    const int64_t tok_n = bd::gemm_pair_tokens(false);
+    const int64_t t_narrow = (rows_x + tok_n - 1) / tok_n;
+    const int64_t first = full * pairs;
+    bd::GemmArgs tail = g;
+    tail.tile_lo = (first / t_wide) * t_narrow + 2 * (first % t_wide);
+    tail.tile_hi = row_tiles * t_narrow;
+    *err = bd::launch_gemm_pair(tail, tw_n, tx_n, tail.tile_hi - tail.tile_lo, false, s);
+    return true;
+  }
   *err = bd::launch_gemm_pair(g, tw, tx, pair_tiles, wide, s);
   if (*err != cudaErrorInvalidConfiguration) return true;
   (void)cudaGetLastError();  // no cluster of two fits: nothing was launched

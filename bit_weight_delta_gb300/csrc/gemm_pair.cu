@@ -184,14 +184,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc->tmem_base;
   const int64_t t_total = misc->t_total;
   const int64_t n_tiles_n = (p.d_out + kPairM - 1) / kPairM;
-  const int64_t num_tiles = n_tiles_n * t_total;
+  const int64_t all_tiles = n_tiles_n * t_total;
+  // a range of the flat tile order (single-variant mode), else all of it
+  const int64_t t_lo = !grouped && p.tile_hi > 0 ? p.tile_lo : 0;
+  const int64_t t_hi = !grouped && p.tile_hi > 0 && p.tile_hi < all_tiles ? p.tile_hi : all_tiles;
+  const int64_t num_tiles = t_hi > t_lo ? t_hi - t_lo : 0;
   const int64_t pair_id = blockIdx.x >> 1;
   const int64_t n_pairs = gridDim.x >> 1;
   const int64_t my_tiles = pair_id < num_tiles ? (num_tiles - 1 - pair_id) / n_pairs + 1 : 0;
   const int n_kb = static_cast<int>(p.d_in / kBK);
   const int32_t* seg_off_tbl = grouped ? s_seg_off : nullptr;
   auto my_tile = [&](int64_t i) {
-    return tile_at<kPairM, kBN>(p, pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
+    return tile_at<kPairM, kBN>(p, t_lo + pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
                                 s_prefix);
   };
   const int64_t row0 = static_cast<int64_t>(rank) * kBM;     // this CTA's rows in the tile

@@ -92,6 +92,9 @@ struct GemmArgs {
   const uint8_t* const* packed_table;
   const float* const* alpha_table;
   DevCtx ctx;
+  // single-variant mode: when tile_hi > 0, only flat tiles [tile_lo,
+  // tile_hi) of the call's tile order (row tiles outer, token tiles inner)
+  int64_t tile_lo, tile_hi;
 };
 
 constexpr int kGemmMaxSegs = 1024;
@@ -118,7 +121,7 @@ cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
 // bounds the CTAs of a launch (the launch takes at most one wave of the
 // device); workspace (sign_similarity_workspace_bytes): 256 bytes of
 // counters, zeroed before the first call, then (2·n_b + 1) doubles per CTA
-// of that bound and per group of 16 of them.
+// of that bound and per group of 32 of them.
 int sign_similarity_grid(int64_t d_out);
 size_t sign_similarity_workspace_bytes(int64_t d_out, int32_t n_b);
 cudaError_t launch_sign_similarity(const uint8_t* pa, const float* aa,

@@ -157,3 +157,28 @@ def test_tile_widths_agree():
     assert bd.bitdelta_check_error() == 0
     diff = out[256] != out[512]
     assert not diff.any(), f"{int(diff.sum())} of {diff.size} outputs differ between widths"
+
+
+@pytest.mark.parametrize("M", [2048, 2000])
+def test_small_last_round_on_narrow_tiles(M):
+    """40 row tiles x 4 token tiles of 512: on 76 CTA pairs two full rounds of
+    512-token tiles, and the last round's 8 tiles (row tiles 38-39) run as 16
+    tiles of 256 tokens in a second launch; M = 2000 leaves the last token
+    tile of each row ragged.  Sampled outputs everywhere plus whole token rows,
+    which cross both launches' row tiles, element-wise."""
+    d_out, d_in = 256 * 40, 256
+    wb, packed, alpha = _big_layer(25, d_out, d_in, True)
+    x = synth.activations(25, M, d_in)
+    y = _linear(x, wb, packed, alpha, True)
+    assert bd.bitdelta_check_error() == 0
+    weff = _weff(wb, packed, alpha, True)
+    xa = np.abs(synth.bf16_to_f32(x).astype(np.float64))
+    rng = np.random.default_rng(M)
+    mi = rng.integers(0, M, 4000)
+    ni = np.concatenate([rng.integers(0, d_out, 3000), rng.integers(38 * 256, d_out, 1000)])
+    ref = oracle.linear_at(x, wb, packed, alpha, True, mi, ni)
+    absmag = np.einsum("ik,ik->i", xa[mi], np.abs(weff[ni]))
+    _assert_elementwise(y[mi, ni], ref, absmag, d_in, f"M={M} sampled")
+    for m in (0, 255, 256, 511, 512, 1535, 1536, 1791, 1792, M - 1):
+        ref_m = oracle.linear(x[m:m + 1], wb, packed, alpha, True)[0]
+        _assert_elementwise(y[m], ref_m, xa[m] @ np.abs(weff).T, d_in, f"M={M} row {m}")
