@@ -417,6 +417,17 @@ class Prefill:
         torch.cuda.synchronize()
         self.flops = {nm: 2.0 * self.M * d_out * d_in for nm, d_out, d_in in self.shapes}
         self.phases = [nm for nm, _, _ in self.shapes]
+        # split-schedule workspace (bitdelta_linear_ws): one for every shape
+        need = max(bd.bitdelta_linear_workspace_bytes(self.M, d_out, d_in)
+                   for _, d_out, d_in in self.shapes)
+        self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda") if need else None
+        self.split = True
+
+    def linear(self, x, wb, packed, alpha, y):
+        if self.split:
+            self.bd.bitdelta_linear_ws(x, wb, packed, alpha, self.ws, per_row=True, out=y)
+        else:
+            self.bd.bitdelta_linear(x, wb, packed, alpha, per_row=True, out=y)
 
     def launches_per_step(self):
         return len(self.phases)
@@ -427,8 +438,7 @@ class Prefill:
     def run_phase(self, phase):
         d_in = dict((nm, di) for nm, _, di in self.shapes)[phase]
         wb, packed, alpha = self.mats[phase]
-        self.bd.bitdelta_linear(self.x[d_in], wb, packed, alpha, per_row=True,
-                                out=self.y[phase])
+        self.linear(self.x[d_in], wb, packed, alpha, self.y[phase])
 
     def oracle_sample(self):
         """The oracle on 16 of the 2048 tokens through the O projection
@@ -494,7 +504,7 @@ class Prefill:
                                                          out=w_eff[nm])
                             torch.matmul(x, w_eff[nm].T, out=y)
                         else:
-                            self.bd.bitdelta_linear(x, wb, packed, alpha, per_row=True, out=y)
+                            self.linear(x, wb, packed, alpha, y)
                     e.record()
                     torch.cuda.synchronize()
                     times.append(s.elapsed_time(e))
@@ -1444,6 +1454,9 @@ def main():
     if "prefill" in wanted:
         pre = Prefill(bd)
         pms, pph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
+        pre.split = False
+        nms, nph = timed_run(cudart, pre, 10, 3, dist, None, graph_steps=10)
+        pre.split = True
         ref = pre.cublas_reference()
         tfl = pre.flops_per_step() / (pms * 1e-3) / 1e12
         workloads["prefill"] = {
@@ -1457,6 +1470,14 @@ def main():
             "unfused_reconstruct_plus_cublas": ref["unfused"],
             "fused_vs_unfused_by_tokens": ref["fused_vs_unfused_by_tokens"],
             "frac_of_cublas": ref["cublas_plain"]["ms_per_step"] / pms,
+            "call": "bitdelta_linear_ws (split schedule, workspace "
+                    f"{0 if pre.ws is None else pre.ws.numel() >> 20} MiB)",
+            "without_workspace": {
+                "call": "bitdelta_linear", "ms_per_step": nms,
+                "TFLOP/s": pre.flops_per_step() / (nms * 1e-3) / 1e12,
+                "per_projection": {p: {"ms": nph[p],
+                                       "TFLOP/s": pre.flops[p] / (nph[p] * 1e-3) / 1e12}
+                                   for p in pre.phases}},
         }
         if cpu_on:
             workloads["prefill"]["cpu_baseline"] = pre.oracle_sample()

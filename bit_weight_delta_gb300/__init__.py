@@ -30,7 +30,8 @@ _STATUS = {
 
 EXPORTED = (
     "bitdelta_packed_bytes", "bitdelta_compress_workspace_bytes", "bitdelta_compress",
-    "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_grouped",
+    "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_ws",
+    "bitdelta_linear_workspace_bytes", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
     "bitdelta_set_prefill_tile",
     "bitdelta_status_string", "bitdelta_compress_noalloc", "bitdelta_sign_similarity",
@@ -84,6 +85,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_reconstruct.restype = st
     lib.bitdelta_linear.argtypes = [p, i64, p, p, p, st, i64, i64, p, p]
     lib.bitdelta_linear.restype = st
+    lib.bitdelta_linear_ws.argtypes = [p, i64, p, p, p, st, i64, i64, p, p, sz, p]
+    lib.bitdelta_linear_ws.restype = st
+    lib.bitdelta_linear_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.bitdelta_linear_workspace_bytes.restype = sz
     lib.bitdelta_linear_grouped.argtypes = [p, i64, p, p, i32, i32, p, p, p, i32, st, i64, i64,
                                             p, p]
     lib.bitdelta_linear_grouped.restype = st
@@ -235,6 +240,35 @@ def bitdelta_linear(x, w_base, packed, alpha, per_row: bool = True, out=None, st
     _check("bitdelta_linear", load().bitdelta_linear(
         _ptr(x), M, _ptr(w_base), _ptr(packed), _ptr(alpha), _mode(per_row), d_out, d_in,
         _ptr(out), _stream(stream)))
+    return out
+
+
+def bitdelta_linear_workspace_bytes(M: int, d_out: int, d_in: int) -> int:
+    """Bytes of the split-schedule workspace of bitdelta_linear_ws (0: never split)."""
+    return int(load().bitdelta_linear_workspace_bytes(M, d_out, d_in))
+
+
+def bitdelta_linear_ws(x, w_base, packed, alpha, workspace, per_row: bool = True, out=None,
+                       stream=None):
+    """bitdelta_linear with a split-schedule workspace (uint8 CUDA tensor on a
+    256-byte boundary of at least bitdelta_linear_workspace_bytes(M, d_out,
+    d_in) bytes, or None)."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(w_base, torch.bfloat16, "w_base")
+    _dev(packed, torch.uint8, "packed")
+    _dev(alpha, torch.float32, "alpha")
+    d_out, d_in = w_base.shape
+    lead = x.shape[:-1]
+    M = x.numel() // d_in if x.numel() else 0
+    if out is None:
+        out = torch.empty((*lead, d_out), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = 0
+    if workspace is not None:
+        _dev(workspace, torch.uint8, "workspace")
+        ws_bytes = workspace.numel()
+    _check("bitdelta_linear_ws", load().bitdelta_linear_ws(
+        _ptr(x), M, _ptr(w_base), _ptr(packed), _ptr(alpha), _mode(per_row), d_out, d_in,
+        _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -152,7 +152,8 @@ bool use_wide_tiles(int64_t d_out, int64_t rows_x, int64_t long_tokens) {
 // cannot be encoded or the device cannot place a cluster of two of its CTAs
 // (every GB300 can); the caller then runs the rows on the decode kernel.
 bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t rows_x,
-               int64_t long_tokens, int64_t extra_tiles, cudaStream_t s, cudaError_t* err) {
+               int64_t long_tokens, int64_t extra_tiles, void* ws, size_t ws_bytes,
+               cudaStream_t s, cudaError_t* err) {
   CUtensorMap tw, tx;
   const bool wide = use_wide_tiles(g.d_out, rows_x, long_tokens);
   const int bk = wide ? bd::gemm_pair_wide_block_k() : bd::gemm_pair_block_k();
@@ -162,6 +163,37 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
     return false;
   const int64_t row_tiles = (g.d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows());
   const int64_t pair_tiles = row_tiles * ((rows_x + tok - 1) / tok + extra_tiles);
+  // With a split workspace, one run of M rows on 512-token tiles whose tiles
+  // do not fill whole rounds of the device's pairs: all rounds but the last
+  // whole one run as whole tiles, and the k-blocks of the rest (that round's
+  // tiles and the remainder) are cut evenly over the pairs, so every pair
+  // ends at about the same time instead of a last round with idle pairs.
+  // Each pair's range spans more than one tile, so at most two pairs share a
+  // tile; their fp32 partials are summed in k order (deterministic).
+  if (ws != nullptr && wide && g.seg_off == nullptr) {
+    const int pairs = bd::gemm_pair_capacity(true);
+    const int64_t full = pairs > 0 ? pair_tiles / pairs : 0;
+    const int64_t rem = pairs > 0 ? pair_tiles - full * pairs : 0;
+    if (full >= 1 && rem > 0) {
+      const int64_t sk_tiles = rem + pairs;
+      const size_t count_bytes = bd::gemm_split_count_bytes(sk_tiles);
+      if (count_bytes + bd::gemm_split_part_bytes(pairs) <= ws_bytes) {
+        *err = cudaMemsetAsync(ws, 0, count_bytes, s);
+        if (*err != cudaSuccess) return true;
+        bd::GemmArgs sg = g;
+        sg.tile_lo = 0;
+        sg.tile_hi = (full - 1) * pairs;
+        sg.sk_lo = sg.tile_hi;
+        sg.sk_tiles = sk_tiles;
+        sg.sk_count = static_cast<unsigned int*>(ws);
+        sg.sk_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + count_bytes);
+        *err = bd::launch_gemm_pair(sg, tw, tx, pairs, true, s);
+        if (*err != cudaErrorInvalidConfiguration) return true;
+        (void)cudaGetLastError();  // no cluster of two fits: nothing was launched
+        return false;
+      }
+    }
+  }
   // One run of M rows on 512-token tiles (width chosen per shape) whose last
   // round is small (at most half the pairs): that round's tiles (a suffix of
   // the flat tile order) run instead as twice as many 256-token tiles in a
@@ -294,10 +326,31 @@ bd_status bitdelta_reconstruct(const uint16_t* w_base, const uint8_t* packed, co
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t bitdelta_linear_workspace_bytes(int64_t M, int64_t d_out, int64_t d_in) {
+  if (check_dims(d_out, d_in) != BD_OK || M <= kDecodeMaxRows || M > INT32_MAX ||
+      !tc_shape_ok(M, d_out, d_in))
+    return 0;
+  DeviceState* dev = nullptr;
+  if (current_device(&dev) != BD_OK) return 0;
+  const int pairs = bd::gemm_pair_capacity(true);
+  if (pairs < 1) return 0;
+  return bd::gemm_split_count_bytes(2 * static_cast<int64_t>(pairs)) +
+         bd::gemm_split_part_bytes(pairs);
+}
+
 bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
                           const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
                           int64_t d_out, int64_t d_in, uint16_t* y, bd_stream_t stream) {
+  return bitdelta_linear_ws(x, M, w_base, packed, alpha, mode, d_out, d_in, y, nullptr, 0,
+                            stream);
+}
+
+bd_status bitdelta_linear_ws(const uint16_t* x, int64_t M, const uint16_t* w_base,
+                             const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
+                             int64_t d_out, int64_t d_in, uint16_t* y, void* ws,
+                             size_t ws_bytes, bd_stream_t stream) {
   if (M < 0 || !mode_ok(mode)) return BD_ERR_INVALID_ARG;
+  if (ws != nullptr && !aligned(ws, 256)) return BD_ERR_MISALIGNED;
   if (M > 0 && (!x || !w_base || !packed || !alpha || !y)) return BD_ERR_INVALID_ARG;
   bd_status st = check_dims(d_out, d_in);
   if (st != BD_OK) return st;
@@ -305,6 +358,8 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
   if (M > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(x, 16) || !aligned(w_base, 16) || !aligned(y, 16) || !aligned(alpha, 4))
     return BD_ERR_MISALIGNED;
+  if (ws != nullptr && ws_bytes < bitdelta_linear_workspace_bytes(M, d_out, d_in))
+    return BD_ERR_WORKSPACE;
   DeviceState* dev = nullptr;
   if ((st = current_device(&dev)) != BD_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -321,7 +376,7 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
     g.y = y;
     g.ctx = ctx;
     cudaError_t e = cudaSuccess;
-    if (launch_tc(g, w_base, x, M, M, 0, s, &e)) return from_cuda(e);
+    if (launch_tc(g, w_base, x, M, M, 0, ws, ws_bytes, s, &e)) return from_cuda(e);
   }
   bd::GemvArgs a{};
   a.x = x;
@@ -392,7 +447,8 @@ bd_status bitdelta_linear_grouped(const uint16_t* x, int64_t M_total, const int3
       // token tiles over the slice's segments <= tiles of M_total + one
       // ragged tile per segment
       cudaError_t e = cudaSuccess;
-      const bool launched = launch_tc(g, w_base, x, M_total, max_seg_len, g.n_seg, s, &e);
+      const bool launched =
+          launch_tc(g, w_base, x, M_total, max_seg_len, g.n_seg, nullptr, 0, s, &e);
       if (launched && (st = from_cuda(e)) != BD_OK) return st;
       if (!launched) {
         if (s0 > 0) return BD_ERR_CUDA;  // the first slice launched: cannot happen

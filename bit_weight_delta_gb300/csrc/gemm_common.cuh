@@ -223,6 +223,56 @@ __device__ __forceinline__ void store_acc_rows(uint32_t taddr, uint16_t* y, int6
   }
 }
 
+// Epilogue of one warp for a part of a split tile: the warp's 32
+// accumulator lanes x the first `cols` token columns, stored as fp32 to the
+// slot at `slot` (this thread's row already added): element (token c, row)
+// at slot[c * 128], so each store of the warp writes 128 contiguous bytes.
+__device__ __forceinline__ void store_acc_partial(uint32_t taddr, float* slot, int cols) {
+#pragma unroll 1
+  for (int c = 0; c < cols; c += 32) {
+    uint32_t rr[32];
+    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), rr);
+    tmem_ld_wait();
+    float* q = slot + static_cast<int64_t>(c) * 128;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c + j < cols) __stcg(q + j * 128, __uint_as_float(rr[j]));
+  }
+}
+
+// The last contributor's sum of a split tile: for each of its `cols` tokens,
+// the partials of pairs q_lo .. q_hi in that order (the k order of their
+// ranges), rounded once to bf16 and stored to y[tok0 + c][n].  `slots` is
+// the first slot of this CTA half, this thread's row already added; pair q's
+// part is in its slot 0 when the tile (split-region index su) holds the
+// start of q's range, else in its slot 1.
+__device__ __forceinline__ void sum_partials_store(const float* slots, int64_t q_lo, int64_t q_hi,
+                                                   int64_t su, int64_t sk_w, int64_t n_pairs,
+                                                   int n_kb, int64_t slot_elems, uint16_t* y,
+                                                   int64_t d_out, int64_t n, int64_t tok0,
+                                                   int cols) {
+  if (n >= d_out) return;
+  constexpr int kCols = 16;  // tokens per pass (registers: the kernel's roles share a budget)
+  uint16_t* yp = y + tok0 * d_out + n;
+#pragma unroll 1
+  for (int c = 0; c < cols; c += kCols) {
+    float acc[kCols];
+#pragma unroll 1
+    for (int64_t q = q_lo; q <= q_hi; ++q) {
+      const int jj = (q * sk_w / n_pairs) / n_kb == su ? 0 : 1;
+      const float* src = slots + (q * 2 + jj) * 2 * slot_elems + static_cast<int64_t>(c) * 128;
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        const float v = c + j < cols ? __ldcg(src + j * 128) : 0.0f;
+        acc[j] = q == q_lo ? v : acc[j] + v;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kCols; ++j)
+      if (c + j < cols) yp[static_cast<int64_t>(c + j) * d_out] = bf16_rn(acc[j]);
+  }
+}
+
 // ------------------------------------------------------------------ CTA pairs
 
 __device__ __forceinline__ uint32_t cluster_rank() {

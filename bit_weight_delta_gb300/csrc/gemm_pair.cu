@@ -186,8 +186,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int64_t n_tiles_n = (p.d_out + kPairM - 1) / kPairM;
   const int64_t all_tiles = n_tiles_n * t_total;
   // a range of the flat tile order (single-variant mode), else all of it
-  const int64_t t_lo = !grouped && p.tile_hi > 0 ? p.tile_lo : 0;
-  const int64_t t_hi = !grouped && p.tile_hi > 0 && p.tile_hi < all_tiles ? p.tile_hi : all_tiles;
+  const bool split = !grouped && p.sk_tiles > 0 && p.sk_lo >= 0 && p.sk_lo < all_tiles;
+  const bool ranged = !grouped && (p.tile_hi > 0 || split);
+  const int64_t t_lo = ranged ? p.tile_lo : 0;
+  const int64_t t_hi = ranged && p.tile_hi < all_tiles ? p.tile_hi : all_tiles;
   const int64_t num_tiles = t_hi > t_lo ? t_hi - t_lo : 0;
   const int64_t pair_id = blockIdx.x >> 1;
   const int64_t n_pairs = gridDim.x >> 1;
@@ -197,6 +199,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto my_tile = [&](int64_t i) {
     return tile_at<kPairM, kBN>(p, t_lo + pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
                                 s_prefix);
+  };
+  // Split region: its k-blocks, tile after tile, sk_w in all; this pair takes
+  // [sk_a, sk_b), after its whole tiles.  The pair's work is a list of items
+  // (a tile and a k-block range of it): its whole tiles, then the split
+  // region's tiles that its range meets.
+  const int64_t sk_tiles =
+      split ? (p.sk_tiles < all_tiles - p.sk_lo ? p.sk_tiles : all_tiles - p.sk_lo) : 0;
+  const int64_t sk_w = sk_tiles * n_kb;
+  const int64_t sk_a = pair_id * sk_w / n_pairs;
+  const int64_t sk_b = (pair_id + 1) * sk_w / n_pairs;
+  const int64_t sk_first = sk_a / n_kb;
+  const int64_t n_items = my_tiles + (sk_b > sk_a ? (sk_b - 1) / n_kb - sk_first + 1 : 0);
+  struct Item {
+    Tile t;
+    int kb0, kb1;  // k-blocks [kb0, kb1) of the tile
+    int64_t su;    // split-region tile index, -1 for a whole tile of the range
+    int j;         // partial slot of this pair: 0 first split item, 1 later
+  };
+  auto item_at = [&](int64_t it) {
+    Item im;
+    if (it < my_tiles) {
+      im.t = my_tile(it);
+      im.kb0 = 0;
+      im.kb1 = n_kb;
+      im.su = -1;
+      im.j = 0;
+      return im;
+    }
+    const int64_t su = sk_first + (it - my_tiles);
+    const int64_t base = su * n_kb;
+    im.t = tile_at<kPairM, kBN>(p, p.sk_lo + su, t_total, nullptr, nullptr, nullptr);
+    im.kb0 = static_cast<int>((sk_a > base ? sk_a : base) - base);
+    im.kb1 = static_cast<int>((sk_b < base + n_kb ? sk_b : base + n_kb) - base);
+    im.su = su;
+    im.j = it == my_tiles ? 0 : 1;
+    return im;
   };
   const int64_t row0 = static_cast<int64_t>(rank) * kBM;     // this CTA's rows in the tile
   const int64_t tok_half = static_cast<int64_t>(rank) * kXBox;  // this CTA's x rows per MMA
@@ -213,21 +251,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
     const uint32_t xform_rank0 = map_to_rank(smem_addr(xform_bar), 0);
 
+    // Cursors over this warpgroup's stages: flat positions wg, wg + G, ...
+    // of the pair's k-block stream (the items in turn, k-blocks [kb0, kb1)
+    // of each).  `fresh` marks the warpgroup's first stage of an item.
+    struct Cur {
+      int64_t it;
+      Item im;
+      int kb;
+      bool fresh;
+    };
+    auto cur_carry = [&](Cur& c) {
+      while (c.it < n_items && c.kb >= c.im.kb1) {
+        const int over = c.kb - c.im.kb1;
+        if (++c.it >= n_items) break;
+        c.im = item_at(c.it);
+        c.kb = c.im.kb0 + over;
+        c.fresh = true;
+      }
+    };
+    auto cur_start = [&](Cur& c) {
+      c.it = 0;
+      c.fresh = true;
+      c.kb = wg;
+      c.im.kb1 = 0;
+      if (n_items > 0) {
+        c.im = item_at(0);
+        c.kb += c.im.kb0;
+      }
+      cur_carry(c);
+    };
+    auto cur_step = [&](Cur& c) {
+      c.kb += kXfGroups;
+      c.fresh = false;
+      cur_carry(c);
+    };
+
     // Prefetch cursor, kPrefetch of this warpgroup's stages ahead of the
-    // transform: tile pf_i, k-block pf_kb.  Per tile it holds where this
-    // row's sign bytes come from (mode 1), or a fill of +1 signs for a
-    // variant table entry that is not aligned (mode 2, recorded as a bounds
-    // error), or nothing for base rows (mode 0), so the per-stage step is one
-    // cp.async.  Each thread later reads only what it copied itself, from
-    // private ring slot (own stage index) % kRing.
-    int64_t pf_i = 0;
-    int pf_kb = wg, pf_slot = 0, pf_mode = 0;
+    // transform.  Per item it holds where this row's sign bytes come from
+    // (mode 1), or a fill of +1 signs for a variant table entry that is not
+    // aligned (mode 2, recorded as a bounds error), or nothing for base rows
+    // (mode 0), so the per-stage step is one cp.async.  Each thread later
+    // reads only what it copied itself, from private ring slot (own stage
+    // index) % kRing.
+    Cur pf;
+    cur_start(pf);
+    int64_t pf_loaded = -1;
+    int pf_slot = 0, pf_mode = 0;
     const uint8_t* pf_src = nullptr;
     const float* pf_alpha = nullptr;
-    auto pf_load_tile = [&]() {
+    auto pf_load_item = [&](const Tile& t) {
       pf_mode = 0;
-      if (pf_i >= my_tiles) return;
-      const Tile t = my_tile(pf_i);
       if (t.variant <= 0) return;
       const uint8_t* pk = grouped ? p.packed_table[t.variant - 1] : p.packed;
       const float* al = grouped ? p.alpha_table[t.variant - 1] : p.alpha;
@@ -244,51 +317,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pf_mode = 2;
       }
     };
-    while (pf_kb >= n_kb && pf_i < my_tiles) {
-      pf_kb -= n_kb;
-      ++pf_i;
-    }
-    pf_load_tile();
     auto prefetch_next = [&]() {
       uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
-      if (pf_mode == 1) {
-        if constexpr (C::kSignBytes == 8)
-          cp_async_8(dst, pf_src + pf_kb * C::kSignBytes);
-        else
-          cp_async_4(dst, pf_src + pf_kb * C::kSignBytes);
-      } else if (pf_mode == 2) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+      if (pf.it < n_items) {
+        if (pf.it != pf_loaded) {
+          pf_load_item(pf.im.t);
+          pf_loaded = pf.it;
+        }
+        if (pf_mode == 1) {
+          if constexpr (C::kSignBytes == 8)
+            cp_async_8(dst, pf_src + pf.kb * C::kSignBytes);
+          else
+            cp_async_4(dst, pf_src + pf.kb * C::kSignBytes);
+        } else if (pf_mode == 2) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+        }
+        if (pf_mode != 0 && pf.fresh) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
       }
-      if (pf_mode != 0 && pf_kb < kXfGroups) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
       cp_async_commit();
       pf_slot = pf_slot + 1 == kRing ? 0 : pf_slot + 1;
-      pf_kb += kXfGroups;
-      if (pf_kb >= n_kb) {
-        do {
-          pf_kb -= n_kb;
-          ++pf_i;
-        } while (pf_kb >= n_kb);
-        pf_load_tile();
-      }
+      cur_step(pf);
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch_next();
-    uint32_t alpha_bits = 0u;  // α of the current tile's rows (fp32 bits)
-    // This warpgroup's stages: tile i, k-block kb (kb < G marks its first
-    // stage of a tile); s / ph: ring stage and phase parity of the flat stage
-    // index i * n_kb + kb.
-    int64_t i = 0;
-    int kb = wg;
-    while (kb >= n_kb && i < my_tiles) {
-      kb -= n_kb;
-      ++i;
-    }
-    Tile tl = i < my_tiles ? my_tile(i) : Tile{0, 0, 0, 0};
+    uint32_t alpha_bits = 0u;  // α of the current item's rows (fp32 bits)
+    // s / ph: ring stage and phase parity of the flat position
+    Cur cu;
+    cur_start(cu);
     int slot = 0;
-    const int64_t q0 = i * n_kb + kb;
-    int s = static_cast<int>(q0 % kStages);
-    uint32_t ph = static_cast<uint32_t>((q0 / kStages) & 1);
-    while (i < my_tiles) {
+    int s = wg;
+    uint32_t ph = 0u;
+    while (cu.it < n_items) {
       prefetch_next();
       cp_async_wait<kPrefetch>();
       int ok = 0;
@@ -296,9 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      if (kb < kXfGroups && tl.variant > 0)
-        alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
-      const bool has_delta = tl.variant > 0;
+      const bool has_delta = cu.im.t.variant > 0;
+      if (cu.fresh && has_delta) alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       uint2 sg = make_uint2(0u, 0u);
       if (has_delta) {
         if constexpr (C::kSignBytes == 8)
@@ -360,21 +418,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ph ^= 1u;
       }
       slot = slot + 1 == kRing ? 0 : slot + 1;
-      kb += kXfGroups;
-      if (kb >= n_kb) {
-        do {
-          kb -= n_kb;
-          ++i;
-        } while (kb >= n_kb);
-        if (i < my_tiles) tl = my_tile(i);
-      }
+      cur_step(cu);
     }
     cp_async_wait<0>();
   } else if (warp < kTmaWarp) {
     // ============================================================ epilogue
     const int quarter = warp - kEpiWarp0;  // TMEM lanes 32*quarter ..
     const uint32_t accempty_rank0 = map_to_rank(smem_addr(accempty_bar), 0);
-    for (int64_t i = 0; i < my_tiles; ++i) {
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+    const int rr = 32 * quarter + lane;  // this thread's row of the CTA's 128
+    for (int64_t i = 0; i < n_items; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i & 1);
       int ok = 0;
       if (lane == 0) ok = mbar_wait_cluster(accfull_bar, ph, p.ctx, abort) ? 1 : 0;
@@ -382,12 +435,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      const Tile tl = my_tile(i);
-      store_acc_rows<kBN>(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16), p.y, p.d_out,
-                          tl.n0 + row0 + 32 * quarter + lane, tl.tok0, tl.tok_end);
+      const Item im = item_at(i);
+      const int64_t n = im.t.n0 + row0 + rr;
+      if (im.su < 0 || (im.kb0 == 0 && im.kb1 == n_kb)) {
+        store_acc_rows<kBN>(taddr, p.y, p.d_out, n, im.t.tok0, im.t.tok_end);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(accempty_rank0);
+        continue;
+      }
+      // A part of a split tile: the fp32 partial goes to this pair's slot
+      // (token-major, 128 rows a token), the accumulator is released, and the
+      // last of the tile's contributors (one counter per CTA half and warp)
+      // sums every slot in k order into y.
+      const int64_t span = im.t.tok_end - im.t.tok0;
+      const int cols = span <= 0 ? 0 : (span < kBN ? static_cast<int>(span) : kBN);
+      constexpr int64_t kSlot = static_cast<int64_t>(kBN) * kBM;
+      store_acc_partial(taddr, p.sk_part + ((pair_id * 2 + im.j) * 2 + rank) * kSlot + rr, cols);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(accempty_rank0);
+      __threadfence();
+      __syncwarp();
+      // contributors: the pairs whose ranges meet k-blocks x0 .. x1 (the
+      // largest pair q with q * sk_w / n_pairs <= x is ((x + 1) * n_pairs -
+      // 1) / sk_w)
+      const int64_t x0 = im.su * n_kb, x1 = x0 + n_kb - 1;
+      const int64_t q_lo = ((x0 + 1) * n_pairs - 1) / sk_w;
+      const int64_t q_hi0 = ((x1 + 1) * n_pairs - 1) / sk_w;
+      const int64_t q_hi = q_hi0 < n_pairs - 1 ? q_hi0 : n_pairs - 1;
+      int last = 0;
+      if (lane == 0) {
+        unsigned int* cnt = p.sk_count + (im.su * 2 + rank) * 4 + quarter;
+        last = atomicAdd(cnt, 1u) + 1u == static_cast<unsigned int>(q_hi - q_lo + 1) ? 1 : 0;
+      }
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      if (!last) continue;
+      __threadfence();
+      sum_partials_store(p.sk_part + rank * kSlot + rr, q_lo, q_hi, im.su, sk_w, n_pairs, n_kb,
+                         kSlot, p.y, p.d_out, n, im.t.tok0, cols);
     }
   } else if (warp == kTmaWarp) {
     // ============================================================ TMA producer
@@ -396,9 +482,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       int64_t q = 0;
       bool ok = true;
-      for (int64_t i = 0; i < my_tiles && ok; ++i) {
-        const Tile tl = my_tile(i);
-        for (int kb = 0; kb < n_kb; ++kb, ++q) {
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        const Item im = item_at(i);
+        const Tile& tl = im.t;
+        for (int kb = im.kb0; kb < im.kb1; ++kb, ++q) {
           const int s = static_cast<int>(q % kStages);
           const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
           if (!mbar_wait_cluster(&empty_bar[s], ph ^ 1u, p.ctx, abort)) {
@@ -429,19 +516,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int64_t q = 0;
       bool ok = true;
       bool issued = false;
-      for (int64_t i = 0; i < my_tiles && ok; ++i) {
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        const Item im = item_at(i);
         // N = 256 MMAs with at least one output token (the wide tile's second
         // half is skipped when the tile ends in its first half)
         int n_mma = 1;
-        if constexpr (kWide) {
-          const Tile tl = my_tile(i);
-          n_mma = tl.tok0 + kMmaN < tl.tok_end ? 2 : 1;
-        }
+        if constexpr (kWide) n_mma = im.t.tok0 + kMmaN < im.t.tok_end ? 2 : 1;
         // both CTAs' accumulators must have been drained by their epilogues
         if (!mbar_wait_cluster(accempty_bar, static_cast<uint32_t>((i & 1) ^ 1), p.ctx, abort))
           break;
         tc_fence_after();
-        for (int kb = 0; kb < n_kb; ++kb, ++q) {
+        for (int kb = im.kb0; kb < im.kb1; ++kb, ++q) {
           const int s = static_cast<int>(q % kStages);
           const uint32_t ph = static_cast<uint32_t>((q / kStages) & 1);
           if (!mbar_wait_cluster(&xform_bar[s], ph, p.ctx, abort)) {
@@ -458,7 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               // K step 16: +32 bytes inside both operands' swizzle atoms
-              const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+              const uint32_t acc = (kb > im.kb0 || k > 0) ? 1u : 0u;
               umma_bf16_pair(tmem_base, a_desc + 2 * k, b_desc + 2 * k, kIdesc, acc);
               if (n_mma > 1)
                 umma_bf16_pair(tmem_base + kMmaN, a_desc + 2 * k, b_desc + kBoxStep + 2 * k,
@@ -471,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBK / 16; ++k) {
               // K step 16: 8 TMEM columns of A; +32 bytes inside B's swizzle atom
               umma_bf16_tmem_a_pair(tmem_base, a_tmem + 8 * k, b_desc + 2 * k, kIdesc,
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+                                    (kb > im.kb0 || k > 0) ? 1u : 0u);
             }
           }
           issued = true;
@@ -482,7 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (issued) umma_commit_pair(drain_bar);
       if (issued) mbar_wait_cluster(drain_bar, 0, p.ctx, nullptr);
-    } else if (lane == 0 && my_tiles > 0) {
+    } else if (lane == 0 && n_items > 0) {
       // rank 1: its shared and tensor memory are operands of rank 0's MMAs;
       // stay until the last of them has completed
       mbar_wait_cluster(drain_bar, 0, p.ctx, nullptr);
@@ -554,6 +639,14 @@ int gemm_pair_capacity(bool wide) {
   int n = 0;
   const cudaError_t e = wide ? pair_capacity<true>(&n) : pair_capacity<false>(&n);
   return e == cudaSuccess ? n : -static_cast<int>(e);
+}
+
+size_t gemm_split_count_bytes(int64_t sk_tiles) {
+  const size_t b = static_cast<size_t>(sk_tiles > 0 ? sk_tiles : 0) * 2 * 4 * sizeof(unsigned int);
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+size_t gemm_split_part_bytes(int64_t pairs) {
+  return static_cast<size_t>(pairs > 0 ? pairs : 0) * 2 * 2 * Cfg<true>::kBN * kBM * sizeof(float);
 }
 
 cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,

@@ -95,6 +95,15 @@ struct GemmArgs {
   // single-variant mode: when tile_hi > 0, only flat tiles [tile_lo,
   // tile_hi) of the call's tile order (row tiles outer, token tiles inner)
   int64_t tile_lo, tile_hi;
+  // single-variant mode, split region (sk_tiles > 0; needs tile_hi > 0):
+  // flat tiles [sk_lo, sk_lo + sk_tiles), taken after each pair's whole tiles
+  // of [tile_lo, tile_hi).  Their k-blocks, tile after tile, are cut into one
+  // contiguous range per pair of the launch; a tile that several pairs share
+  // is summed from fp32 partials in sk_part, in k order, by the last of its
+  // contributors (sk_count), so the result does not depend on timing.
+  int64_t sk_lo, sk_tiles;
+  float* sk_part;          // [n_pairs][2][2 CTAs][BN tokens][128 rows] fp32
+  unsigned int* sk_count;  // [sk_tiles][2 CTAs][4 epilogue warps], zero at launch
 };
 
 constexpr int kGemmMaxSegs = 1024;
@@ -113,6 +122,11 @@ int gemm_pair_tokens(bool wide);
 // CTA pairs of that kernel the current device holds at once (0 if none fits;
 // negative cudaError_t on a failed query).
 int gemm_pair_capacity(bool wide);
+// Split-region workspace of a launch of `pairs` pairs of the 512-token kernel
+// over sk_tiles tiles: counters first (sk_count, 256-byte padded), then the
+// partial slots (sk_part).
+size_t gemm_split_count_bytes(int64_t sk_tiles);
+size_t gemm_split_part_bytes(int64_t pairs);
 cudaError_t launch_gemm_pair(const GemmArgs& p, const CUtensorMap& tmap_w,
                              const CUtensorMap& tmap_x, int64_t pair_tiles_bound, bool wide,
                              cudaStream_t stream);

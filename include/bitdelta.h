@@ -130,6 +130,36 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
                           int64_t d_out, int64_t d_in, uint16_t* y, bd_stream_t stream);
 
 /*
+ * bitdelta_linear with a caller workspace for the tensor-core kernel's split
+ * schedule.  (The page has no counterpart: this is a scheduling choice of
+ * this library, not of the method.)  When the call's 512-token tiles do not
+ * fill whole rounds of the device's CTA pairs, the last whole round and the
+ * remainder are cut by k-blocks into one even range per pair; a tile that
+ * two pairs share is summed from their fp32 partials in k order by the pair
+ * that finishes its part last.  The result is deterministic, but its fp32
+ * sum order differs from bitdelta_linear's for those tiles, so single bf16
+ * outputs may differ by the rounding of the split sum.
+ *   workspace   device memory of at least bitdelta_linear_workspace_bytes
+ *               (M, d_out, d_in) bytes on a 256-byte boundary, or NULL (the
+ *               call is then exactly bitdelta_linear).  Its first bytes are
+ *               cleared by the call (stream-ordered); nothing in it needs to
+ *               survive between calls.  Calls that can overlap on the GPU
+ *               need separate workspaces.
+ *   Errors as bitdelta_linear; BD_ERR_WORKSPACE when workspace is not NULL
+ *   and smaller than the size above, BD_ERR_MISALIGNED when it is not on a
+ *   256-byte boundary.
+ * bitdelta_linear_workspace_bytes returns 0 for calls that never split
+ * (M <= 16, shapes the tensor-core kernel does not take) and when the
+ * current device cannot be queried; the size depends on the device (about
+ * 1 MiB per CTA pair that fits at once: 76 MiB on a 152-SM GB300).
+ */
+size_t bitdelta_linear_workspace_bytes(int64_t M, int64_t d_out, int64_t d_in);
+bd_status bitdelta_linear_ws(const uint16_t* x, int64_t M, const uint16_t* w_base,
+                             const uint8_t* packed, const float* alpha, bd_alpha_mode mode,
+                             int64_t d_out, int64_t d_in, uint16_t* y, void* workspace,
+                             size_t ws_bytes, bd_stream_t stream);
+
+/*
  * Multi-tenant linear over one shared W_base ("Serving architecture": base
  * weights shared-read by every variant; a request's model id selects its
  * delta).  Rows [seg_offsets[s], seg_offsets[s+1]) of x use variant

@@ -200,3 +200,22 @@ def test_prefill_tile_setting(lib):
         bd.bitdelta_set_prefill_tile(128)
     bd.bitdelta_set_prefill_tile(512)
     bd.bitdelta_set_prefill_tile("auto")
+
+
+def test_linear_ws_rejects_bad_arguments(lib):
+    f = lib.bitdelta_linear_ws
+    ws = ctypes.c_void_p(0x200000)     # 256-byte aligned fake address, never dereferenced
+    ws_bad = ctypes.c_void_p(0x200010)
+    assert f(GOOD, -1, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, ws, 1 << 20, NULL) == INVALID
+    assert f(GOOD, 4, GOOD, GOOD, GOOD, 3, 8, 16, GOOD, ws, 1 << 20, NULL) == INVALID
+    assert f(GOOD, 4, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, ws_bad, 1 << 20, NULL) == MISALIGNED
+    assert f(NULL, 4, GOOD, GOOD, GOOD, 1, 8, 16, GOOD, ws, 1 << 20, NULL) == INVALID
+    assert f(GOOD, 4, GOOD, GOOD, GOOD, 1, 8, 9, GOOD, ws, 1 << 20, NULL) == SHAPE
+    assert f(NULL, 0, NULL, NULL, NULL, 1, 8, 16, NULL, NULL, 0, NULL) == OK
+
+
+def test_linear_workspace_bytes_without_split(lib):
+    # decode-size calls and shapes the tensor-core kernel does not take never split
+    assert lib.bitdelta_linear_workspace_bytes(16, 4096, 4096) == 0
+    assert lib.bitdelta_linear_workspace_bytes(2048, 4096, 4104) == 0
+    assert lib.bitdelta_linear_workspace_bytes(2048, 4096, 9) == 0
