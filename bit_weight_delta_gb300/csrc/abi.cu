@@ -163,18 +163,23 @@ bool launch_tc(const bd::GemmArgs& g, const void* w_base, const void* x, int64_t
     return false;
   const int64_t row_tiles = (g.d_out + 2 * bd::gemm_block_rows() - 1) / (2 * bd::gemm_block_rows());
   const int64_t pair_tiles = row_tiles * ((rows_x + tok - 1) / tok + extra_tiles);
-  // With a split workspace, one run of M rows on 512-token tiles whose tiles
-  // do not fill whole rounds of the device's pairs: all rounds but the last
-  // whole one run as whole tiles, and the k-blocks of the rest (that round's
-  // tiles and the remainder) are cut evenly over the pairs, so every pair
-  // ends at about the same time instead of a last round with idle pairs.
-  // Each pair's range spans more than one tile, so at most two pairs share a
-  // tile; their fp32 partials are summed in k order (deterministic).
+  // With a split workspace, one run of M rows on 512-token tiles whose last
+  // round is small (at most a quarter of the device's pairs): all rounds but
+  // the last whole one run as whole tiles, and the k-blocks of the rest (that
+  // round's tiles and the remainder) are cut evenly over the pairs, so every
+  // pair ends at about the same time instead of a last round with idle
+  // pairs.  Each pair's range spans more than one tile, so at most two pairs
+  // share a tile; their fp32 partials are summed in k order (deterministic).
+  // Measured on GB300, the split region runs ~20% slower per k-block than
+  // rounds of whole tiles (its pairs no longer read the same x blocks at the
+  // same time): 8192 -> 10240 at M = 2048 (160 tiles, a last round of 8)
+  // 287 -> 261 µs, but 8192 -> 8192 (128 tiles, 52 in the last round)
+  // 211 -> 218 µs, hence the quarter.
   if (ws != nullptr && wide && g.seg_off == nullptr) {
     const int pairs = bd::gemm_pair_capacity(true);
     const int64_t full = pairs > 0 ? pair_tiles / pairs : 0;
     const int64_t rem = pairs > 0 ? pair_tiles - full * pairs : 0;
-    if (full >= 1 && rem > 0) {
+    if (full >= 1 && rem > 0 && 4 * rem <= pairs) {
       const int64_t sk_tiles = rem + pairs;
       const size_t count_bytes = bd::gemm_split_count_bytes(sk_tiles);
       if (count_bytes + bd::gemm_split_part_bytes(pairs) <= ws_bytes) {

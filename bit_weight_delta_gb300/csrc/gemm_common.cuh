@@ -223,53 +223,111 @@ __device__ __forceinline__ void store_acc_rows(uint32_t taddr, uint16_t* y, int6
   }
 }
 
-// Epilogue of one warp for a part of a split tile: the warp's 32
-// accumulator lanes x the first `cols` token columns, stored as fp32 to the
-// slot at `slot` (this thread's row already added): element (token c, row)
-// at slot[c * 128], so each store of the warp writes 128 contiguous bytes.
-__device__ __forceinline__ void store_acc_partial(uint32_t taddr, float* slot, int cols) {
+// Partial slots of a split tile (one per CTA half): 128 rows x BN tokens of
+// fp32, four tokens of a row together: (token c, row r) at float
+// ((c / 4) * 128 + r) * 4 + c % 4.  A warp's 16-byte access for four tokens
+// of its 32 rows is then 512 contiguous bytes, in the store and in the sum.
+
+__device__ __forceinline__ void st_global_v4_hint(float4* p, float4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Epilogue of one warp for a part of a split tile: its 32 accumulator lanes
+// (row r = this thread's row of the CTA's 128) x the first `cols` tokens
+// (rounded up to four), stored as fp32 to the slot under an L2 evict-last
+// policy (the partner reads it, often at the end of the kernel, while the
+// weight stream passes through L2 as evict-first).
+__device__ __forceinline__ void store_acc_partial(uint32_t taddr, float* slot, int r, int cols) {
+  const uint64_t keep = policy_evict_last();
+  float4* s4 = reinterpret_cast<float4*>(slot) + r;
 #pragma unroll 1
   for (int c = 0; c < cols; c += 32) {
-    uint32_t rr[32];
-    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), rr);
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), v);
     tmem_ld_wait();
-    float* q = slot + static_cast<int64_t>(c) * 128;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (c + j < cols) __stcg(q + j * 128, __uint_as_float(rr[j]));
+    for (int k = 0; k < 8; ++k)
+      if (c + 4 * k < cols)
+        st_global_v4_hint(s4 + static_cast<int64_t>(c / 4 + k) * 128,
+                          make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                      __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])),
+                          keep);
   }
 }
 
-// The last contributor's sum of a split tile: for each of its `cols` tokens,
-// the partials of pairs q_lo .. q_hi in that order (the k order of their
-// ranges), rounded once to bf16 and stored to y[tok0 + c][n].  `slots` is
-// the first slot of this CTA half, this thread's row already added; pair q's
-// part is in its slot 0 when the tile (split-region index su) holds the
-// start of q's range, else in its slot 1.
-__device__ __forceinline__ void sum_partials_store(const float* slots, int64_t q_lo, int64_t q_hi,
-                                                   int64_t su, int64_t sk_w, int64_t n_pairs,
-                                                   int n_kb, int64_t slot_elems, uint16_t* y,
-                                                   int64_t d_out, int64_t n, int64_t tok0,
-                                                   int cols) {
-  if (n >= d_out) return;
-  constexpr int kCols = 16;  // tokens per pass (registers: the kernel's roles share a budget)
+// The second contributor's sum of a split tile while it still holds its own
+// part in tensor memory: own accumulator + the partner's partial (fp32
+// addition of two terms is commutative, so the result equals the sum in k
+// order), rounded once to bf16 and stored to y[tok0 + c][n].  The partner's
+// eight 16-byte loads of a step are issued before the tensor-memory load
+// completes.
+__device__ __forceinline__ void sum_tmem_partial_store(uint32_t taddr, const float* slot, int r,
+                                                       uint16_t* y, int64_t d_out, int64_t n,
+                                                       int64_t tok0, int cols) {
+  const bool n_ok = n < d_out;
+  const float4* s4 = reinterpret_cast<const float4*>(slot) + r;
   uint16_t* yp = y + tok0 * d_out + n;
 #pragma unroll 1
-  for (int c = 0; c < cols; c += kCols) {
-    float acc[kCols];
-#pragma unroll 1
-    for (int64_t q = q_lo; q <= q_hi; ++q) {
-      const int jj = (q * sk_w / n_pairs) / n_kb == su ? 0 : 1;
-      const float* src = slots + (q * 2 + jj) * 2 * slot_elems + static_cast<int64_t>(c) * 128;
+  for (int c = 0; c < cols; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c), v);
+    float4 pv[8];
 #pragma unroll
-      for (int j = 0; j < kCols; ++j) {
-        const float v = c + j < cols ? __ldcg(src + j * 128) : 0.0f;
-        acc[j] = q == q_lo ? v : acc[j] + v;
+    for (int k = 0; k < 8; ++k)
+      pv[k] = n_ok && c + 4 * k < cols ? __ldcg(s4 + static_cast<int64_t>(c / 4 + k) * 128)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    tmem_ld_wait();
+    if (n_ok) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float sum[4] = {__uint_as_float(v[4 * k]) + pv[k].x,
+                              __uint_as_float(v[4 * k + 1]) + pv[k].y,
+                              __uint_as_float(v[4 * k + 2]) + pv[k].z,
+                              __uint_as_float(v[4 * k + 3]) + pv[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c + 4 * k + e < cols)
+            yp[static_cast<int64_t>(c + 4 * k + e) * d_out] = bf16_rn(sum[e]);
       }
     }
+  }
+}
+
+// The last contributor's sum of a split tile: for row r and each of the
+// tile's `cols` tokens, the partials in slot a then slot b (the k order of
+// the two contributors' ranges), rounded once to bf16 and stored to
+// y[tok0 + c][n].  Eight 16-byte loads in flight per thread per step.
+__device__ __forceinline__ void sum_pair_partials_store(const float* slot_a, const float* slot_b,
+                                                        int r, uint16_t* y, int64_t d_out,
+                                                        int64_t n, int64_t tok0, int cols) {
+  if (n >= d_out) return;
+  const float4* a4 = reinterpret_cast<const float4*>(slot_a) + r;
+  const float4* b4 = reinterpret_cast<const float4*>(slot_b) + r;
+  uint16_t* yp = y + tok0 * d_out + n;
+#pragma unroll 1
+  for (int c = 0; c < cols; c += 16) {
+    float4 va[4], vb[4];
 #pragma unroll
-    for (int j = 0; j < kCols; ++j)
-      if (c + j < cols) yp[static_cast<int64_t>(c + j) * d_out] = bf16_rn(acc[j]);
+    for (int k = 0; k < 4; ++k) {
+      const int64_t off = static_cast<int64_t>(c / 4 + k) * 128;
+      va[k] = c + 4 * k < cols ? __ldcg(a4 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      vb[k] = c + 4 * k < cols ? __ldcg(b4 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float s[4] = {va[k].x + vb[k].x, va[k].y + vb[k].y, va[k].z + vb[k].z,
+                          va[k].w + vb[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c + 4 * k + e < cols) yp[static_cast<int64_t>(c + 4 * k + e) * d_out] = bf16_rn(s[e]);
+    }
   }
 }
 

@@ -200,21 +200,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return tile_at<kPairM, kBN>(p, t_lo + pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
                                 s_prefix);
   };
-  // Split region: its k-blocks, tile after tile, sk_w in all; this pair takes
-  // [sk_a, sk_b), after its whole tiles.  The pair's work is a list of items
-  // (a tile and a k-block range of it): its whole tiles, then the split
-  // region's tiles that its range meets.
-  const int64_t sk_tiles =
+  // Split region.  When it is whole row tiles and the token tiles of a row
+  // tile divide the pairs, it splits into sk_g = t_total groups, one per
+  // token tile, of n_pairs / sk_g pairs each; else into one group.  Group g
+  // holds the region's tiles of token tile g (local tile u is flat tile
+  // sk_lo + u * sk_g + g), and its k-blocks, tile after tile, sk_w in all,
+  // are cut into one contiguous range per pair of the group: [sk_a, sk_b)
+  // for the pair of index g_idx.  The pairs of equal g_idx cover the same
+  // row tiles at the same k-blocks at about the same time, so each W_base
+  // block they read is read from memory once, as in the rounds of whole
+  // tiles.  A pair's work is a list of items (a tile and a k-block range of
+  // it): its whole tiles, then the group's tiles its range meets.
+  int64_t sk_tiles =
       split ? (p.sk_tiles < all_tiles - p.sk_lo ? p.sk_tiles : all_tiles - p.sk_lo) : 0;
-  const int64_t sk_w = sk_tiles * n_kb;
-  const int64_t sk_a = pair_id * sk_w / n_pairs;
-  const int64_t sk_b = (pair_id + 1) * sk_w / n_pairs;
+  if (sk_tiles > 0 && sk_tiles < n_pairs) {
+    // fewer tiles than pairs would give a tile more than two contributors
+    // (the sum below takes two): the host never launches this
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
+    sk_tiles = 0;
+  }
+  const int64_t sk_g = sk_tiles > 0 && n_pairs % t_total == 0 && p.sk_lo % t_total == 0 &&
+                               sk_tiles % t_total == 0
+                           ? t_total
+                           : 1;
+  const int64_t g_pairs = n_pairs / sk_g;
+  const int64_t g_id = pair_id % sk_g;
+  const int64_t g_idx = pair_id / sk_g;
+  const int64_t sk_w = sk_tiles / sk_g * n_kb;
+  const int64_t sk_a = g_idx * sk_w / g_pairs;
+  const int64_t sk_b = (g_idx + 1) * sk_w / g_pairs;
   const int64_t sk_first = sk_a / n_kb;
   const int64_t n_items = my_tiles + (sk_b > sk_a ? (sk_b - 1) / n_kb - sk_first + 1 : 0);
   struct Item {
     Tile t;
     int kb0, kb1;  // k-blocks [kb0, kb1) of the tile
-    int64_t su;    // split-region tile index, -1 for a whole tile of the range
+    int64_t su;    // the group's local tile index, -1 for a whole tile of the range
     int j;         // partial slot of this pair: 0 first split item, 1 later
   };
   auto item_at = [&](int64_t it) {
@@ -229,7 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const int64_t su = sk_first + (it - my_tiles);
     const int64_t base = su * n_kb;
-    im.t = tile_at<kPairM, kBN>(p, p.sk_lo + su, t_total, nullptr, nullptr, nullptr);
+    im.t = tile_at<kPairM, kBN>(p, p.sk_lo + su * sk_g + g_id, t_total, nullptr, nullptr,
+                                nullptr);
     im.kb0 = static_cast<int>((sk_a > base ? sk_a : base) - base);
     im.kb1 = static_cast<int>((sk_b < base + n_kb ? sk_b : base + n_kb) - base);
     im.su = su;
@@ -253,50 +274,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // Cursors over this warpgroup's stages: flat positions wg, wg + G, ...
     // of the pair's k-block stream (the items in turn, k-blocks [kb0, kb1)
-    // of each).  `fresh` marks the warpgroup's first stage of an item.
-    struct Cur {
-      int64_t it;
-      Item im;
-      int kb;
-      bool fresh;
-    };
-    auto cur_carry = [&](Cur& c) {
-      while (c.it < n_items && c.kb >= c.im.kb1) {
-        const int over = c.kb - c.im.kb1;
-        if (++c.it >= n_items) break;
-        c.im = item_at(c.it);
-        c.kb = c.im.kb0 + over;
-        c.fresh = true;
-      }
-    };
-    auto cur_start = [&](Cur& c) {
-      c.it = 0;
-      c.fresh = true;
-      c.kb = wg;
-      c.im.kb1 = 0;
-      if (n_items > 0) {
-        c.im = item_at(0);
-        c.kb += c.im.kb0;
-      }
-      cur_carry(c);
-    };
-    auto cur_step = [&](Cur& c) {
-      c.kb += kXfGroups;
-      c.fresh = false;
-      cur_carry(c);
-    };
-
-    // Prefetch cursor, kPrefetch of this warpgroup's stages ahead of the
-    // transform.  Per item it holds where this row's sign bytes come from
+    // of each).  kb < kb0g marks the warpgroup's first stage of an item; the
+    // per-stage step is kb += G and one compare, the item change a slow path.
+    // The prefetch cursor also holds where this row's sign bytes come from
     // (mode 1), or a fill of +1 signs for a variant table entry that is not
     // aligned (mode 2, recorded as a bounds error), or nothing for base rows
-    // (mode 0), so the per-stage step is one cp.async.  Each thread later
-    // reads only what it copied itself, from private ring slot (own stage
-    // index) % kRing.
-    Cur pf;
-    cur_start(pf);
-    int64_t pf_loaded = -1;
-    int pf_slot = 0, pf_mode = 0;
+    // and past the last item (mode 0), so the per-stage copy is one cp.async.
+    // Each thread later reads only what it copied itself, from private ring
+    // slot (own stage index) % kRing.
+    struct Cur {
+      int it, kb, kb1, kb0g, var;
+    };
+    const int n_it = static_cast<int>(n_items);
+    int pf_mode = 0;
     const uint8_t* pf_src = nullptr;
     const float* pf_alpha = nullptr;
     auto pf_load_item = [&](const Tile& t) {
@@ -317,37 +307,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pf_mode = 2;
       }
     };
+    auto cur_set = [&](Cur& c, const Item& im, int over, bool is_pf) {
+      c.kb = im.kb0 + over;
+      c.kb1 = im.kb1;
+      c.kb0g = im.kb0 + kXfGroups;
+      c.var = im.t.variant;
+      if (is_pf) pf_load_item(im.t);
+    };
+    auto cur_carry = [&](Cur& c, bool is_pf) {
+      do {
+        const int over = c.kb - c.kb1;
+        if (++c.it >= n_it) {
+          c.kb1 = 0x7FFFFFFF;
+          if (is_pf) pf_mode = 0;
+          return;
+        }
+        cur_set(c, item_at(c.it), over, is_pf);
+      } while (c.kb >= c.kb1);
+    };
+    auto cur_start = [&](Cur& c, bool is_pf) {
+      c.it = 0;
+      c.kb = 0;
+      c.kb1 = 0x7FFFFFFF;
+      c.kb0g = 0;
+      c.var = 0;
+      if (n_it <= 0) return;
+      cur_set(c, item_at(0), wg, is_pf);
+      if (c.kb >= c.kb1) cur_carry(c, is_pf);
+    };
+
+    Cur pf;
+    cur_start(pf, true);
+    int pf_slot = 0;
     auto prefetch_next = [&]() {
       uint8_t* dst = sign_ring + (pf_slot * kBM + r) * 8;
-      if (pf.it < n_items) {
-        if (pf.it != pf_loaded) {
-          pf_load_item(pf.im.t);
-          pf_loaded = pf.it;
-        }
-        if (pf_mode == 1) {
-          if constexpr (C::kSignBytes == 8)
-            cp_async_8(dst, pf_src + pf.kb * C::kSignBytes);
-          else
-            cp_async_4(dst, pf_src + pf.kb * C::kSignBytes);
-        } else if (pf_mode == 2) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-        }
-        if (pf_mode != 0 && pf.fresh) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
+      if (pf_mode == 1) {
+        if constexpr (C::kSignBytes == 8)
+          cp_async_8(dst, pf_src + pf.kb * C::kSignBytes);
+        else
+          cp_async_4(dst, pf_src + pf.kb * C::kSignBytes);
+      } else if (pf_mode == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
       }
+      if (pf_mode != 0 && pf.kb < pf.kb0g) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
       cp_async_commit();
       pf_slot = pf_slot + 1 == kRing ? 0 : pf_slot + 1;
-      cur_step(pf);
+      pf.kb += kXfGroups;
+      if (pf.kb >= pf.kb1) cur_carry(pf, true);
     };
 
     for (int d = 0; d < kPrefetch; ++d) prefetch_next();
     uint32_t alpha_bits = 0u;  // α of the current item's rows (fp32 bits)
     // s / ph: ring stage and phase parity of the flat position
     Cur cu;
-    cur_start(cu);
+    cur_start(cu, false);
     int slot = 0;
     int s = wg;
     uint32_t ph = 0u;
-    while (cu.it < n_items) {
+    while (cu.it < n_it) {
       prefetch_next();
       cp_async_wait<kPrefetch>();
       int ok = 0;
@@ -355,8 +372,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      const bool has_delta = cu.im.t.variant > 0;
-      if (cu.fresh && has_delta) alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
+      const bool has_delta = cu.var > 0;
+      if (cu.kb < cu.kb0g && has_delta) alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       uint2 sg = make_uint2(0u, 0u);
       if (has_delta) {
         if constexpr (C::kSignBytes == 8)
@@ -418,7 +435,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ph ^= 1u;
       }
       slot = slot + 1 == kRing ? 0 : slot + 1;
-      cur_step(cu);
+      cu.kb += kXfGroups;
+      if (cu.kb >= cu.kb1) cur_carry(cu, false);
     }
     cp_async_wait<0>();
   } else if (warp < kTmaWarp) {
@@ -444,36 +462,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_cluster(accempty_rank0);
         continue;
       }
-      // A part of a split tile: the fp32 partial goes to this pair's slot
-      // (token-major, 128 rows a token), the accumulator is released, and the
-      // last of the tile's contributors (one counter per CTA half and warp)
-      // sums every slot in k order into y.
+      // A part of a split tile, shared with one other pair of the group
+      // (each pair's range spans more than one tile): the group's pairs of
+      // index q_lo and q_hi, whose ranges meet k-blocks x0 .. x1 (the largest
+      // index q with q * sk_w / g_pairs <= x is ((x + 1) * g_pairs - 1) /
+      // sk_w).  q_hi's part is in its slot 0 (its range starts in the tile),
+      // q_lo's in its slot 1 unless the tile also holds the start of q_lo's
+      // range.  One counter per tile, CTA half and epilogue warp counts the
+      // parts stored.
       const int64_t span = im.t.tok_end - im.t.tok0;
       const int cols = span <= 0 ? 0 : (span < kBN ? static_cast<int>(span) : kBN);
       constexpr int64_t kSlot = static_cast<int64_t>(kBN) * kBM;
-      store_acc_partial(taddr, p.sk_part + ((pair_id * 2 + im.j) * 2 + rank) * kSlot + rr, cols);
+      const int64_t x0 = im.su * n_kb, x1 = x0 + n_kb - 1;
+      const int64_t q_lo = ((x0 + 1) * g_pairs - 1) / sk_w;
+      const int64_t q_hi0 = ((x1 + 1) * g_pairs - 1) / sk_w;
+      const int64_t q_hi = q_hi0 < g_pairs - 1 ? q_hi0 : g_pairs - 1;
+      const int j_lo = (q_lo * sk_w / g_pairs) / n_kb == im.su ? 0 : 1;
+      const int64_t pair_lo = q_lo * sk_g + g_id, pair_hi = q_hi * sk_g + g_id;
+      const float* slot_lo = p.sk_part + ((pair_lo * 2 + j_lo) * 2 + rank) * kSlot;
+      const float* slot_hi = p.sk_part + ((pair_hi * 2 + 0) * 2 + rank) * kSlot;
+      unsigned int* cnt = p.sk_count + ((im.su * sk_g + g_id) * 2 + rank) * 4 + quarter;
+      int other_done = 0;
+      if (lane == 0) other_done = ld_acquire_u32(cnt) != 0u ? 1 : 0;
+      other_done = __shfl_sync(0xFFFFFFFFu, other_done, 0);
+      if (other_done) {
+        // the other part is stored: add it to this one straight from tensor
+        // memory (nothing else reads this part, so it is neither stored nor
+        // counted)
+        __threadfence();
+        sum_tmem_partial_store(taddr, pair_id == pair_lo ? slot_hi : slot_lo, rr, p.y, p.d_out, n,
+                               im.t.tok0, cols);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(accempty_rank0);
+        continue;
+      }
+      store_acc_partial(taddr, p.sk_part + ((pair_id * 2 + im.j) * 2 + rank) * kSlot, rr, cols);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(accempty_rank0);
       __threadfence();
       __syncwarp();
-      // contributors: the pairs whose ranges meet k-blocks x0 .. x1 (the
-      // largest pair q with q * sk_w / n_pairs <= x is ((x + 1) * n_pairs -
-      // 1) / sk_w)
-      const int64_t x0 = im.su * n_kb, x1 = x0 + n_kb - 1;
-      const int64_t q_lo = ((x0 + 1) * n_pairs - 1) / sk_w;
-      const int64_t q_hi0 = ((x1 + 1) * n_pairs - 1) / sk_w;
-      const int64_t q_hi = q_hi0 < n_pairs - 1 ? q_hi0 : n_pairs - 1;
       int last = 0;
-      if (lane == 0) {
-        unsigned int* cnt = p.sk_count + (im.su * 2 + rank) * 4 + quarter;
-        last = atomicAdd(cnt, 1u) + 1u == static_cast<unsigned int>(q_hi - q_lo + 1) ? 1 : 0;
-      }
+      if (lane == 0) last = atomicAdd(cnt, 1u) == 1u ? 1 : 0;
       last = __shfl_sync(0xFFFFFFFFu, last, 0);
       if (!last) continue;
+      // both parts were stored at about the same time: sum the two slots
       __threadfence();
-      sum_partials_store(p.sk_part + rank * kSlot + rr, q_lo, q_hi, im.su, sk_w, n_pairs, n_kb,
-                         kSlot, p.y, p.d_out, n, im.t.tok0, cols);
+      sum_pair_partials_store(slot_lo, slot_hi, rr, p.y, p.d_out, n, im.t.tok0, cols);
     }
   } else if (warp == kTmaWarp) {
     // ============================================================ TMA producer

@@ -132,13 +132,15 @@ bd_status bitdelta_linear(const uint16_t* x, int64_t M, const uint16_t* w_base,
 /*
  * bitdelta_linear with a caller workspace for the tensor-core kernel's split
  * schedule.  (The page has no counterpart: this is a scheduling choice of
- * this library, not of the method.)  When the call's 512-token tiles do not
- * fill whole rounds of the device's CTA pairs, the last whole round and the
- * remainder are cut by k-blocks into one even range per pair; a tile that
- * two pairs share is summed from their fp32 partials in k order by the pair
- * that finishes its part last.  The result is deterministic, but its fp32
- * sum order differs from bitdelta_linear's for those tiles, so single bf16
- * outputs may differ by the rounding of the split sum.
+ * this library, not of the method.)  When the call's 512-token tiles leave
+ * a small last round (at most a quarter of the device's CTA pairs busy), the
+ * last whole round and that remainder are cut by k-blocks into one even
+ * range per pair instead; a tile that two pairs share is the sum of their
+ * two fp32 partials, formed by the pair that finishes its part last.  The
+ * result is deterministic, but its fp32 sum order differs from
+ * bitdelta_linear's for those tiles, so single bf16 outputs may differ by
+ * the rounding of the split sum.  Other calls run exactly as
+ * bitdelta_linear.
  *   workspace   device memory of at least bitdelta_linear_workspace_bytes
  *               (M, d_out, d_in) bytes on a 256-byte boundary, or NULL (the
  *               call is then exactly bitdelta_linear).  Its first bytes are

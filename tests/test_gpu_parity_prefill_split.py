@@ -2,9 +2,10 @@
 against the oracle.
 
 Page section "Serving architecture": y = x·(W_base + α·unpack(bits))ᵀ with
-W_eff built on chip.  With a workspace, tiles beyond the last full round of
-the device's CTA pairs (plus one full round) are cut by k-blocks over the
-pairs; a tile shared by two pairs is the sum of their fp32 partials.  A
+W_eff built on chip.  With a workspace and a small last round of tiles (at
+most a quarter of the device's 76 CTA pairs), that round and the one before
+it are cut by k-blocks over the pairs; a tile shared by two pairs is the sum
+of their fp32 partials.  A
 partial lost, counted twice, stored to the wrong slot or summed from a stale
 slot shifts y by the products of a whole k range, far beyond the element-wise
 bound used here (the bound of the prefill tile tests: bf16 output rounding
@@ -64,11 +65,13 @@ def wide():
 
 
 @pytest.mark.parametrize("M,d_out,d_in,per_row", [
-    (2048, 256 * 40, 256, True),    # 160 tiles: whole tiles, then 84 split over the pairs
+    (2048, 256 * 40, 256, True),    # 160 tiles on 76 pairs: a round of whole tiles, then
+                                    # 84 split in four token-tile groups
     (2000, 256 * 40, 256, False),   # ragged last token tile of every row tile
-    (1100, 9990, 1024, True),       # 120 tiles, all split; 76-token last tiles (one MMA),
-                                    # last row tile partly past d_out
-    (1536, 256 * 53, 384, True),    # 159 tiles
+    (1100, 6902, 1024, True),       # 81 tiles, all split in one group (3 token tiles);
+                                    # 76-token last tiles (one MMA), last row tile partly
+                                    # past d_out
+    (1536, 256 * 53, 384, True),    # 159 tiles: two rounds, then 83 split
 ])
 def test_split_elementwise(M, d_out, d_in, per_row, wide):
     wb, packed, alpha = _layer(31, d_out, d_in, per_row)
@@ -87,7 +90,7 @@ def test_split_deterministic_and_reusable(wide):
     x = synth.activations(32, M, d_in)
     ws = _workspace(M, d_out, d_in)
     a = _run(x, wb, packed, alpha, True, ws)
-    wb2, packed2, alpha2 = _layer(33, 9990, 1024, True)
+    wb2, packed2, alpha2 = _layer(33, 6902, 1024, True)
     x2 = synth.activations(33, 1100, 1024)
     _run(x2, wb2, packed2, alpha2, True, ws)
     b = _run(x, wb, packed, alpha, True, ws)
