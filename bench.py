@@ -1340,6 +1340,18 @@ def run_profile(kind: str, prefill_tile: str = "auto"):
         y = torch.empty((2048, 8192), dtype=torch.bfloat16, device="cuda")
         for _ in range(4):
             bd.bitdelta_linear(x, wb, p, a, per_row=True, out=y)
+    elif kind == "prefill_split":
+        # the QKV projection (8192 -> 10240), whose last round of 512-token
+        # tiles is small: through bitdelta_linear_ws, split over the pairs
+        wb, wf = sd.layer(3, 10240, 8192, stream=0)
+        p, a = bd.bitdelta_compress(wb, wf, per_row=True)
+        del wf
+        x = sd.normal_bf16((2048, 8192), 3, 5000)
+        y = torch.empty((2048, 10240), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(bd.bitdelta_linear_workspace_bytes(2048, 10240, 8192),
+                         dtype=torch.uint8, device="cuda")
+        for _ in range(4):
+            bd.bitdelta_linear_ws(x, wb, p, a, ws, per_row=True, out=y)
     elif kind == "grouped":
         grp = Grouped(bd)
         for i in range(4):
@@ -1397,8 +1409,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the per-workload oracle samples (cpu_baseline of each workload)")
     ap.add_argument("--profile", default=None,
-                    help="decode|decode16|compress|reconstruct|prefill|grouped|slice_decode|"
-                         "kmerge|monosoup: a few eager launches for ncu")
+                    help="decode|decode16|compress|reconstruct|prefill|prefill_split|grouped|"
+                         "slice_decode|kmerge|monosoup: a few eager launches for ncu")
     ap.add_argument("--prefill-tile", default="auto", choices=["auto", "256", "512"],
                     help="token width of the tensor-core kernel's pair tiles (profile runs)")
     args = ap.parse_args()
