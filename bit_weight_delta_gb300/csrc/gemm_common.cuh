@@ -107,17 +107,19 @@ __device__ __forceinline__ uint32_t pair_flip_mask(uint32_t nb) {
   return (nb * (0x40008000u >> (2 * J))) & 0x80008000u;
 }
 
-// bf16x2_rne(fp32(w.lo) + a, fp32(w.hi) + a), one packed fp32x2 add.
+// bf16x2_rne(fp32(w.lo) + a, fp32(w.hi) + a): two mixed-precision adds (the
+// bf16 operand widened exactly to fp32 inside the add, one fp32 rounding)
+// and one packing conversion, with no shifts to unpack the halves.
 __device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t w, uint32_t a) {
-  uint32_t lo, hi;
-  asm("{\n\t.reg .b64 x, y, d;\n\t"
-      "mov.b64 x, {%2, %3};\n\t"
-      "mov.b64 y, {%4, %4};\n\t"
-      "add.rn.f32x2 d, x, y;\n\t"
-      "mov.b64 {%0, %1}, d;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w << 16), "r"(w & 0xFFFF0000u), "r"(a));
-  return pack_bf16x2_rn(__uint_as_float(lo), __uint_as_float(hi));
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 fl, fh;\n\t"
+      "mov.b32 {l, h}, %1;\n\t"
+      "add.rn.f32.bf16 fl, l, %2;\n\t"
+      "add.rn.f32.bf16 fh, h, %2;\n\t"
+      "cvt.rn.bf16x2.f32 %0, fh, fl;\n\t}"
+      : "=r"(r)
+      : "r"(w), "f"(__uint_as_float(a)));
+  return r;
 }
 
 // W_eff of one row's 8·C columns held as C 16-byte chunks of bf16 W_base:

@@ -120,7 +120,9 @@ struct Misc {
   int64_t t_total;  // token tiles over all segments
 };
 
-template <bool kWide>
+// kGrouped: the multi-tenant call (segment table, per-tile variant); the
+// single-variant instance drops its per-stage variant and alignment cases.
+template <bool kWide, bool kGrouped>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bitdelta_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                               const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
@@ -146,7 +148,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool grouped = p.seg_off != nullptr;
+  constexpr bool grouped = kGrouped;
   const uint32_t rank = cluster_rank();
 
   // ---------------------------------------------------------------- set-up
@@ -303,8 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pf_src = pk + row * row_bytes;
         pf_mode = 1;
       } else {
+        // a variant table entry off its boundary (the single-variant call's
+        // pointer is checked on the host): recorded, and read as +1 signs
         if (blockIdx.x == 0) record_error(p.ctx, kErrBounds);
-        pf_mode = 2;
+        pf_mode = kGrouped ? 2 : 0;
       }
     };
     auto cur_set = [&](Cur& c, const Item& im, int over, bool is_pf) {
@@ -346,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           cp_async_8(dst, pf_src + pf.kb * C::kSignBytes);
         else
           cp_async_4(dst, pf_src + pf.kb * C::kSignBytes);
-      } else if (pf_mode == 2) {
+      } else if (kGrouped && pf_mode == 2) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
       }
       if (pf_mode != 0 && pf.kb < pf.kb0g) cp_async_4(alpha_ring + pf_slot * kBM + r, pf_alpha);
@@ -372,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      const bool has_delta = cu.var > 0;
+      const bool has_delta = !kGrouped || cu.var > 0;
       if (cu.kb < cu.kb0g && has_delta) alpha_bits = __float_as_uint(alpha_ring[slot * kBM + r]);
       uint2 sg = make_uint2(0u, 0u);
       if (has_delta) {
@@ -630,7 +634,10 @@ cudaError_t pair_capacity(int* pairs) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(host_cache_mutex());
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel<kWide>,
+    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel<kWide, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kWide>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bitdelta_gemm_pair_kernel<kWide, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kWide>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -638,7 +645,7 @@ cudaError_t pair_capacity(int* pairs) {
     cfg.dynamicSmemBytes = Cfg<kWide>::kSmemBytes;
     cfg.gridDim = dim3(2);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, bitdelta_gemm_pair_kernel<kWide>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, bitdelta_gemm_pair_kernel<kWide, false>, &cfg);
     if (e != cudaSuccess) return e;
     max_pairs[dev] = n;
     done[dev] = true;
@@ -661,7 +668,9 @@ cudaError_t launch_pair_instance(const GemmArgs& p, const CUtensorMap& tmap_w,
   cfg.stream = stream;
   const int64_t pairs = pair_tiles_bound < max_pairs ? pair_tiles_bound : max_pairs;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (pairs > 0 ? pairs : 1)));
-  return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel<kWide>, tmap_w, tmap_x, p);
+  if (p.seg_off != nullptr)
+    return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel<kWide, true>, tmap_w, tmap_x, p);
+  return cudaLaunchKernelEx(&cfg, bitdelta_gemm_pair_kernel<kWide, false>, tmap_w, tmap_x, p);
 }
 
 }  // namespace
