@@ -26,13 +26,21 @@
 // per stage (tok0 + 128r and tok0 + 256 + 128r); eight 24 KB stages of
 // 32 K (64-byte swizzle).
 //
-// Warp roles per CTA (448 threads, one CTA per SM, persistent over tiles):
+// Work of a pair: a list of items, each a tile and a range of its k-blocks:
+// whole tiles of the call's flat tile order (pair p takes tiles p, p + n_pairs,
+// ...), then, in the split schedule, the k-block range of a split region
+// that falls to the pair (a tile there is shared by at most two pairs, whose
+// fp32 partials the later of the two adds up).  Every role walks the same
+// list.
+//
+// Warp roles per CTA (448 threads, one CTA per SM, persistent over items):
 //   warps 0-7   transform: two warpgroups take the stages in turn; thread i
-//               of a warpgroup owns W row i (TMEM lane i), forms 64 W_eff
-//               values per stage and stores them to the stage's A slot
-//               (tcgen05.st, narrow) or back to shared memory (wide), then
-//               its warp arrives on rank 0's xform barrier.
-//   warps 8-11  epilogue: tcgen05.ld this CTA's accumulator, store bf16 y.
+//               of a warpgroup owns W row i (TMEM lane i), forms the stage's
+//               W_eff values of its row and stores them to the stage's A
+//               slot (tcgen05.st, narrow) or back to shared memory (wide),
+//               then its warp arrives on rank 0's xform barrier.
+//   warps 8-11  epilogue: tcgen05.ld this CTA's accumulator, store bf16 y
+//               (or a split tile's fp32 partial, or the pair sum).
 //   warp 12     TMA producer for this CTA's W_base rows and its x rows.
 //   warp 13     rank 0: MMA issuer; rank 1: waits for the pair's last MMA.
 // Barriers: full[s] (TMA -> transform, local), xform[s] (both CTAs'
