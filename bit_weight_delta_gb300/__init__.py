@@ -33,6 +33,7 @@ EXPORTED = (
     "bitdelta_reconstruct", "bitdelta_linear", "bitdelta_linear_ws",
     "bitdelta_linear_workspace_bytes", "bitdelta_linear_grouped",
     "bitdelta_check_error", "bitdelta_set_wait_limit_ns", "bitdelta_debug_wait_timeout",
+    "bitdelta_debug_split_schedule",
     "bitdelta_set_prefill_tile",
     "bitdelta_status_string", "bitdelta_compress_noalloc", "bitdelta_sign_similarity",
     "bitdelta_sign_similarity_workspace_bytes", "bitdelta_monosoup",
@@ -100,6 +101,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.bitdelta_set_prefill_tile.restype = st
     lib.bitdelta_debug_wait_timeout.argtypes = [p]
     lib.bitdelta_debug_wait_timeout.restype = st
+    lib.bitdelta_debug_split_schedule.argtypes = [i64, i64, i64, i64, i64, p, i64,
+                                                  ctypes.POINTER(i64)]
+    lib.bitdelta_debug_split_schedule.restype = st
     lib.bitdelta_status_string.argtypes = [st]
     lib.bitdelta_status_string.restype = ctypes.c_char_p
     lib.bitdelta_sign_similarity_workspace_bytes.argtypes = [i64, i32]

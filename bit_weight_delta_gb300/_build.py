@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(HERE, "libbitdelta.so")
 
 SOURCES = ["abi.cu", "compress.cu", "reconstruct.cu", "gemv.cu", "gemm_pair.cu", "cache.cu",
            "kmerge.cu", "similarity.cu", "monosoup.cu"]
-HEADERS = ["common.cuh", "kernels.h", "gemm_common.cuh"]
+HEADERS = ["common.cuh", "kernels.h", "gemm_common.cuh", "split_schedule.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "-I", CSRC]

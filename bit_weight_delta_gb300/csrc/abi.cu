@@ -12,6 +12,7 @@
 
 #include "bitdelta.h"
 #include "kernels.h"
+#include "split_schedule.h"
 
 namespace {
 
@@ -589,6 +590,39 @@ bd_status bitdelta_debug_wait_timeout(bd_stream_t stream) {
   if (st != BD_OK) return st;
   return from_cuda(
       bd::launch_wait_timeout_probe(make_ctx(dev), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bd_status bitdelta_debug_split_schedule(int64_t n_pairs, int64_t t_total, int64_t sk_lo,
+                                        int64_t sk_tiles, int64_t n_kb, int64_t* out,
+                                        int64_t out_len, int64_t* n_records) {
+  if (n_pairs <= 0 || t_total <= 0 || sk_lo < 0 || n_kb <= 0 || n_kb > INT32_MAX ||
+      sk_tiles < n_pairs || n_records == nullptr || out_len < 0 || (out_len > 0 && !out))
+    return BD_ERR_INVALID_ARG;
+  int64_t n = 0;
+  for (int64_t pair = 0; pair < n_pairs; ++pair) {
+    const bd::SplitPair sp = bd::split_pair(pair, n_pairs, t_total, sk_lo, sk_tiles, n_kb);
+    for (int64_t k = 0; k < sp.n_items; ++k, ++n) {
+      if (n >= out_len) continue;
+      const bd::SplitItem it = bd::split_item(sp, k, sk_lo, n_kb);
+      int64_t* r = out + 10 * n;
+      r[0] = pair;
+      r[1] = it.tile;
+      r[2] = it.kb0;
+      r[3] = it.kb1;
+      r[4] = it.j;
+      r[5] = it.partial ? 1 : 0;
+      r[6] = r[7] = r[8] = r[9] = -1;
+      if (it.partial) {
+        const bd::SplitShare sh = bd::split_share(sp, it.su, n_kb);
+        r[6] = sh.pair_lo;
+        r[7] = sh.pair_hi;
+        r[8] = sh.j_lo;
+        r[9] = sh.counter;
+      }
+    }
+  }
+  *n_records = n;
+  return BD_OK;
 }
 
 const char* bitdelta_status_string(bd_status status) {

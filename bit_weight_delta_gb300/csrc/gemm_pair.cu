@@ -50,6 +50,7 @@
 #include <cstdint>
 
 #include "gemm_common.cuh"
+#include "split_schedule.h"
 
 namespace bd {
 namespace {
@@ -210,17 +211,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return tile_at<kPairM, kBN>(p, t_lo + pair_id + i * n_pairs, t_total, seg_off_tbl, s_seg_var,
                                 s_prefix);
   };
-  // Split region.  When it is whole row tiles and the token tiles of a row
-  // tile divide the pairs, it splits into sk_g = t_total groups, one per
-  // token tile, of n_pairs / sk_g pairs each; else into one group.  Group g
-  // holds the region's tiles of token tile g (local tile u is flat tile
-  // sk_lo + u * sk_g + g), and its k-blocks, tile after tile, sk_w in all,
-  // are cut into one contiguous range per pair of the group: [sk_a, sk_b)
-  // for the pair of index g_idx.  The pairs of equal g_idx cover the same
-  // row tiles at the same k-blocks at about the same time, so each W_base
-  // block they read is read from memory once, as in the rounds of whole
-  // tiles.  A pair's work is a list of items (a tile and a k-block range of
-  // it): its whole tiles, then the group's tiles its range meets.
+  // Split region (split_schedule.h): this pair's k-block range of its
+  // group's tiles, after its whole tiles.  A pair's work is a list of items
+  // (a tile and a k-block range of it): its whole tiles, then the split
+  // tiles its range meets.
   int64_t sk_tiles =
       split ? (p.sk_tiles < all_tiles - p.sk_lo ? p.sk_tiles : all_tiles - p.sk_lo) : 0;
   if (sk_tiles > 0 && sk_tiles < n_pairs) {
@@ -229,18 +223,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.ctx, kErrBounds);
     sk_tiles = 0;
   }
-  const int64_t sk_g = sk_tiles > 0 && n_pairs % t_total == 0 && p.sk_lo % t_total == 0 &&
-                               sk_tiles % t_total == 0
-                           ? t_total
-                           : 1;
-  const int64_t g_pairs = n_pairs / sk_g;
-  const int64_t g_id = pair_id % sk_g;
-  const int64_t g_idx = pair_id / sk_g;
-  const int64_t sk_w = sk_tiles / sk_g * n_kb;
-  const int64_t sk_a = g_idx * sk_w / g_pairs;
-  const int64_t sk_b = (g_idx + 1) * sk_w / g_pairs;
-  const int64_t sk_first = sk_a / n_kb;
-  const int64_t n_items = my_tiles + (sk_b > sk_a ? (sk_b - 1) / n_kb - sk_first + 1 : 0);
+  const SplitPair sp = split_pair(pair_id, n_pairs, t_total, p.sk_lo, sk_tiles, n_kb);
+  const int64_t n_items = my_tiles + sp.n_items;
   struct Item {
     Tile t;
     int kb0, kb1;  // k-blocks [kb0, kb1) of the tile
@@ -257,14 +241,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       im.j = 0;
       return im;
     }
-    const int64_t su = sk_first + (it - my_tiles);
-    const int64_t base = su * n_kb;
-    im.t = tile_at<kPairM, kBN>(p, p.sk_lo + su * sk_g + g_id, t_total, nullptr, nullptr,
-                                nullptr);
-    im.kb0 = static_cast<int>((sk_a > base ? sk_a : base) - base);
-    im.kb1 = static_cast<int>((sk_b < base + n_kb ? sk_b : base + n_kb) - base);
-    im.su = su;
-    im.j = it == my_tiles ? 0 : 1;
+    const SplitItem si = split_item(sp, it - my_tiles, p.sk_lo, n_kb);
+    im.t = tile_at<kPairM, kBN>(p, si.tile, t_total, nullptr, nullptr, nullptr);
+    im.kb0 = si.kb0;
+    im.kb1 = si.kb1;
+    im.su = si.su;
+    im.j = si.j;
     return im;
   };
   const int64_t row0 = static_cast<int64_t>(rank) * kBM;     // this CTA's rows in the tile
@@ -475,25 +457,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         continue;
       }
       // A part of a split tile, shared with one other pair of the group
-      // (each pair's range spans more than one tile): the group's pairs of
-      // index q_lo and q_hi, whose ranges meet k-blocks x0 .. x1 (the largest
-      // index q with q * sk_w / g_pairs <= x is ((x + 1) * g_pairs - 1) /
-      // sk_w).  q_hi's part is in its slot 0 (its range starts in the tile),
-      // q_lo's in its slot 1 unless the tile also holds the start of q_lo's
-      // range.  One counter per tile, CTA half and epilogue warp counts the
-      // parts stored.
+      // (split_share: the two contributors in k order and their slots).  One
+      // counter per tile, CTA half and epilogue warp counts the parts stored.
       const int64_t span = im.t.tok_end - im.t.tok0;
       const int cols = span <= 0 ? 0 : (span < kBN ? static_cast<int>(span) : kBN);
       constexpr int64_t kSlot = static_cast<int64_t>(kBN) * kBM;
-      const int64_t x0 = im.su * n_kb, x1 = x0 + n_kb - 1;
-      const int64_t q_lo = ((x0 + 1) * g_pairs - 1) / sk_w;
-      const int64_t q_hi0 = ((x1 + 1) * g_pairs - 1) / sk_w;
-      const int64_t q_hi = q_hi0 < g_pairs - 1 ? q_hi0 : g_pairs - 1;
-      const int j_lo = (q_lo * sk_w / g_pairs) / n_kb == im.su ? 0 : 1;
-      const int64_t pair_lo = q_lo * sk_g + g_id, pair_hi = q_hi * sk_g + g_id;
-      const float* slot_lo = p.sk_part + ((pair_lo * 2 + j_lo) * 2 + rank) * kSlot;
-      const float* slot_hi = p.sk_part + ((pair_hi * 2 + 0) * 2 + rank) * kSlot;
-      unsigned int* cnt = p.sk_count + ((im.su * sk_g + g_id) * 2 + rank) * 4 + quarter;
+      const SplitShare sh = split_share(sp, im.su, n_kb);
+      const int64_t pair_lo = sh.pair_lo;
+      const float* slot_lo = p.sk_part + ((sh.pair_lo * 2 + sh.j_lo) * 2 + rank) * kSlot;
+      const float* slot_hi = p.sk_part + ((sh.pair_hi * 2 + 0) * 2 + rank) * kSlot;
+      unsigned int* cnt = p.sk_count + (sh.counter * 2 + rank) * 4 + quarter;
       int other_done = 0;
       if (lane == 0) other_done = ld_acquire_u32(cnt) != 0u ? 1 : 0;
       other_done = __shfl_sync(0xFFFFFFFFu, other_done, 0);

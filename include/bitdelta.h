@@ -312,6 +312,22 @@ bd_status bitdelta_set_prefill_tile(bd_prefill_tile tile);
  * BD_ERR_DEVICE_TIMEOUT in the error word and the kernel returns normally. */
 bd_status bitdelta_debug_wait_timeout(bd_stream_t stream);
 
+/* Test hook (host only, no device needed): the split schedule of
+ * bitdelta_linear_ws as the tensor-core kernel computes it, for a launch of
+ * n_pairs CTA pairs over a split region of sk_tiles tiles starting at flat
+ * tile sk_lo, t_total token tiles per row tile and n_kb k-blocks per tile
+ * (sk_tiles >= n_pairs).  Writes one record of 10 int64 per split item of
+ * every pair, pairs in order: pair, flat tile, kb0, kb1 (the item's k-blocks
+ * [kb0, kb1)), partial slot j, shared (1 if the tile is shared with another
+ * pair), and for a shared tile its first contributor, its second, the first
+ * one's slot and the tile's counter index (else -1).  *n_records receives the
+ * number of records; out_len (records) bounds what is written.
+ * BD_ERR_INVALID_ARG for a non-positive size, sk_tiles < n_pairs or a NULL
+ * n_records. */
+bd_status bitdelta_debug_split_schedule(int64_t n_pairs, int64_t t_total, int64_t sk_lo,
+                                        int64_t sk_tiles, int64_t n_kb, int64_t* out,
+                                        int64_t out_len, int64_t* n_records);
+
 /* Static string for a status code. */
 const char* bitdelta_status_string(bd_status status);
 
